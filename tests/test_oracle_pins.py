@@ -1,0 +1,35 @@
+"""The oracle against its pins (CPU only), and the pins against planted mistakes."""
+
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as P
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(orc, pin):
+    fails = pin(orc)
+    assert not fails, fails
+
+
+# Each planted mistake (oracle.c, ORACLE_MUTANT) must make at least one pin fail.
+MUTANTS = {
+    1: "rotation by the negative angle",
+    2: "interleaved pairs instead of half-split",
+    3: "global token index as the position",
+    4: "exclusive window |i-j| < w",
+    5: "scale dropped",
+    6: "log base 2 in the lse",
+    7: "keys used as values",
+    8: "key range one short at the window's far edge",
+    9: "key range one too wide at the window's near edge",
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=lambda m: MUTANTS[m])
+def test_pins_catch_planted_mistake(tmp_path, mutant):
+    path = oracle.compile_oracle(str(tmp_path / f"liboracle_m{mutant}.so"), mutant=mutant)
+    bad = oracle.Oracle(path)
+    assert P.all_failures(bad), f"no pin fails for mutant {mutant}: {MUTANTS[mutant]}"
