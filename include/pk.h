@@ -1,0 +1,145 @@
+/*
+ * pk.h -- packed-sequence RoPE attention, forward pass, on one GB300 (sm_103a).
+ *
+ * The operation (hanzo-kernel 0.2.42 packed.rs, module doc and fn attend / fn attend_ref):
+ * attention over packed variable-length sequences straight from a packed QKV projection,
+ * with the rotary embedding applied to q and k inside the kernel and each query reading
+ * only its own sequence's keys, optionally within a symmetric window.
+ *
+ *   qkv  [T, 3*H*64]  row t holds token t's q (columns h*64 .. h*64+63 for head h), then
+ *                     its k (columns H*64 + h*64 ..), then its v (columns 2*H*64 + h*64 ..).
+ *   cos, sin [P, 32]  rotary tables indexed by position within a sequence, same element
+ *                     type as qkv; P must be at least the longest sequence (not checked:
+ *                     P is not an argument).
+ *   cu   [S+1]        uint32 first token of each sequence: cu[0] = 0, non-decreasing,
+ *                     cu[S] = T. Empty sequences are allowed.
+ *   out  [T, H*64]    out[t, h*64 + d], same element type as qkv.
+ *   lse  [H, T]       float32, natural-log log-sum-exp of each row's scaled scores.
+ *
+ * For token t = cu[s] + i of sequence s (length L = cu[s+1] - cu[s]) and head h:
+ *   q' = rot(q_t, i) * scale,  k'_j = rot(k_{cu[s]+j}, j)  with the half-split rotation
+ *        rot(x, p)[u] = x[u] cos[p,u] - x[u+32] sin[p,u],
+ *        rot(x, p)[u+32] = x[u] sin[p,u] + x[u+32] cos[p,u]       (u < 32)
+ *   score_j = q' . k'_j for keys j < L with window == 0 or |i - j| <= window
+ *   lse = m + ln(sum_j exp(score_j - m)), out = sum_j exp(score_j - lse) v_{cu[s]+j}.
+ * `window` = 0 lets every key of the sequence through (the pages' "0: every key").
+ *
+ * Precision: bf16 and fp16 inputs are multiplied on the tensor cores (tcgen05, fp32
+ * accumulation) after rotation in fp32; the probabilities are rounded to the input type
+ * before the product with v. fp32 inputs are computed in fp32 on the CUDA cores.
+ *
+ * Conventions for every entry point below:
+ *   - All array pointers are DEVICE pointers of the current CUDA device; the caller owns
+ *     them and the stream. Calls are asynchronous on `stream` (0 = the legacy stream).
+ *   - qkv, cos, sin and out must be 16-byte aligned; cu and lse 4-byte aligned.
+ *   - The library keeps, per (device, stream), a small workspace it allocates on first use
+ *     and grows when a larger T arrives (tile records and a control word); pk_release()
+ *     frees all of them. Calls on one stream are ordered; calls on different streams use
+ *     different workspaces.
+ *   - Return value: PK_OK, or an error code below. Errors found on the host (arguments,
+ *     alignment, launch) are returned at once and nothing is launched. Errors found by
+ *     the device (a malformed cu, a wait that ran out of time) are recorded in the
+ *     stream's status word, read by pk_last_status(). The kernels never trap.
+ */
+#ifndef PK_H
+#define PK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t */
+
+enum pk_status {
+    PK_OK = 0,
+    PK_ERR_ARG = 1,          /* null pointer with T > 0, S < 0, T < 0, H < 1, window < 0,
+                                T or H beyond the limits, cu inconsistent with S and T */
+    PK_ERR_ALIGN = 2,        /* a pointer is not aligned as required */
+    PK_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed */
+    PK_ERR_UNSUPPORTED = 4,  /* the current device is not sm_103 (GB300) */
+    PK_ERR_BAD_CU = 5,       /* device: cu[0] != 0, cu decreasing, or cu[S] != T */
+    PK_ERR_TIMEOUT = 6,      /* device: a pipeline wait exceeded its bound; results invalid */
+    PK_ERR_NOMEM = 7,        /* workspace allocation failed */
+    PK_ERR_INTERNAL = 8      /* device: schedule exceeded its capacity (a library bug) */
+};
+
+enum pk_dtype { PK_F32 = 0, PK_BF16 = 1, PK_F16 = 2 };
+
+/* Limits: T <= PK_MAX_T, H <= PK_MAX_H. */
+#define PK_MAX_T 2147483647LL
+#define PK_MAX_H 1024
+
+/*
+ * Forward pass, bf16 qkv / cos / sin / out (the parameter list of the method's entry
+ * point: pk_attend(qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream)).
+ */
+int pk_attend(const void *qkv, const void *cos, const void *sin, const uint32_t *cu, int S,
+              int64_t T, int H, int window, float scale, void *out, float *lse,
+              struct CUstream_st *stream);
+
+/* The same for an explicit element type: bf16, fp16, fp32. */
+int pk_attend_bf16(const void *qkv, const void *cos, const void *sin, const uint32_t *cu, int S,
+                   int64_t T, int H, int window, float scale, void *out, float *lse,
+                   struct CUstream_st *stream);
+int pk_attend_f16(const void *qkv, const void *cos, const void *sin, const uint32_t *cu, int S,
+                  int64_t T, int H, int window, float scale, void *out, float *lse,
+                  struct CUstream_st *stream);
+int pk_attend_f32(const void *qkv, const void *cos, const void *sin, const uint32_t *cu, int S,
+                  int64_t T, int H, int window, float scale, void *out, float *lse,
+                  struct CUstream_st *stream);
+
+/* The same with the element type as an argument (enum pk_dtype). */
+int pk_attend_dt(int dtype, const void *qkv, const void *cos, const void *sin,
+                 const uint32_t *cu, int S, int64_t T, int H, int window, float scale, void *out,
+                 float *lse, struct CUstream_st *stream);
+
+/*
+ * The tile schedule alone (for inspection and tests). Runs the device scheduler on `cu`
+ * (device pointer) and copies its records to `tiles` (device pointer, room for `cap`
+ * records of 8 uint32 each: q0, rows, k0, nk, seq, nseq, kind, ktiles -- query tokens
+ * [q0, q0+rows), key tokens [k0, k0+nk), member sequences [seq, seq+nseq), kind 0 for a
+ * 128-row piece of one sequence and 1 for a group of short sequences, ktiles =
+ * ceil(nk/128)). Synchronizes `stream` and writes the record count to *nt (host pointer).
+ * Returns PK_ERR_BAD_CU for a malformed cu (then *nt = 0), PK_ERR_ARG when cap is too small.
+ * The rule (packed.rs fn layout for sequences longer than 64 tokens; grouping of short
+ * sequences by the 64-token granule their first token falls in) is stated in full in the
+ * oracle that checks it.
+ */
+int pk_schedule(const uint32_t *cu, int S, int64_t T, int window, uint32_t *tiles, int64_t cap,
+                int64_t *nt, struct CUstream_st *stream);
+
+/* Records pk_schedule can write for T tokens: enough room for `tiles`. */
+int64_t pk_schedule_capacity(int64_t T);
+
+/*
+ * Synchronizes `stream`, returns the first device-detected error recorded for it since
+ * the last call (PK_OK if none) and clears it.
+ */
+int pk_last_status(struct CUstream_st *stream);
+
+/*
+ * Kernel timing. pk_profile_start(n) makes the next n attention calls on the current device
+ * record a CUDA event pair on their stream around each of their two kernels (the tile
+ * scheduler and the attention kernel). pk_profile_stop() synchronizes those events, writes
+ * the summed durations in milliseconds and the number of calls recorded, and stops the
+ * recording. Returns PK_ERR_ARG for n < 1 or null outputs, PK_ERR_CUDA on event failures.
+ */
+int pk_profile_start(int n);
+int pk_profile_stop(double *schedule_ms, double *attend_ms, int *calls);
+
+/* Text of a status code (static storage). */
+const char *pk_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int pk_version(void);
+
+/* Frees every workspace (synchronizing the streams that own them). */
+int pk_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PK_H */

@@ -1,0 +1,190 @@
+"""Python binding of libpk: packed-sequence RoPE attention forward on GB300.
+
+Argument marshalling only: every step of the computation runs in the CUDA library
+(`libpk.so`, built from `csrc/` by `build.py`); there is no fallback of any kind. If the
+library is missing or cannot load, every call raises.
+
+The entry points mirror include/pk.h:
+    attend(qkv, cos, sin, cu, H, window, scale, out=None, lse=None, stream=None)
+    pk_attend(qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream)   (raw pointers)
+    schedule(cu, T, window)      -> tile records [NT, 8]
+    last_status(stream=None)     -> int
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpk.so")
+
+PK_F32, PK_BF16, PK_F16 = 0, 1, 2
+STATUS = {
+    0: "PK_OK", 1: "PK_ERR_ARG", 2: "PK_ERR_ALIGN", 3: "PK_ERR_CUDA", 4: "PK_ERR_UNSUPPORTED",
+    5: "PK_ERR_BAD_CU", 6: "PK_ERR_TIMEOUT", 7: "PK_ERR_NOMEM", 8: "PK_ERR_INTERNAL",
+}
+
+# names declared in include/pk.h
+EXPORTS = ("pk_attend", "pk_attend_bf16", "pk_attend_f16", "pk_attend_f32", "pk_attend_dt",
+           "pk_schedule", "pk_schedule_capacity", "pk_last_status", "pk_status_string",
+           "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop")
+
+_lib = None
+
+
+class PKError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        msg = f"{STATUS.get(code, code)}: {status_string(code) if _lib else ''}"
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+def load(path: str | None = None):
+    """Load libpk.so (raises if it is missing: there is no other implementation)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libpk.so not built ({p}); run __graft_entry__.build()")
+    L = ctypes.CDLL(p)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    sig = [vp, vp, vp, vp, i32, i64, i32, i32, f32, vp, vp, vp]
+    for name in ("pk_attend", "pk_attend_bf16", "pk_attend_f16", "pk_attend_f32"):
+        getattr(L, name).argtypes = sig
+        getattr(L, name).restype = i32
+    L.pk_attend_dt.argtypes = [i32] + sig
+    L.pk_attend_dt.restype = i32
+    L.pk_schedule.argtypes = [vp, i32, i64, i32, vp, i64, ctypes.POINTER(i64), vp]
+    L.pk_schedule.restype = i32
+    L.pk_schedule_capacity.argtypes = [i64]
+    L.pk_schedule_capacity.restype = i64
+    L.pk_last_status.argtypes = [vp]
+    L.pk_last_status.restype = i32
+    L.pk_status_string.argtypes = [i32]
+    L.pk_status_string.restype = ctypes.c_char_p
+    L.pk_version.argtypes = []
+    L.pk_version.restype = i32
+    L.pk_release.argtypes = []
+    L.pk_release.restype = i32
+    L.pk_profile_start.argtypes = [i32]
+    L.pk_profile_start.restype = i32
+    dp = ctypes.POINTER(ctypes.c_double)
+    L.pk_profile_stop.argtypes = [dp, dp, ctypes.POINTER(i32)]
+    L.pk_profile_stop.restype = i32
+    _lib = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return load().pk_status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise PKError(rc, what)
+
+
+# ------------------------------------------------------------------------------------------
+# raw-pointer entry points (same names and argument order as the C ABI)
+
+
+def pk_attend(qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream) -> int:
+    return load().pk_attend(qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream)
+
+
+def pk_attend_dt(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream) -> int:
+    return load().pk_attend_dt(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream)
+
+
+def pk_schedule(cu, S, T, window, tiles, cap, stream):
+    nt = ctypes.c_int64(0)
+    rc = load().pk_schedule(cu, S, T, window, tiles, cap, ctypes.byref(nt), stream)
+    return rc, nt.value
+
+
+def pk_last_status(stream) -> int:
+    return load().pk_last_status(stream)
+
+
+# ------------------------------------------------------------------------------------------
+# torch-tensor front (torch only allocates and supplies the stream)
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def dtype_code(t) -> int:
+    torch = _torch()
+    m = {torch.float32: PK_F32, torch.bfloat16: PK_BF16, torch.float16: PK_F16}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=None, stream=None):
+    """out [T, H*64] (qkv's dtype) and lse [H, T] float32 for device tensors qkv [T, 3*H*64],
+    cos/sin [P, 32] (qkv's dtype) and cu [S+1] (int32 or uint32)."""
+    torch = _torch()
+    T = qkv.shape[0]
+    S = cu.shape[0] - 1
+    if qkv.dim() != 2 or qkv.shape[1] != 3 * H * 64:
+        raise ValueError("qkv must be [T, 3*H*64]")
+    if cos.dtype != qkv.dtype or sin.dtype != qkv.dtype:
+        raise TypeError("cos/sin must have qkv's dtype")
+    if cu.dtype not in (torch.int32, torch.uint32):
+        raise TypeError("cu must be int32 or uint32")
+    for t in (qkv, cos, sin, cu):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if out is None:
+        out = torch.empty((T, H * 64), dtype=qkv.dtype, device=qkv.device)
+    if lse is None:
+        lse = torch.empty((H, T), dtype=torch.float32, device=qkv.device)
+    rc = pk_attend_dt(dtype_code(qkv), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(),
+                      S, T, H, window, float(scale), out.data_ptr(), lse.data_ptr(),
+                      _stream_handle(stream))
+    _check(rc, "pk_attend")
+    return out, lse
+
+
+def schedule(cu, T: int, window: int, stream=None):
+    """Tile records [NT, 8] (int32 tensor holding the uint32 fields) of the device scheduler."""
+    torch = _torch()
+    cap = int(load().pk_schedule_capacity(T))
+    tiles = torch.zeros((max(cap, 1), 8), dtype=torch.int32, device=cu.device)
+    rc, nt = pk_schedule(cu.data_ptr(), cu.shape[0] - 1, T, window, tiles.data_ptr(), cap,
+                         _stream_handle(stream))
+    _check(rc, "pk_schedule")
+    return tiles[:nt]
+
+
+def last_status(stream=None) -> int:
+    return pk_last_status(_stream_handle(stream))
+
+
+def profile_start(n: int):
+    """Record kernel events around the next n attention calls (see pk_profile_start)."""
+    _check(load().pk_profile_start(int(n)), "pk_profile_start")
+
+
+def profile_stop():
+    """(schedule_ms_total, attend_ms_total, calls) recorded since profile_start."""
+    a, b, n = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_int(0)
+    _check(load().pk_profile_stop(ctypes.byref(a), ctypes.byref(b), ctypes.byref(n)), "pk_profile_stop")
+    return a.value, b.value, n.value
+
+
+def release():
+    _check(load().pk_release(), "pk_release")

@@ -1,0 +1,391 @@
+// pk_host.cu -- the C ABI of include/pk.h: argument checks, the per-(device, stream)
+// workspace, the qkv tensor map, and the two launches of a call (scheduler, then the
+// attention kernel of the element type).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "pk.h"
+#include "pk_dev.cuh"
+
+namespace pk {
+
+cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, TileRec* tiles, long long cap,
+                            Ctl* ctl, cudaStream_t stream);
+cudaError_t attend_tc_prepare();
+cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
+                             const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
+                             long long T, int window, float scale, unsigned long long timeout_ns, int grid,
+                             cudaStream_t stream);
+cudaError_t attend_f32_launch(const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu,
+                              const TileRec* tiles, float* out, float* lse, Ctl* ctl, int H, long long T,
+                              int window, float scale, int grid, cudaStream_t stream);
+
+namespace {
+
+int64_t schedule_capacity(int64_t T) { return 3 * ((T + kGrain - 1) / kGrain) + 1; }
+
+struct Workspace {
+  void* base = nullptr;
+  Ctl* ctl = nullptr;
+  TileRec* tiles = nullptr;
+  int64_t cap = 0;
+};
+
+struct DeviceInfo {
+  bool checked = false;
+  bool supported = false;
+  int sms = 0;
+  bool attrs_set = false;
+};
+
+// kernel timing (pk_profile_start / pk_profile_stop)
+struct Profile {
+  bool on = false;
+  int dev = -1;
+  int cap = 0;
+  int used = 0;
+  cudaEvent_t* ev = nullptr;  // 3 per call: before schedule, before attention, after attention
+};
+
+std::mutex g_mu;
+Profile g_prof;
+std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
+std::map<int, DeviceInfo> g_dev;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+unsigned long long timeout_ns() {
+  static unsigned long long t = 0;
+  if (!t) {
+    const char* e = std::getenv("PK_TIMEOUT_MS");
+    long long ms = e ? std::atoll(e) : 0;
+    t = static_cast<unsigned long long>(ms > 0 ? ms : 2000) * 1000000ull;
+  }
+  return t;
+}
+
+// device checks (caller holds g_mu)
+int device_info(int dev, DeviceInfo** out) {
+  DeviceInfo& di = g_dev[dev];
+  if (!di.checked) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return PK_ERR_CUDA;
+    di.checked = true;
+    di.supported = prop.major == 10 && prop.minor == 3;
+    di.sms = prop.multiProcessorCount;
+  }
+  if (!di.supported) return PK_ERR_UNSUPPORTED;
+  if (!di.attrs_set) {
+    if (attend_tc_prepare() != cudaSuccess) return PK_ERR_CUDA;
+    di.attrs_set = true;
+  }
+  *out = &di;
+  return PK_OK;
+}
+
+// the workspace of (dev, stream) with room for `cap` records (caller holds g_mu)
+int workspace(int dev, cudaStream_t stream, int64_t cap, Workspace** out) {
+  Workspace& ws = g_ws[std::make_pair(dev, stream)];
+  if (ws.base && ws.cap >= cap) {
+    *out = &ws;
+    return PK_OK;
+  }
+  int carried = 0;
+  if (ws.base) {
+    // keep the sticky status across the move
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PK_ERR_CUDA;
+    if (cudaMemcpy(&carried, &ws.ctl->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return PK_ERR_CUDA;
+    cudaFree(ws.base);
+    ws = Workspace();
+  }
+  int64_t want = cap < 4096 ? 4096 : cap;
+  want = want + want / 4;  // headroom against regrowth
+  const size_t bytes = sizeof(Ctl) + static_cast<size_t>(want) * sizeof(TileRec);
+  void* p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_NOMEM;
+  }
+  Ctl init;
+  std::memset(&init, 0, sizeof init);
+  init.status = carried;
+  if (cudaMemcpy(p, &init, sizeof init, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(p);
+    return PK_ERR_CUDA;
+  }
+  ws.base = p;
+  ws.ctl = static_cast<Ctl*>(p);
+  ws.tiles = reinterpret_cast<TileRec*>(static_cast<char*>(p) + sizeof(Ctl));
+  ws.cap = want;
+  *out = &ws;
+  return PK_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_args(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S,
+               int64_t T, int H, int window, const void* out, const float* lse) {
+  if (dtype != PK_F32 && dtype != PK_BF16 && dtype != PK_F16) return PK_ERR_ARG;
+  if (S < 0 || T < 0 || T > PK_MAX_T || H < 1 || H > PK_MAX_H || window < 0) return PK_ERR_ARG;
+  if (S == 0 && T != 0) return PK_ERR_ARG;
+  if (T > 0 && (!qkv || !cos || !sin || !cu || !out || !lse)) return PK_ERR_ARG;
+  if (T > 0 && (!aligned(qkv, 16) || !aligned(cos, 16) || !aligned(sin, 16) || !aligned(out, 16) ||
+                !aligned(cu, 4) || !aligned(lse, 4)))
+    return PK_ERR_ALIGN;
+  return PK_OK;
+}
+
+int launch_schedule(const uint32_t* cu, int S, int64_t T, int window, Workspace* ws, cudaStream_t stream) {
+  return schedule_launch(cu, S, static_cast<long long>(T), window, ws->tiles, static_cast<long long>(ws->cap),
+                         ws->ctl, stream) == cudaSuccess
+             ? PK_OK
+             : PK_ERR_CUDA;
+}
+
+int launch_attend(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int64_t T,
+                  int H, int window, float scale, void* out, float* lse, Workspace* ws, DeviceInfo* di,
+                  cudaStream_t stream);
+
+int attend(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T,
+           int H, int window, float scale, void* out, float* lse, cudaStream_t stream) {
+  int rc = check_args(dtype, qkv, cos, sin, cu, S, T, H, window, out, lse);
+  if (rc != PK_OK || T == 0) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PK_ERR_CUDA;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(dev, &di)) != PK_OK) return rc;
+  Workspace* ws = nullptr;
+  if ((rc = workspace(dev, stream, schedule_capacity(T), &ws)) != PK_OK) return rc;
+  cudaEvent_t* ev = nullptr;
+  if (g_prof.on && g_prof.dev == dev && g_prof.used < g_prof.cap) ev = g_prof.ev + 3 * g_prof.used++;
+  if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return PK_ERR_CUDA;
+  if ((rc = launch_schedule(cu, S, T, window, ws, stream)) != PK_OK) return rc;
+  if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return PK_ERR_CUDA;
+  rc = launch_attend(dtype, qkv, cos, sin, cu, T, H, window, scale, out, lse, ws, di, stream);
+  if (rc == PK_OK && ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return PK_ERR_CUDA;
+  return rc;
+}
+
+int launch_attend(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int64_t T,
+                  int H, int window, float scale, void* out, float* lse, Workspace* ws, DeviceInfo* di,
+                  cudaStream_t stream) {
+  if (dtype == PK_F32) {
+    return attend_f32_launch(static_cast<const float*>(qkv), static_cast<const float*>(cos),
+                             static_cast<const float*>(sin), cu, ws->tiles, static_cast<float*>(out), lse, ws->ctl, H,
+                             static_cast<long long>(T), window, scale, di->sms * 4, stream) == cudaSuccess
+               ? PK_OK
+               : PK_ERR_CUDA;
+  }
+
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PK_ERR_CUDA;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(3) * H * kD, static_cast<cuuint64_t>(T)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(3) * H * kD * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBR)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      dtype == PK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (enc(&tmap, dt, 2, const_cast<void*>(qkv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PK_ERR_CUDA;
+  return attend_tc_launch(dtype == PK_BF16, tmap, cos, sin, cu, ws->tiles, out, lse, ws->ctl, H,
+                          static_cast<long long>(T), window, scale, timeout_ns(), di->sms * 2, stream) == cudaSuccess
+             ? PK_OK
+             : PK_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pk
+
+using namespace pk;
+
+extern "C" {
+
+int pk_attend_dt(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S,
+                 int64_t T, int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
+  return attend(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+}
+
+int pk_attend(const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T, int H,
+              int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
+  return attend(PK_BF16, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+}
+
+int pk_attend_bf16(const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T,
+                   int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
+  return attend(PK_BF16, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+}
+
+int pk_attend_f16(const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T,
+                  int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
+  return attend(PK_F16, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+}
+
+int pk_attend_f32(const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T,
+                  int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
+  return attend(PK_F32, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+}
+
+int64_t pk_schedule_capacity(int64_t T) { return T < 0 ? 0 : schedule_capacity(T); }
+
+int pk_schedule(const uint32_t* cu, int S, int64_t T, int window, uint32_t* tiles, int64_t cap, int64_t* nt,
+                struct CUstream_st* stream) {
+  if (!nt) return PK_ERR_ARG;
+  *nt = 0;
+  if (S < 0 || T < 0 || T > PK_MAX_T || window < 0 || (S == 0 && T != 0)) return PK_ERR_ARG;
+  if (T == 0) return PK_OK;
+  if (!cu || !tiles || !aligned(tiles, 16) || !aligned(cu, 4)) return PK_ERR_ARG;
+  if (cap < schedule_capacity(T)) return PK_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PK_ERR_CUDA;
+  DeviceInfo* di = nullptr;
+  int rc = device_info(dev, &di);
+  if (rc != PK_OK) return rc;
+  Workspace* ws = nullptr;
+  if ((rc = workspace(dev, stream, schedule_capacity(T), &ws)) != PK_OK) return rc;
+  if ((rc = launch_schedule(cu, S, T, window, ws, stream)) != PK_OK) return rc;
+  Ctl ctl;
+  if (cudaMemcpyAsync(&ctl, ws->ctl, sizeof ctl, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return PK_ERR_CUDA;
+  if (ctl.status == PK_ERR_BAD_CU) {
+    int zero = 0;
+    cudaMemcpy(&ws->ctl->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    return PK_ERR_BAD_CU;
+  }
+  if (ctl.ntiles > 0 &&
+      cudaMemcpyAsync(tiles, ws->tiles, static_cast<size_t>(ctl.ntiles) * sizeof(TileRec), cudaMemcpyDeviceToDevice,
+                      stream) != cudaSuccess)
+    return PK_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PK_ERR_CUDA;
+  *nt = ctl.ntiles;
+  return PK_OK;
+}
+
+int pk_last_status(struct CUstream_st* stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PK_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PK_ERR_CUDA;
+  auto it = g_ws.find(std::make_pair(dev, static_cast<cudaStream_t>(stream)));
+  if (it == g_ws.end() || !it->second.base) return PK_OK;
+  int st = 0, zero = 0;
+  if (cudaMemcpy(&st, &it->second.ctl->status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(&it->second.ctl->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return PK_ERR_CUDA;
+  return st;
+}
+
+int pk_profile_start(int n) {
+  if (n < 1) return PK_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PK_ERR_CUDA;
+  if (g_prof.ev) {
+    for (int i = 0; i < 3 * g_prof.cap; ++i) cudaEventDestroy(g_prof.ev[i]);
+    delete[] g_prof.ev;
+  }
+  g_prof = Profile();
+  g_prof.ev = new cudaEvent_t[3 * n];
+  for (int i = 0; i < 3 * n; ++i)
+    if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
+      for (int k = 0; k < i; ++k) cudaEventDestroy(g_prof.ev[k]);
+      delete[] g_prof.ev;
+      g_prof = Profile();
+      return PK_ERR_CUDA;
+    }
+  g_prof.cap = n;
+  g_prof.dev = dev;
+  g_prof.on = true;
+  return PK_OK;
+}
+
+int pk_profile_stop(double* schedule_ms, double* attend_ms, int* calls) {
+  if (!schedule_ms || !attend_ms || !calls) return PK_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  *schedule_ms = 0.0;
+  *attend_ms = 0.0;
+  *calls = 0;
+  int rc = PK_OK;
+  for (int i = 0; i < g_prof.used; ++i) {
+    float a = 0.f, b = 0.f;
+    cudaEvent_t* e = g_prof.ev + 3 * i;
+    if (cudaEventSynchronize(e[2]) != cudaSuccess || cudaEventElapsedTime(&a, e[0], e[1]) != cudaSuccess ||
+        cudaEventElapsedTime(&b, e[1], e[2]) != cudaSuccess) {
+      rc = PK_ERR_CUDA;
+      break;
+    }
+    *schedule_ms += a;
+    *attend_ms += b;
+    ++*calls;
+  }
+  if (g_prof.ev) {
+    for (int i = 0; i < 3 * g_prof.cap; ++i) cudaEventDestroy(g_prof.ev[i]);
+    delete[] g_prof.ev;
+  }
+  g_prof = Profile();
+  return rc;
+}
+
+const char* pk_status_string(int status) {
+  switch (status) {
+    case PK_OK: return "ok";
+    case PK_ERR_ARG: return "invalid argument";
+    case PK_ERR_ALIGN: return "pointer not aligned (qkv, cos, sin, out: 16 bytes; cu, lse: 4 bytes)";
+    case PK_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case PK_ERR_UNSUPPORTED: return "device is not sm_103 (GB300)";
+    case PK_ERR_BAD_CU: return "cu malformed: cu[0] != 0, decreasing, or cu[S] != T";
+    case PK_ERR_TIMEOUT: return "a device wait exceeded its bound; results invalid";
+    case PK_ERR_NOMEM: return "workspace allocation failed";
+    case PK_ERR_INTERNAL: return "schedule capacity exceeded (library bug)";
+    default: return "unknown status";
+  }
+}
+
+int pk_version(void) { return 100; }
+
+int pk_release(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int rc = PK_OK;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_ws) {
+    if (!kv.second.base) continue;
+    cudaSetDevice(kv.first.first);
+    if (cudaStreamSynchronize(kv.first.second) != cudaSuccess) rc = PK_ERR_CUDA;
+    cudaFree(kv.second.base);
+  }
+  g_ws.clear();
+  cudaSetDevice(cur);
+  return rc;
+}
+
+}  // extern "C"

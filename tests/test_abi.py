@@ -1,0 +1,82 @@
+"""The C-ABI library: every symbol include/pk.h declares is exported, and host-side argument
+checks answer without touching a GPU (no compute call runs here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import rope_cu_tile_gb300 as pk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(pk_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rope_cu_tile_gb300 import build
+
+    build.build()
+    return pk.load()
+
+
+def test_header_declares_the_binding_exports():
+    assert set(declared_functions()) == set(pk.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert pk.status_string(code) != "unknown status"
+    assert pk.status_string(99) == "unknown status"
+    assert lib.pk_version() >= 100
+
+
+def test_argument_checks_need_no_gpu(lib):
+    # rejected before any CUDA call: negative sizes, H < 1, null pointers, misalignment
+    p = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1002)
+    null = ctypes.c_void_p(0)
+    args = dict(qkv=p, cos=p, sin=p, cu=p, S=1, T=5, H=2, window=0, scale=0.125, out=p, lse=p, stream=null)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return pk.pk_attend(a["qkv"], a["cos"], a["sin"], a["cu"], a["S"], a["T"], a["H"], a["window"],
+                            a["scale"], a["out"], a["lse"], a["stream"])
+
+    assert call(S=-1) == 1
+    assert call(T=-1) == 1
+    assert call(H=0) == 1
+    assert call(H=100000) == 1
+    assert call(window=-3) == 1
+    assert call(S=0) == 1            # T > 0 with no sequences
+    assert call(qkv=null) == 1
+    assert call(lse=null) == 1
+    assert call(qkv=odd) == 2
+    assert call(out=odd) == 2
+    assert call(T=0, S=0, qkv=null, cos=null, sin=null, cu=null, out=null, lse=null) == 0  # nothing to do
+    assert pk.pk_attend_dt(7, p, p, p, p, 1, 5, 2, 0, 0.125, p, p, null) == 1
+    assert lib.pk_schedule_capacity(0) == 1
+    assert lib.pk_schedule_capacity(64) == 4
+    assert lib.pk_schedule_capacity(65) == 7
+
+
+def test_schedule_capacity_matches_oracle(lib, orc):
+    for T in (0, 1, 63, 64, 65, 131072, 10**9):
+        assert lib.pk_schedule_capacity(T) == orc.schedule_cap(T)

@@ -1,0 +1,100 @@
+"""The five measured configurations at full size, in the launch configuration the benchmark
+times (GPU): sampled rows against the oracle one by one, plus properties of every row.
+
+Properties checked on the whole output (they hold at any size):
+  - every value is finite;
+  - lse of a row is at least the row's own (diagonal) score, scale * q'_i . k'_i;
+  - every output element lies between the smallest and largest value of that dimension over
+    the row's visible keys (out is a convex combination of them), up to the tolerance.
+"""
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import TOL, device_inputs, max_err, run
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_rows(wl, n_random=160, seed=0):
+    """(token, head) pairs: first/last rows of sequences, rows around 128-row tile edges,
+    and random rows."""
+    rng = np.random.default_rng(seed)
+    cu = wl.cu.astype(np.int64)
+    S, T, H = wl.S, wl.T, wl.H
+    toks = []
+    for s in rng.choice(S, size=min(S, 24), replace=False):
+        a, b = cu[s], cu[s + 1]
+        if b > a:
+            toks += [a, b - 1]
+            for e in (127, 128, 129):
+                if a + e < b:
+                    toks.append(a + e)
+    toks += list(rng.integers(0, T, n_random))
+    toks = np.asarray(toks, dtype=np.int64)
+    heads = rng.integers(0, H, toks.shape[0]).astype(np.int32)
+    return toks, heads
+
+
+def rotate(x, cos_rows, sin_rows):
+    z = x[..., :32] + 1j * x[..., 32:]
+    r = z * (cos_rows + 1j * sin_rows)
+    return np.concatenate([r.real, r.imag], axis=-1)
+
+
+def check_properties(wl, out, lse):
+    from scipy.ndimage import maximum_filter1d, minimum_filter1d
+
+    to, tl = TOL[wl.dtype]
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    cu = wl.cu.astype(np.int64)
+    H = wl.H
+    cosf = synth.to_f64(wl.cos, wl.dtype)
+    sinf = synth.to_f64(wl.sin, wl.dtype)
+    worst_lse, worst_hull = 0.0, 0.0
+    for s in range(wl.S):
+        a, b = int(cu[s]), int(cu[s + 1])
+        L = b - a
+        if L == 0:
+            continue
+        rows = synth.to_f64(wl.qkv[a:b], wl.dtype)
+        c, sn = cosf[:L], sinf[:L]
+        for h in range(H):
+            q = rotate(rows[:, h * 64:(h + 1) * 64], c, sn)
+            k = rotate(rows[:, (H + h) * 64:(H + h + 1) * 64], c, sn)
+            diag = wl.scale * np.einsum("ij,ij->i", q, k)
+            worst_lse = max(worst_lse, float(np.max(diag - lse[h, a:b])))
+            v = rows[:, (2 * H + h) * 64:(2 * H + h + 1) * 64]
+            if wl.window == 0 or wl.window >= L - 1:
+                lo, hi = v.min(axis=0)[None, :], v.max(axis=0)[None, :]
+            else:
+                size = 2 * wl.window + 1
+                lo = minimum_filter1d(v, size=size, axis=0, mode="nearest")
+                hi = maximum_filter1d(v, size=size, axis=0, mode="nearest")
+            o = out[a:b, h * 64:(h + 1) * 64]
+            worst_hull = max(worst_hull, float(np.max(lo - o)), float(np.max(o - hi)))
+    assert worst_lse <= tl, f"lse below the diagonal score by {worst_lse:.3e}"
+    assert worst_hull <= to, f"out outside the visible values' range by {worst_hull:.3e}"
+
+
+@pytest.mark.parametrize("name", ["global", "local", "long", "short"])
+def test_config_full_size(pk, orc, name):
+    wl = synth.make_config(name)
+    got_o, got_l = run(pk, wl, inputs=device_inputs(wl))
+    tok, hd = sample_rows(wl)
+    want_o, want_l = orc.attend_rows(wl.qkv, wl.cos, wl.sin, wl.cu, wl.H, wl.window, wl.scale, wl.dtype,
+                                     tok, hd)
+    go = np.stack([got_o[t, h * 64:(h + 1) * 64] for t, h in zip(tok, hd)])
+    gl = np.array([got_l[h, t] for t, h in zip(tok, hd)])
+    to, tl = TOL[wl.dtype]
+    eo, el = max_err(go, want_o), max_err(gl, want_l)
+    assert eo <= to and el <= tl, f"{name}: max|dout| {eo:.3e}, max|dlse| {el:.3e} over {len(tok)} rows"
+    check_properties(wl, got_o, got_l)
+
+
+def test_tiny_full(pk, orc):
+    wl = synth.make_config("tiny")
+    got_o, got_l = run(pk, wl)
+    want_o, want_l = orc.attend(wl.qkv, wl.cos, wl.sin, wl.cu, wl.H, wl.window, wl.scale, wl.dtype)
+    assert max_err(got_o, want_o) <= 1e-4 and max_err(got_l, want_l) <= 1e-4

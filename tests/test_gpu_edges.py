@@ -1,0 +1,136 @@
+"""Edge cases, stray-write canaries, device-detected errors and streams (GPU)."""
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import TOL, device_inputs, max_err, out_to_f64, run, to_device
+
+pytestmark = pytest.mark.gpu
+
+SENT = -12345.0
+
+
+def _padded(torch, T, H, dtype, pad=7):
+    """out and lse views with `pad` extra sentinel-filled rows / entries after them."""
+    out_buf = torch.full(((T + pad) * H * 64,), SENT, dtype=dtype, device="cuda")
+    lse_buf = torch.full((H * T + pad,), SENT, dtype=torch.float32, device="cuda")
+    return out_buf, lse_buf, out_buf[: T * H * 64].view(T, H * 64), lse_buf[: H * T].view(H, T)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_no_stray_writes(pk, orc, dtype):
+    import torch
+
+    wl = synth.make_lens_workload("canary", [3, 130, 64, 1, 70], dtype, H=2, window=0, seed=1)
+    qkv, cos, sin, cu = device_inputs(wl)
+    td = qkv.dtype
+    out_buf, lse_buf, out, lse = _padded(torch, wl.T, wl.H, td)
+    pk.attend(qkv, cos, sin, cu, wl.H, 0, wl.scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert pk.last_status() == 0
+    assert torch.all(out_buf[wl.T * wl.H * 64:] == SENT)
+    assert torch.all(lse_buf[wl.H * wl.T:] == SENT)
+    want_o, want_l = orc.attend(wl.qkv, wl.cos, wl.sin, wl.cu, wl.H, 0, wl.scale, dtype)
+    to, tl = TOL[dtype]
+    assert max_err(out_to_f64(out), want_o) <= to
+    assert max_err(lse.cpu().numpy().astype(np.float64), want_l) <= tl
+
+
+@pytest.mark.parametrize("bad", ["first_not_zero", "decreasing", "last_not_T"])
+def test_malformed_cu_sets_status(pk, bad):
+    import torch
+
+    wl = synth.make_lens_workload("bad", [10, 20, 30], "bf16", H=1, window=0, seed=2)
+    qkv, cos, sin, _ = device_inputs(wl)
+    cu = wl.cu.astype(np.int64).copy()
+    if bad == "first_not_zero":
+        cu[0] = 1
+    elif bad == "decreasing":
+        cu[1], cu[2] = cu[2], cu[1]
+    else:
+        cu[-1] -= 1
+    cu_d = torch.from_numpy(cu.astype(np.int32)).cuda()
+    out_buf, lse_buf, out, lse = _padded(torch, wl.T, wl.H, torch.bfloat16, pad=0)
+    pk.attend(qkv, cos, sin, cu_d, wl.H, 0, wl.scale, out=out, lse=lse)   # returns: error is on the device
+    assert pk.last_status() == 5   # PK_ERR_BAD_CU
+    assert pk.last_status() == 0   # cleared by the read
+    assert torch.all(out_buf == SENT) and torch.all(lse_buf == SENT)   # nothing written
+    with pytest.raises(pk.PKError):
+        pk.schedule(cu_d, wl.T, 0)
+
+
+def test_empty_batch(pk):
+    import torch
+
+    qkv = torch.empty((0, 3 * 64), dtype=torch.bfloat16, device="cuda")
+    cos = torch.zeros((1, 32), dtype=torch.bfloat16, device="cuda")
+    cu = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    out, lse = pk.attend(qkv, cos, cos, cu, 1, 0, 0.125)
+    assert out.shape == (0, 64) and lse.shape == (1, 0)
+    assert pk.last_status() == 0
+
+
+def test_misaligned_pointer_rejected(pk):
+    import torch
+
+    wl = synth.make_lens_workload("align", [8], "bf16", H=1, window=0, seed=0)
+    _, cos, sin, cu = device_inputs(wl)
+    flat = torch.zeros(wl.T * 192 + 1, dtype=torch.bfloat16, device="cuda")
+    qkv = flat[1:].view(wl.T, 192)
+    with pytest.raises(pk.PKError) as e:
+        pk.attend(qkv, cos, sin, cu, 1, 0, 0.125)
+    assert e.value.code == 2
+
+
+def test_side_streams(pk, orc):
+    """Calls on two non-default streams at once each get their own workspace."""
+    import torch
+
+    a = synth.make_lens_workload("sa", [200, 3, 77], "bf16", H=2, window=0, seed=11)
+    b = synth.make_lens_workload("sb", [5, 300, 64, 9], "bf16", H=2, window=16, seed=12)
+    ia, ib = device_inputs(a), device_inputs(b)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    res = []
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            oa = pk.attend(*ia, a.H, a.window, a.scale, stream=s1)
+        with torch.cuda.stream(s2):
+            ob = pk.attend(*ib, b.H, b.window, b.scale, stream=s2)
+        res.append((oa, ob))
+    torch.cuda.synchronize()
+    assert pk.last_status(s1) == 0 and pk.last_status(s2) == 0
+    wa = orc.attend(a.qkv, a.cos, a.sin, a.cu, a.H, a.window, a.scale, "bf16")
+    wb = orc.attend(b.qkv, b.cos, b.sin, b.cu, b.H, b.window, b.scale, "bf16")
+    for (oa, ob) in res:
+        assert max_err(out_to_f64(oa[0]), wa[0]) <= TOL["bf16"][0]
+        assert max_err(out_to_f64(ob[0]), wb[0]) <= TOL["bf16"][0]
+
+
+def test_window_zero_equals_large_window(pk):
+    wl = synth.make_lens_workload("wz", [100, 300, 7], "bf16", H=2, window=0, seed=4)
+    inputs = device_inputs(wl)
+    o0, l0 = run(pk, wl, 0, inputs)
+    o1, l1 = run(pk, wl, 299, inputs)
+    o2, l2 = run(pk, wl, 100000, inputs)
+    # the same keys are visible; the key ranges of windowed pieces are the same here too
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    assert np.array_equal(o0, o2) and np.array_equal(l0, l2)
+
+
+def test_constant_values(pk):
+    """v constant over each sequence's keys gives out = that constant (P rows sum to l)."""
+    wl = synth.make_lens_workload("const", [50, 200, 1, 129], "f16", H=2, window=5, seed=6)
+    qkv = wl.qkv.copy()
+    rng = np.random.default_rng(3)
+    want = np.zeros((wl.T, wl.H * 64))
+    for s in range(wl.S):
+        a, b = int(wl.cu[s]), int(wl.cu[s + 1])
+        for h in range(wl.H):
+            c = rng.standard_normal(64).astype(np.float16)
+            qkv[a:b, (2 * wl.H + h) * 64:(2 * wl.H + h + 1) * 64] = c
+            want[a:b, h * 64:(h + 1) * 64] = c.astype(np.float64)
+    wl.qkv = qkv
+    o, _ = run(pk, wl)
+    assert max_err(o, want) <= TOL["f16"][0]
