@@ -62,7 +62,8 @@ enum pk_status {
     PK_ERR_BAD_CU = 5,       /* device: cu[0] != 0, cu decreasing, or cu[S] != T */
     PK_ERR_TIMEOUT = 6,      /* device: a pipeline wait exceeded its bound; results invalid */
     PK_ERR_NOMEM = 7,        /* workspace allocation failed */
-    PK_ERR_INTERNAL = 8      /* device: schedule exceeded its capacity (a library bug) */
+    PK_ERR_INTERNAL = 8,     /* device: schedule exceeded its capacity (a library bug) */
+    PK_ERR_TOO_LARGE = 9     /* pk_attend_noalloc: T above PK_NOALLOC_MAX_T */
 };
 
 enum pk_dtype { PK_F32 = 0, PK_BF16 = 1, PK_F16 = 2 };
@@ -128,6 +129,34 @@ int pk_last_status(struct CUstream_st *stream);
  */
 int pk_profile_start(int n);
 int pk_profile_stop(double *schedule_ms, double *attend_ms, int *calls);
+
+/*
+ * pk_attend_noalloc: the same forward pass for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point.
+ *
+ * pk_attend allocates a small workspace with cudaMalloc on first use per stream. Callers
+ * that plan every byte of device memory themselves (a serving process with a fixed budget,
+ * a plugin whose enqueue step may not allocate, an application whose pool allocator owns
+ * the device) or that cannot afford the synchronization a cudaMalloc brings use this call
+ * instead: it allocates nothing, and runs the same kernels on a scratch area compiled into
+ * the library (a static __device__ array of about 1.5 MB, present on every GPU that loads
+ * the library until the process exits).
+ *   - dtype: enum pk_dtype; the other arguments as pk_attend.
+ *   - T at most PK_NOALLOC_MAX_T tokens; larger T returns PK_ERR_TOO_LARGE, nothing launched.
+ *   - status: optional device pointer (NULL: none). The call writes there, in stream order,
+ *     the device-detected result of this call (PK_OK, PK_ERR_BAD_CU, PK_ERR_TIMEOUT).
+ *     pk_last_status does not see this entry point's device errors.
+ *   - The first call on a device does a one-time set-up with that device current (device
+ *     check, kernel attributes, the scratch array's device address); make it before any
+ *     stream capture.
+ *   - All calls share the one scratch area, which keeps the last call's contents (each call
+ *     clears its control block first): calls that overlap on the GPU race, so order them
+ *     (one stream, or events between streams).
+ */
+#define PK_NOALLOC_MAX_T 1048576LL
+int pk_attend_noalloc(int dtype, const void *qkv, const void *cos, const void *sin,
+                      const uint32_t *cu, int S, int64_t T, int H, int window, float scale,
+                      void *out, float *lse, int *status, struct CUstream_st *stream);
 
 /* Text of a status code (static storage). */
 const char *pk_status_string(int status);

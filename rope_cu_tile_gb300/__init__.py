@@ -23,12 +23,14 @@ PK_F32, PK_BF16, PK_F16 = 0, 1, 2
 STATUS = {
     0: "PK_OK", 1: "PK_ERR_ARG", 2: "PK_ERR_ALIGN", 3: "PK_ERR_CUDA", 4: "PK_ERR_UNSUPPORTED",
     5: "PK_ERR_BAD_CU", 6: "PK_ERR_TIMEOUT", 7: "PK_ERR_NOMEM", 8: "PK_ERR_INTERNAL",
+    9: "PK_ERR_TOO_LARGE",
 }
+NOALLOC_MAX_T = 1048576
 
 # names declared in include/pk.h
 EXPORTS = ("pk_attend", "pk_attend_bf16", "pk_attend_f16", "pk_attend_f32", "pk_attend_dt",
            "pk_schedule", "pk_schedule_capacity", "pk_last_status", "pk_status_string",
-           "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop")
+           "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop", "pk_attend_noalloc")
 
 _lib = None
 
@@ -56,6 +58,8 @@ def load(path: str | None = None):
         getattr(L, name).restype = i32
     L.pk_attend_dt.argtypes = [i32] + sig
     L.pk_attend_dt.restype = i32
+    L.pk_attend_noalloc.argtypes = [i32] + sig[:11] + [vp, vp]
+    L.pk_attend_noalloc.restype = i32
     L.pk_schedule.argtypes = [vp, i32, i64, i32, vp, i64, ctypes.POINTER(i64), vp]
     L.pk_schedule.restype = i32
     L.pk_schedule_capacity.argtypes = [i64]
@@ -96,6 +100,12 @@ def pk_attend(qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream) -> in
 
 def pk_attend_dt(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream) -> int:
     return load().pk_attend_dt(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream)
+
+
+def pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, status, stream) -> int:
+    """The allocation-free variant (see include/pk.h): for callers that cannot let the library
+    cudaMalloc a workspace; `status` is an optional device pointer to one int."""
+    return load().pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, status, stream)
 
 
 def pk_schedule(cu, S, T, window, tiles, cap, stream):

@@ -366,6 +366,7 @@ const char* pk_status_string(int status) {
     case PK_ERR_TIMEOUT: return "a device wait exceeded its bound; results invalid";
     case PK_ERR_NOMEM: return "workspace allocation failed";
     case PK_ERR_INTERNAL: return "schedule capacity exceeded (library bug)";
+    case PK_ERR_TOO_LARGE: return "T exceeds PK_NOALLOC_MAX_T, the static scratch capacity of pk_attend_noalloc";
     default: return "unknown status";
   }
 }

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(9):
+    for code in range(10):
         assert pk.status_string(code) != "unknown status"
     assert pk.status_string(99) == "unknown status"
     assert lib.pk_version() >= 100
