@@ -216,7 +216,7 @@ int launch_attend(int dtype, const void* qkv, const void* cos, const void* sin, 
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return PK_ERR_CUDA;
   return attend_tc_launch(dtype == PK_BF16, tmap, cos, sin, cu, ws->tiles, out, lse, ws->ctl, H,
-                          static_cast<long long>(T), window, scale, timeout_ns(), di->sms * 2, stream) == cudaSuccess
+                          static_cast<long long>(T), window, scale, timeout_ns(), di->sms, stream) == cudaSuccess
              ? PK_OK
              : PK_ERR_CUDA;
 }

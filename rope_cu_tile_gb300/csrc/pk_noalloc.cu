@@ -162,7 +162,7 @@ extern "C" int pk_attend_noalloc(int dtype, const void* qkv, const void* cos, co
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PK_ERR_CUDA;
     e = attend_tc_launch(dtype == PK_BF16, tmap, cos, sin, cu, tiles, out, lse, ctl, H, static_cast<long long>(T),
-                         window, scale, noalloc_timeout_ns(), s->sms * 2, st);
+                         window, scale, noalloc_timeout_ns(), s->sms, st);
   }
   if (e != cudaSuccess) return PK_ERR_CUDA;
   if (status && cudaMemcpyAsync(status, &ctl->status, sizeof(int), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
