@@ -88,6 +88,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, letting the thread sleep up to `hint_ns` while the phase is incomplete
+// (it resumes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for phase `parity` of `bar`. Returns false when `timeout_ns` passes first.
 // A caller that already gave up (`give_up`) does not wait at all.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
@@ -306,14 +320,77 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Split form of a 32-column TMEM load: tmem_ld32_issue starts the load into r;
+// tmem_ld32_wait waits for every outstanding load of this thread and takes r as in/out
+// operands, so no use of r can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+      "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+      "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+      "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+      "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+      "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+      "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane <- r
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane, waited for before returning.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // ------------------------------------------------------------------------------------
 // 16-bit element helpers
 
 template <bool BF16>
 struct Elem;
 
+// fp32 products of 16-bit operands without unpacking: lo/hi half of a packed pair times
+// the matching half of another pair, accumulated in fp32 (fma.rn.f32.bf16 / .f16).
+#define PK_MIXED_FMA(TY)                                                                          \
+  __device__ static __forceinline__ float fma_lo(uint32_t a, uint32_t b, float c) {               \
+    float d;                                                                                      \
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"      \
+        "fma.rn.f32." TY " %0, al, bl, %3;\n\t}"                                                    \
+        : "=f"(d)                                                                                 \
+        : "r"(a), "r"(b), "f"(c));                                                                \
+    return d;                                                                                     \
+  }                                                                                               \
+  __device__ static __forceinline__ float fma_hi(uint32_t a, uint32_t b, float c) {               \
+    float d;                                                                                      \
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"      \
+        "fma.rn.f32." TY " %0, ah, bh, %3;\n\t}"                                                    \
+        : "=f"(d)                                                                                 \
+        : "r"(a), "r"(b), "f"(c));                                                                \
+    return d;                                                                                     \
+  }
+
 template <>
 struct Elem<true> {
+  PK_MIXED_FMA("bf16")
   __device__ static __forceinline__ float2 unpack(uint32_t u) {
     // low half is the element at the lower address
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
@@ -327,6 +404,7 @@ struct Elem<true> {
 
 template <>
 struct Elem<false> {
+  PK_MIXED_FMA("f16")
   __device__ static __forceinline__ float2 unpack(uint32_t u) {
     float lo, hi;
     asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
