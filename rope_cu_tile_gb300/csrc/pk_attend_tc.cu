@@ -6,75 +6,100 @@
 // scores and the output product on the matrix units, the softmax online per row with
 // masked keys weighing exactly zero, then out = O / l and lse = m + ln l.
 //
-// How (GB300): one persistent 512-thread CTA per SM runs two independent pipelines
-// ("slots"); each slot takes work items (tile record x head) from a global counter and
-// owns, in shared memory, two Q buffers (the next item's Q is fetched and rotated while
-// the current item runs), a 3-stage K ring and a 2-stage V ring, and 256 tensor-memory
-// columns:
-//     S [128 x 128] fp32    scores of the current key tile
-//     P [128 x 128] 16-bit  probabilities, the A operand of the PV product
-//     O [128 x  64] fp32    output accumulator
+// How (GB300): one persistent 512-thread CTA per SM. A work item is a PAIR of consecutive
+// tile records (A, B) of one head. When both are pieces of the same sequence they share
+// one key stream -- key tiles of 128 tokens from A's first key to the last key either can
+// see -- so every K / V tile is loaded and rotated once for two query tiles; otherwise B's
+// key tiles follow A's in the stream. A uses stream tiles [0, a1), B uses [b0, b1).
+//
+// Shared memory: Q tiles A and B, double-buffered across items (the next item's Q is
+// fetched and rotated while the current one runs), a K ring and a V ring over the stream,
+// and per rotation thread two 128-byte cos / sin table rows. Tensor memory (512 columns):
+//     S_A, S_B [128 x 128] fp32    scores of the current key tile
+//     P_A, P_B [128 x 128] 16-bit  probabilities, the A operand of the PV product
+//     O_A, O_B [128 x  64] fp32    output accumulators
 // Warpgroups (each warp's TMEM lane quarter is its index mod 4):
-//   WG0  warp s (s = 0, 1): producer of slot s (one lane): claims items, TMA-loads Q, K and V
-//        tiles (128-byte swizzle, straight from the strided qkv), K one tile ahead of V;
-//        warp 2 + s: MMA issuer of slot s (one lane): S(j) = Q K(j)^T once K(j) is rotated
-//        and the S columns were read, O += P(j) V(j) once P(j) is written.
-//   WG1  warps 4 + 2s, 5 + 2s: rotation of slot s: 64 threads rotate (and for Q scale) two
-//        rows each of every Q and K tile in shared memory as soon as it lands.
-//   WG2, WG3  softmax of slot 0, 1: thread r owns query row r. It reads its S row from TMEM,
+//   WG0  warp 0: producer (one lane): claims items, TMA-loads Q_A, Q_B and the stream's
+//        K and V tiles (128-byte swizzle, straight from the strided qkv), K two tiles ahead
+//        of V; warps 1, 2: MMA issuers of A, B (one lane each): per stream tile j,
+//        S_X(j) = Q_X K(j)^T when X uses j, then O_X += P_X(j-1) V(j-1); warp 3 idle.
+//   WG1  rotation: thread t rotates (and for Q scales) row t of every Q and K tile in
+//        shared memory as soon as it lands, from table rows it prefetched with cp.async.
+//   WG2, WG3  softmax of A, B: thread r owns query row r. It reads its S row from TMEM,
 //        masks it by the row's visible key interval, keeps a running max (O is rescaled
 //        only when the max grows by more than a factor 2^8), writes P to TMEM, and at the
 //        end of the item writes out = O / l and lse = m + ln l.
 // Every wait is bounded. A wait that times out records PK_ERR_TIMEOUT and raises the
-// CTA's abort flag, which every other wait watches; the producers then wait (bounded)
-// for their copies in flight, the MMA issuers for their MMAs, and the CTA frees its
-// tensor memory and returns.
+// CTA's abort flag, which every other wait watches; the producer then waits (bounded)
+// for its copies in flight, the MMA issuer for its MMAs, and the CTA frees its tensor
+// memory and returns.
 #include "pk_dev.cuh"
 
 namespace pk {
 
 namespace {
 
-constexpr int kSlots = 2;
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
 constexpr int kThreads = 512;
-constexpr int kWarpMma = 2;    // warps 2, 3
-constexpr int kWarpRot = 4;    // warps 4, 5 (slot 0), 6, 7 (slot 1)
-constexpr int kWarpSm = 8;     // warps 8..11 (slot 0), 12..15 (slot 1)
-constexpr int kRotThreads = 64;
+constexpr int kKStages = 4;
+constexpr int kVStages = 3;
+constexpr int kWarpProd = 0;
+constexpr int kWarpMma = 1;  // warps 1 (A), 2 (B)
+constexpr int kWarpRot = 4;  // warps 4..7
+constexpr int kWarpSm = 8;   // warps 8..11 (A), 12..15 (B)
 
 constexpr uint32_t kTileBytes = 128 * 128;  // 128 rows x 64 x 16-bit
-constexpr uint32_t kSlotBytes = kTileBytes * (2 + kKStages + kVStages);
+constexpr uint32_t kRowTblBytes = 128;      // cos (64 B) + sin (64 B) of one position
+// shared-memory map (offsets from the 1024-aligned base)
+constexpr uint32_t kOffQ = 0;                                      // [X][buffer] tiles
+constexpr uint32_t kOffK = kOffQ + 4 * kTileBytes;                 // K ring
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;          // V ring
+constexpr uint32_t kOffTbl = kOffV + kVStages * kTileBytes;        // [thread][2] table rows
+constexpr uint32_t kOffMeta = kOffTbl + 128 * 2 * kRowTblBytes;
 
+// One work item as the producer hands it to the other roles.
 struct ItemBox {
-  TileRec rec;
+  TileRec a, b;
   int32_t head;
-  int32_t valid;
-  int32_t pad[6];
+  int32_t valid;     // 0: no more work
+  uint32_t has_b;    // 1: B is a record
+  uint32_t shared;   // 1: B reads A's key stream
+  uint32_t nstream;  // key tiles in the stream
+  uint32_t a1;       // A uses stream tiles [0, a1)
+  uint32_t b0, b1;   // B uses stream tiles [b0, b1) (empty without B)
+  uint32_t end;      // shared stream: one past its last key token
+  uint32_t pad[7];
 };
+static_assert(sizeof(ItemBox) % 16 == 0, "item box keeps 16-byte alignment");
 
-struct SlotBars {
+struct Bars {
   uint64_t item_full[2], item_empty[2];
-  uint64_t q_full[2], q_ready[2], q_empty[2];
+  uint64_t q_full[2][2], q_ready[2][2], q_empty[2][2];  // [X][buffer]
   uint64_t k_full[kKStages], k_ready[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full, s_consumed, p_ready, pv_done;
-  uint64_t drain;
+  uint64_t s_full[2], s_consumed[2], p_ready[2], pv_done[2];  // [X]
+  uint64_t cu_rot[2], cu_sm[2][2];  // staged offsets ready: [item parity], [X][item parity]
+  uint64_t drain[2];
 };
 
+// Member sequence offsets of an item's records, staged by the rotation warpgroup (A's and
+// B's) and by each softmax warpgroup (its own record's).
+constexpr int kCuStage = kShort + 2;
 struct Meta {
-  SlotBars bars[kSlots];
-  ItemBox box[kSlots][2];
+  Bars bars;
+  ItemBox box[2];
+  uint32_t cu_rot[2][2][kCuStage];  // [item parity][X]
+  uint32_t cu_sm[2][2][kCuStage];   // [X][item parity]
   uint32_t tmem;
   int32_t abort;
 };
 
-constexpr uint32_t kOffMeta = kSlots * kSlotBytes;
 constexpr uint32_t kSmemUsed = kOffMeta + sizeof(Meta);
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;  // within a slot's 256 columns
-constexpr uint32_t kItemConsumers = 1 + kRotThreads / 32 + 4;  // MMA issuer + rotation warps + softmax warps
+// tensor-memory columns of query tile X
+__host__ __device__ constexpr uint32_t col_s(int x) { return 128u * x; }
+__host__ __device__ constexpr uint32_t col_p(int x) { return 256u + 64u * x; }
+__host__ __device__ constexpr uint32_t col_o(int x) { return 384u + 64u * x; }
+constexpr uint32_t kItemConsumers = 2 + 4 + 4 + 4;  // MMA issuers + rotation, softmax A, B warps
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -98,15 +123,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return y;
 }
 
-__device__ __forceinline__ uint8_t* slot_q(uint8_t* smem, int s, uint32_t b) {
-  return smem + s * kSlotBytes + kTileBytes * b;
+__device__ __forceinline__ uint8_t* q_tile(uint8_t* smem, int x, uint32_t b) {
+  return smem + kOffQ + kTileBytes * (2 * x + b);
 }
-__device__ __forceinline__ uint8_t* slot_k(uint8_t* smem, int s, uint32_t st) {
-  return smem + s * kSlotBytes + kTileBytes * (2 + st);
-}
-__device__ __forceinline__ uint8_t* slot_v(uint8_t* smem, int s, uint32_t st) {
-  return smem + s * kSlotBytes + kTileBytes * (2 + kKStages + st);
-}
+__device__ __forceinline__ uint8_t* k_tile(uint8_t* smem, uint32_t st) { return smem + kOffK + kTileBytes * st; }
+__device__ __forceinline__ uint8_t* v_tile(uint8_t* smem, uint32_t st) { return smem + kOffV + kTileBytes * st; }
 
 __device__ __forceinline__ bool aborted(const Meta* meta) {
   return *reinterpret_cast<const volatile int32_t*>(&meta->abort) != 0;
@@ -134,71 +155,61 @@ __device__ __forceinline__ bool wait_bar(Meta* meta, Ctl* ctl, uint64_t* bar, ui
   }
 }
 
-// keys of key tile j of a record: min(128, nk - 128 j)
-__device__ __forceinline__ uint32_t tile_keys(const TileRec& rec, uint32_t j) {
-  return min(static_cast<uint32_t>(kBC), rec.nk - j * kBC);
-}
-__device__ __forceinline__ uint32_t round16(uint32_t n) { return (n + 15u) & ~15u; }
-
-// The cos / sin table rows of one position (32 16-bit values each, four 16-byte chunks).
-struct RopeRow {
-  uint4 c[4], s[4];
+// A ring position: uses so far, giving stage and phase parity.
+struct Ring {
+  uint32_t n = 0;
+  __device__ __forceinline__ uint32_t stage(uint32_t depth) const { return n % depth; }
+  __device__ __forceinline__ uint32_t phase(uint32_t depth) const { return (n / depth) & 1u; }
 };
 
-__device__ __forceinline__ RopeRow load_rope_row(const uint16_t* cos_t, const uint16_t* sin_t, uint32_t pos) {
-  RopeRow t;
-  const uint4* c = reinterpret_cast<const uint4*>(cos_t + static_cast<size_t>(pos) * kHalf);
-  const uint4* s = reinterpret_cast<const uint4*>(sin_t + static_cast<size_t>(pos) * kHalf);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    t.c[k] = __ldg(c + k);
-    t.s[k] = __ldg(s + k);
-  }
-  return t;
+__device__ __forceinline__ uint32_t round16(uint32_t n) { return (n + 15u) & ~15u; }
+
+// The key stream of an item, as every role keeps it in registers.
+struct Stream {
+  uint32_t a_k0, a_nk, b_k0, b_nk;
+  uint32_t end;     // shared stream: one past its last key token
+  uint32_t a1;      // A uses stream tiles [0, a1)
+  uint32_t b0, b1;  // B uses stream tiles [b0, b1)
+  uint32_t n;       // stream tiles
+  uint32_t shared;  // 1: B reads A's key stream; 0: B's tiles follow A's
+};
+__device__ __forceinline__ Stream stream_of(const ItemBox& bx) {
+  Stream s;
+  s.a_k0 = bx.a.k0;
+  s.a_nk = bx.a.nk;
+  s.b_k0 = bx.b.k0;
+  s.b_nk = bx.b.nk;
+  s.end = bx.end;
+  s.a1 = bx.a1;
+  s.b0 = bx.b0;
+  s.b1 = bx.b1;
+  s.n = bx.nstream;
+  s.shared = bx.shared;
+  return s;
 }
 
-// Rotate and multiply by `mul` row r of a 128-byte-swizzled 64-column tile in
-// place: y[u] = x[u] c - x[u+32] s, y[u+32] = x[u] s + x[u+32] c, in fp32 straight from the
-// 16-bit operands. Elements u and u + 32 are logical 16-byte chunks c and c + 4, stored at
-// chunks (c ^ (r & 7)) and ((c + 4) ^ (r & 7)).
-template <bool BF16>
-__device__ __forceinline__ void rope_row_sw128(uint8_t* tile, int r, const RopeRow t, float mul) {
-  using E = Elem<BF16>;
-  uint8_t* row = tile + r * 128;
-  const int sw = r & 7;
-  // two halves of the row; within a half every chunk is read before any is written back
-#pragma unroll 1
-  for (int hh = 0; hh < 2; ++hh) {
-    uint4 x1[2], x2[2];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int c = 2 * hh + q;
-      x1[q] = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
-      x2[q] = *reinterpret_cast<const uint4*>(row + (((c + 4) ^ sw) << 4));
-    }
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int c = 2 * hh + q;
-      const uint4 tc = hh ? t.c[2 + q] : t.c[q];
-      const uint4 ts = hh ? t.s[2 + q] : t.s[q];
-      const uint32_t a[4] = {x1[q].x, x1[q].y, x1[q].z, x1[q].w};
-      const uint32_t b[4] = {x2[q].x, x2[q].y, x2[q].z, x2[q].w};
-      const uint32_t cc[4] = {tc.x, tc.y, tc.z, tc.w};
-      const uint32_t ss[4] = {ts.x, ts.y, ts.z, ts.w};
-      uint32_t y1[4], y2[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float lo1 = E::fma_lo(a[k], cc[k], -E::fma_lo(b[k], ss[k], 0.f));
-        const float hi1 = E::fma_hi(a[k], cc[k], -E::fma_hi(b[k], ss[k], 0.f));
-        const float lo2 = E::fma_lo(a[k], ss[k], E::fma_lo(b[k], cc[k], 0.f));
-        const float hi2 = E::fma_hi(a[k], ss[k], E::fma_hi(b[k], cc[k], 0.f));
-        y1[k] = E::pack(lo1 * mul, hi1 * mul);
-        y2[k] = E::pack(lo2 * mul, hi2 * mul);
-      }
-      *reinterpret_cast<uint4*>(row + ((c ^ sw) << 4)) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
-      *reinterpret_cast<uint4*>(row + (((c + 4) ^ sw) << 4)) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
-    }
+// Stream tile j of an item: its first key token, its key count, and whether it is one of
+// B's own tiles (a concatenated stream past A's tiles).
+struct StreamTile {
+  uint32_t j0, nkeys;
+  bool from_b;
+};
+__device__ __forceinline__ StreamTile stream_tile(const Stream& s, uint32_t j) {
+  StreamTile st;
+  if (s.shared) {
+    st.j0 = s.a_k0 + j * kBC;
+    st.nkeys = min(static_cast<uint32_t>(kBC), s.end - st.j0);
+    st.from_b = false;
+  } else if (j < s.a1) {
+    st.j0 = s.a_k0 + j * kBC;
+    st.nkeys = min(static_cast<uint32_t>(kBC), s.a_nk - j * kBC);
+    st.from_b = false;
+  } else {
+    st.j0 = s.b_k0 + (j - s.a1) * kBC;
+    st.nkeys = min(static_cast<uint32_t>(kBC), s.b_nk - (j - s.a1) * kBC);
+    st.from_b = true;
   }
+  return st;
 }
 
 struct Params {
@@ -216,51 +227,118 @@ struct Params {
   unsigned long long timeout_ns;
 };
 
-// in-sequence position of token a of a record (a group's rows belong to several sequences)
-__device__ __forceinline__ uint32_t position_of(const Params& p, const TileRec& rec, uint32_t a,
-                                                uint32_t piece_start) {
-  if (rec.kind == 0) return a - piece_start;
-  const uint32_t sq = seq_of_token(p.cu, rec.seq, rec.nseq, a);
-  return a - __ldg(p.cu + sq);
+// The member sequence offsets cu[rec.seq .. rec.seq + rec.nseq] of a record, copied by the
+// `nthr` threads of a warpgroup into `dst` when they fit (a group can hold any number of
+// empty sequences; past kCuStage - 1 members only the first offset is staged).
+__device__ __forceinline__ bool staged_all(const TileRec& rec) { return rec.nseq + 1 <= kCuStage; }
+__device__ __forceinline__ void stage_cu(const Params& p, const TileRec& rec, uint32_t* dst, int t, int nthr) {
+  const int n = staged_all(rec) ? static_cast<int>(rec.nseq) : 0;
+  for (int i = t; i <= n; i += nthr) dst[i] = __ldg(p.cu + rec.seq + i);
+}
+
+// The sequence (index into a staged offset list of n + 1 values) holding token a:
+// the last i < n with off[i] <= a.
+__device__ __forceinline__ int staged_seq(const uint32_t* off, int n, uint32_t a) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= a)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// Start and end tokens of the sequence of record `rec` that holds token a, from the staged
+// offsets when they are all there, else from cu in global memory.
+__device__ __forceinline__ void seq_bounds(const Params& p, const TileRec& rec, const uint32_t* off, uint32_t a,
+                                           uint32_t& ss, uint32_t& se) {
+  if (rec.kind == 0) {
+    ss = off[0];
+    se = off[1];
+  } else if (staged_all(rec)) {
+    const int i = staged_seq(off, static_cast<int>(rec.nseq), a);
+    ss = off[i];
+    se = off[i + 1];
+  } else {
+    const uint32_t sq = seq_of_token(p.cu, rec.seq, rec.nseq, a);
+    ss = __ldg(p.cu + sq);
+    se = __ldg(p.cu + sq + 1);
+  }
 }
 
 // ------------------------------------------------------------------------------------
-// producer of one slot (one thread): work items and TMA loads. Per item: Q into buffer
-// (item count & 1), then K(0), K(1), V(0), K(2), V(1), ... so each K tile is requested a
-// tile ahead of its V.
+// table rows in shared memory (cp.async, 16 bytes at a time, no registers held; through L1,
+// since the rows of short sequences are the same few table rows for every thread)
 
-struct Ring {
-  uint32_t n = 0;  // uses so far
-  __device__ __forceinline__ uint32_t stage(uint32_t depth) const { return n % depth; }
-  __device__ __forceinline__ uint32_t phase(uint32_t depth) const { return (n / depth) & 1u; }
-};
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-__device__ void producer(const CUtensorMap* tmap, const Params& p, uint8_t* smem, Meta* meta, int s,
+// Copies the cos and sin rows of position `pos` (32 16-bit values each) into the 128-byte
+// row buffer `buf`: logical chunk k (cos 0..3, sin 4..7) at 16-byte slot k ^ (t & 7), so the
+// eight threads of a quarter warp reading the same chunk hit eight different bank groups.
+__device__ __forceinline__ void fetch_table_row(const Params& p, uint32_t buf, uint32_t pos, int t) {
+  const uint16_t* c = p.cos_t + static_cast<size_t>(pos) * kHalf;
+  const uint16_t* s = p.sin_t + static_cast<size_t>(pos) * kHalf;
+  const int sw = t & 7;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    cp_async16(buf + ((k ^ sw) << 4), c + 8 * k);
+    cp_async16(buf + (((k + 4) ^ sw) << 4), s + 8 * k);
+  }
+}
+
+// Rotate and multiply by `mul` row r of a 128-byte-swizzled 64-column tile in place:
+// y[u] = x[u] c - x[u+32] s, y[u+32] = x[u] s + x[u+32] c, in fp32 straight from the 16-bit
+// operands. Elements u and u + 32 are logical 16-byte chunks c and c + 4, stored at chunks
+// (c ^ (r & 7)) and ((c + 4) ^ (r & 7)); the table row is in `tbl` as fetch_table_row left it.
+template <bool BF16>
+__device__ __forceinline__ void rope_row(uint8_t* tile, int r, const uint8_t* tbl, int t, float mul) {
+  using E = Elem<BF16>;
+  uint8_t* row = tile + r * 128;
+  const int sw = r & 7, tw = t & 7;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 x1 = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+    const uint4 x2 = *reinterpret_cast<const uint4*>(row + (((c + 4) ^ sw) << 4));
+    const uint4 tc = *reinterpret_cast<const uint4*>(tbl + ((c ^ tw) << 4));
+    const uint4 ts = *reinterpret_cast<const uint4*>(tbl + (((c + 4) ^ tw) << 4));
+    const uint32_t a[4] = {x1.x, x1.y, x1.z, x1.w};
+    const uint32_t b[4] = {x2.x, x2.y, x2.z, x2.w};
+    const uint32_t cc[4] = {tc.x, tc.y, tc.z, tc.w};
+    const uint32_t ss[4] = {ts.x, ts.y, ts.z, ts.w};
+    uint32_t y1[4], y2[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo1 = E::fma_lo(a[k], cc[k], -E::fma_lo(b[k], ss[k], 0.f));
+      const float hi1 = E::fma_hi(a[k], cc[k], -E::fma_hi(b[k], ss[k], 0.f));
+      const float lo2 = E::fma_lo(a[k], ss[k], E::fma_lo(b[k], cc[k], 0.f));
+      const float hi2 = E::fma_hi(a[k], ss[k], E::fma_hi(b[k], cc[k], 0.f));
+      y1[k] = E::pack(lo1 * mul, hi1 * mul);
+      y2[k] = E::pack(lo2 * mul, hi2 * mul);
+    }
+    *reinterpret_cast<uint4*>(row + ((c ^ sw) << 4)) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+    *reinterpret_cast<uint4*>(row + (((c + 4) ^ sw) << 4)) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// producer (one thread): work items and TMA loads. Per item: Q_A, Q_B into their buffers,
+// then K(0), K(1), V(0), K(2), V(1), ... over the key stream.
+
+__device__ void producer(const CUtensorMap* tmap, const Params& p, uint8_t* smem, Meta* meta,
                          unsigned int n_items) {
-  SlotBars& B = meta->bars[s];
+  Bars& B = meta->bars;
   const int32_t hd = p.H * kD;
+  const unsigned int ntiles = __ldcg(&p.ctl->ntiles);
   uint32_t it = 0;
-  Ring q, k, v;
+  Ring q0r, q1r, k, v;
   bool bad = false;
-
-  auto load_k = [&](const TileRec& rec, int h, uint32_t j) -> bool {
-    const uint32_t st = k.stage(kKStages);
-    if (!wait_bar(meta, p.ctl, &B.k_empty[st], k.phase(kKStages) ^ 1u, p.timeout_ns)) return false;
-    mbar_arrive_expect_tx(smem_u32(&B.k_full[st]), kTileBytes);
-    tma_load_2d(smem_u32(slot_k(smem, s, st)), tmap, smem_u32(&B.k_full[st]), hd + h * kD,
-                static_cast<int32_t>(rec.k0 + j * kBC));
-    ++k.n;
-    return true;
-  };
-  auto load_v = [&](const TileRec& rec, int h, uint32_t j) -> bool {
-    const uint32_t st = v.stage(kVStages);
-    if (!wait_bar(meta, p.ctl, &B.v_empty[st], v.phase(kVStages) ^ 1u, p.timeout_ns)) return false;
-    mbar_arrive_expect_tx(smem_u32(&B.v_full[st]), kTileBytes);
-    tma_load_2d(smem_u32(slot_v(smem, s, st)), tmap, smem_u32(&B.v_full[st]), 2 * hd + h * kD,
-                static_cast<int32_t>(rec.k0 + j * kBC));
-    ++v.n;
-    return true;
-  };
 
   for (;;) {
     const unsigned int item = atomicAdd(&p.ctl->next, 1u);
@@ -269,39 +347,89 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, uint8_t* smem
       bad = true;
       break;
     }
-    ItemBox& bx = meta->box[s][mb];
+    ItemBox& bx = meta->box[mb];
     if (item >= n_items) {
       bx.valid = 0;
       mbar_arrive(smem_u32(&B.item_full[mb]));
       break;
     }
-    const unsigned int ti = item / static_cast<unsigned int>(p.H);
+    const unsigned int pair = item / static_cast<unsigned int>(p.H);
     const int h = static_cast<int>(item % static_cast<unsigned int>(p.H));
-    const TileRec rec = p.tiles[ti];
-    bx.rec = rec;
+    const TileRec ra = p.tiles[2 * pair];
+    const bool has_b = 2 * pair + 1 < ntiles;
+    TileRec rb = ra;
+    if (has_b) rb = p.tiles[2 * pair + 1];
+    const bool shared = has_b && ra.kind == 0 && rb.kind == 0 && ra.seq == rb.seq;
+    uint32_t nstream, b0, b1, end = 0;
+    if (shared) {
+      end = max(ra.k0 + ra.nk, rb.k0 + rb.nk);
+      nstream = (end - ra.k0 + kBC - 1) / kBC;
+      b0 = (rb.k0 - ra.k0) / kBC;
+      b1 = (rb.k0 + rb.nk - ra.k0 + kBC - 1) / kBC;
+    } else {
+      nstream = ra.ktiles + (has_b ? rb.ktiles : 0u);
+      b0 = ra.ktiles;
+      b1 = nstream;
+    }
+    bx.a = ra;
+    bx.b = rb;
     bx.head = h;
     bx.valid = 1;
+    bx.has_b = has_b;
+    bx.shared = shared;
+    bx.nstream = nstream;
+    bx.a1 = ra.ktiles;
+    bx.b0 = b0;
+    bx.b1 = b1;
+    bx.end = end;
     mbar_arrive(smem_u32(&B.item_full[mb]));
     ++it;
-    // Q into its buffer once the item two back has finished its last S
-    const uint32_t qb = q.stage(2);
-    if (!wait_bar(meta, p.ctl, &B.q_empty[qb], q.phase(2) ^ 1u, p.timeout_ns)) {
-      bad = true;
-      break;
+
+    // Q_X into its next buffer once the item two back has issued its last S_X
+    auto load_q = [&](int x, Ring& qr, uint32_t q0) -> bool {
+      const uint32_t qb = qr.stage(2);
+      if (!wait_bar(meta, p.ctl, &B.q_empty[x][qb], qr.phase(2) ^ 1u, p.timeout_ns)) return false;
+      mbar_arrive_expect_tx(smem_u32(&B.q_full[x][qb]), kTileBytes);
+      tma_load_2d(smem_u32(q_tile(smem, x, qb)), tmap, smem_u32(&B.q_full[x][qb]), h * kD, static_cast<int32_t>(q0));
+      ++qr.n;
+      return true;
+    };
+    bad = !load_q(0, q0r, ra.q0) || (has_b && !load_q(1, q1r, rb.q0));
+    if (bad) break;
+    // the stream: K two tiles ahead of V
+    const Stream sm = stream_of(bx);
+    for (uint32_t t = 0; t < nstream + 2 && !bad; ++t) {
+      if (t < nstream) {
+        const uint32_t st = k.stage(kKStages);
+        if (!wait_bar(meta, p.ctl, &B.k_empty[st], k.phase(kKStages) ^ 1u, p.timeout_ns)) {
+          bad = true;
+          break;
+        }
+        mbar_arrive_expect_tx(smem_u32(&B.k_full[st]), kTileBytes);
+        tma_load_2d(smem_u32(k_tile(smem, st)), tmap, smem_u32(&B.k_full[st]), hd + h * kD,
+                    static_cast<int32_t>(stream_tile(sm, t).j0));
+        ++k.n;
+      }
+      if (t >= 2) {
+        const uint32_t st = v.stage(kVStages);
+        if (!wait_bar(meta, p.ctl, &B.v_empty[st], v.phase(kVStages) ^ 1u, p.timeout_ns)) {
+          bad = true;
+          break;
+        }
+        mbar_arrive_expect_tx(smem_u32(&B.v_full[st]), kTileBytes);
+        tma_load_2d(smem_u32(v_tile(smem, st)), tmap, smem_u32(&B.v_full[st]), 2 * hd + h * kD,
+                    static_cast<int32_t>(stream_tile(sm, t - 2).j0));
+        ++v.n;
+      }
     }
-    mbar_arrive_expect_tx(smem_u32(&B.q_full[qb]), kTileBytes);
-    tma_load_2d(smem_u32(slot_q(smem, s, qb)), tmap, smem_u32(&B.q_full[qb]), h * kD, static_cast<int32_t>(rec.q0));
-    ++q.n;
-    const uint32_t n = rec.ktiles;
-    bad = !load_k(rec, h, 0) || (n > 1 && !load_k(rec, h, 1));
-    for (uint32_t j = 0; !bad && j < n; ++j)
-      bad = !load_v(rec, h, j) || (j + 2 < n && !load_k(rec, h, j + 2));
     if (bad) break;
   }
   if (bad || aborted(meta)) {
-    // let this slot's own copies land before the CTA's shared memory goes away
-    for (uint32_t t = q.n > 2 ? q.n - 2 : 0; t < q.n; ++t)
-      mbar_wait(smem_u32(&B.q_full[t % 2]), (t / 2) & 1u, p.timeout_ns);
+    // let the copies in flight land before the CTA's shared memory goes away
+    for (uint32_t t = q0r.n > 2 ? q0r.n - 2 : 0; t < q0r.n; ++t)
+      mbar_wait(smem_u32(&B.q_full[0][t % 2]), (t / 2) & 1u, p.timeout_ns);
+    for (uint32_t t = q1r.n > 2 ? q1r.n - 2 : 0; t < q1r.n; ++t)
+      mbar_wait(smem_u32(&B.q_full[1][t % 2]), (t / 2) & 1u, p.timeout_ns);
     for (uint32_t t = k.n > kKStages ? k.n - kKStages : 0; t < k.n; ++t)
       mbar_wait(smem_u32(&B.k_full[t % kKStages]), (t / kKStages) & 1u, p.timeout_ns);
     for (uint32_t t = v.n > kVStages ? v.n - kVStages : 0; t < v.n; ++t)
@@ -310,166 +438,265 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, uint8_t* smem
 }
 
 // ------------------------------------------------------------------------------------
-// MMA issuer of one slot (one thread)
+// MMA issuer of query tile X (one thread; one issuer per query tile, on different SM
+// sub-partitions, so that each keeps its share of the tensor pipe fed). For every stream
+// tile t: once K(t) is rotated, S_X(t) = Q_X K(t)^T if X's range holds t (after Q_X is
+// rotated and S_X's previous scores were read); then, once V(t - 1) has landed,
+// O_X += P_X(t - 1) V(t - 1) if X's range holds t - 1 (after P_X is written). K and V ring
+// stages are released by both issuers (barriers of count 2): by a commit after the MMAs
+// that read them, or by a plain arrival for a tile outside X's range -- made only after the
+// tile's own ready / full phase was seen, so an issuer never runs a phase ahead.
 
-__device__ void mma_issuer(const Params& p, uint8_t* smem, Meta* meta, int s, uint32_t tmem, bool bf16) {
-  SlotBars& B = meta->bars[s];
-  const uint32_t tS = tmem + s * 256 + kColS, tP = tmem + s * 256 + kColP, tO = tmem + s * 256 + kColO;
+__device__ void mma_issuer(const Params& p, uint8_t* smem, Meta* meta, uint32_t tmem, bool bf16, int x) {
+  Bars& B = meta->bars;
   const uint32_t idesc_pv = idesc_f16(bf16, 128, 64, false, true);
-  // operand descriptors of every buffer, computed once; a K step of 16 adds 32 bytes (Q, K)
-  // or 2048 bytes (V) to the start address field (address >> 4)
-  // (buffers of one kind are consecutive 16 KB tiles: the next one is 1024 further)
-  const uint64_t dq0 = sdesc_sw128(smem_u32(slot_q(smem, s, 0)), 16, 1024);
-  const uint64_t dk0 = sdesc_sw128(smem_u32(slot_k(smem, s, 0)), 16, 1024);
-  const uint64_t dv0 = sdesc_sw128(smem_u32(slot_v(smem, s, 0)), 8192, 1024);
-  uint32_t it = 0, sc = 0, pr = 0;
-  Ring q, k, v;
-  bool pending_sc = false;  // an S was issued whose consumption has not been seen yet
-
-  // S(j) = Q K(j)^T: needs Q rotated (j = 0), K(j) rotated, and the S columns read
-  auto issue_s = [&](const TileRec& rec, uint32_t j, uint32_t qb) -> bool {
-    if (j == 0) {
-      if (!wait_bar(meta, p.ctl, &B.q_ready[qb], q.phase(2), p.timeout_ns)) return false;
-    }
-    const uint32_t st = k.stage(kKStages);
-    if (!wait_bar(meta, p.ctl, &B.k_ready[st], k.phase(kKStages), p.timeout_ns)) return false;
-    if (pending_sc) {
-      if (!wait_bar(meta, p.ctl, &B.s_consumed, sc & 1u, p.timeout_ns)) return false;
-      ++sc;
-    }
-    tc_fence_after();
-    const uint32_t idesc = idesc_f16(bf16, 128, round16(tile_keys(rec, j)), false, false);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      umma_f16_ss(tS, dq0 + qb * 1024 + ks * 2, dk0 + st * 1024 + ks * 2, idesc, ks > 0);
-    umma_commit(smem_u32(&B.s_full));
-    umma_commit(smem_u32(&B.k_empty[st]));
-    if (j + 1 == rec.ktiles) umma_commit(smem_u32(&B.q_empty[qb]));
-    ++k.n;
-    pending_sc = true;
-    return true;
-  };
+  // operand descriptors of the first buffer of each kind; a K step of 16 adds 32 bytes (Q,
+  // K) or 2048 bytes (V) to the start address field (address >> 4), and the next 16 KB tile
+  // of a kind is 1024 further
+  const uint64_t dq0 = sdesc_sw128(smem_u32(q_tile(smem, x, 0)), 16, 1024);
+  const uint64_t dk0 = sdesc_sw128(smem_u32(k_tile(smem, 0)), 16, 1024);
+  const uint64_t dv0 = sdesc_sw128(smem_u32(v_tile(smem, 0)), 8192, 1024);
+  const uint32_t tS = tmem + col_s(x), tP = tmem + col_p(x), tO = tmem + col_o(x);
+  uint32_t it = 0, sc = 0, pr = 0, qn = 0;
+  bool pend = false;  // an S_X was issued whose reading has not been awaited yet
+  Ring k, v;
+  bool bad = false;
 
   for (;;) {
     const uint32_t mb = it & 1u;
     if (!wait_bar(meta, p.ctl, &B.item_full[mb], (it >> 1) & 1u, p.timeout_ns)) break;
-    const ItemBox bx = meta->box[s][mb];
+    const bool valid = meta->box[mb].valid != 0;
+    const Stream sm = stream_of(meta->box[mb]);
     mbar_arrive(smem_u32(&B.item_empty[mb]));
     ++it;
-    if (!bx.valid) break;
-    const TileRec rec = bx.rec;
-    const uint32_t qb = q.stage(2);
-    bool bad = false;
-    // step t: S(t) (t < ktiles), then PV(t - 1) (t >= 1)
-    for (uint32_t t = 0; !bad && t <= rec.ktiles; ++t) {
-      if (t < rec.ktiles && !issue_s(rec, t, qb)) {
-        bad = true;
-        break;
-      }
-      if (t == 0) continue;
-      const uint32_t j = t - 1;
-      // O += P(j) V(j)
-      if (!wait_bar(meta, p.ctl, &B.p_ready, pr & 1u, p.timeout_ns)) {
-        bad = true;
-        break;
-      }
-      ++pr;
-      const uint32_t st = v.stage(kVStages);
-      if (!wait_bar(meta, p.ctl, &B.v_full[st], v.phase(kVStages), p.timeout_ns)) {
-        bad = true;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t ksteps = round16(tile_keys(rec, j)) / 16;
+    if (!valid) break;
+    const uint32_t lo = x == 0 ? 0u : sm.b0, hi = x == 0 ? sm.a1 : sm.b1;
+    for (uint32_t t = 0; t <= sm.n && !bad; ++t) {
+      if (t < sm.n) {
+        const uint32_t st = k.stage(kKStages);
+        if (!wait_bar(meta, p.ctl, &B.k_ready[st], k.phase(kKStages), p.timeout_ns)) {
+          bad = true;
+          break;
+        }
+        if (t >= lo && t < hi) {
+          const uint32_t qb = qn & 1u;
+          if (t == lo && !wait_bar(meta, p.ctl, &B.q_ready[x][qb], (qn >> 1) & 1u, p.timeout_ns)) {
+            bad = true;
+            break;
+          }
+          if (pend) {
+            if (!wait_bar(meta, p.ctl, &B.s_consumed[x], sc & 1u, p.timeout_ns)) {
+              bad = true;
+              break;
+            }
+            ++sc;
+          }
+          tc_fence_after();
+          const uint32_t idesc = idesc_f16(bf16, 128, round16(stream_tile(sm, t).nkeys), false, false);
+          const uint64_t dq = dq0 + qb * 1024, dk = dk0 + st * 1024;
+          umma_f16_ss(tS, dq, dk, idesc, 0u);
 #pragma unroll
-      for (uint32_t ks = 0; ks < 8; ++ks)
-        if (ks < ksteps)
-          umma_f16_ts(tO, tP + ks * 8, dv0 + st * 1024 + ks * 128, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-      umma_commit(smem_u32(&B.pv_done));
-      umma_commit(smem_u32(&B.v_empty[st]));
-      ++v.n;
+          for (int ks = 1; ks < 4; ++ks) umma_f16_ss(tS, dq + ks * 2, dk + ks * 2, idesc, 1u);
+          umma_commit(smem_u32(&B.s_full[x]));
+          umma_commit(smem_u32(&B.k_empty[st]));
+          pend = true;
+          if (t + 1 == hi) {
+            umma_commit(smem_u32(&B.q_empty[x][qb]));
+            ++qn;
+          }
+        } else {
+          mbar_arrive(smem_u32(&B.k_empty[st]));
+        }
+        ++k.n;
+      }
+      if (t >= 1) {
+        const uint32_t j = t - 1;
+        const uint32_t st = v.stage(kVStages);
+        if (!wait_bar(meta, p.ctl, &B.v_full[st], v.phase(kVStages), p.timeout_ns)) {
+          bad = true;
+          break;
+        }
+        if (j >= lo && j < hi) {
+          if (!wait_bar(meta, p.ctl, &B.p_ready[x], pr & 1u, p.timeout_ns)) {
+            bad = true;
+            break;
+          }
+          ++pr;
+          tc_fence_after();
+          const uint32_t ksteps = round16(stream_tile(sm, j).nkeys) / 16;
+          const uint64_t dv = dv0 + st * 1024;
+          umma_f16_ts(tO, tP, dv, idesc_pv, j > lo ? 1u : 0u);
+#pragma unroll
+          for (uint32_t ks = 1; ks < 8; ++ks)
+            if (ks < ksteps) umma_f16_ts(tO, tP + ks * 8, dv + ks * 128, idesc_pv, 1u);
+          umma_commit(smem_u32(&B.pv_done[x]));
+          umma_commit(smem_u32(&B.v_empty[st]));
+        } else {
+          mbar_arrive(smem_u32(&B.v_empty[st]));
+        }
+        ++v.n;
+      }
     }
     if (bad) break;
-    ++q.n;
   }
   // every MMA this thread issued has completed before the CTA frees tensor memory
-  umma_commit(smem_u32(&B.drain));
-  mbar_wait(smem_u32(&B.drain), 0, p.timeout_ns);
+  umma_commit(smem_u32(&B.drain[x]));
+  mbar_wait(smem_u32(&B.drain[x]), 0, p.timeout_ns);
 }
 
 // ------------------------------------------------------------------------------------
-// rotation warps of one slot (64 threads, rows t and t + 64 of every tile)
+// rotation warpgroup (128 threads; thread t rotates row t of every tile)
 //
-// For each item: job 0 rotates and scales the Q tile, job 1 + j rotates K tile j, each as
-// soon as it lands. Each warp arrives on the ready barrier once its rows are written and
-// fenced (count 2); a failed wait is voted across the warp so a warp leaves together.
+// Jobs of an item, in order: Q_A, Q_B (when B is a record), then K(0) .. K(n - 1). The
+// table rows of job i + 1 are in flight (cp.async) while job i is rotated. A row's position
+// is its token minus the start of its sequence: one subtraction for a piece of a sequence, a
+// search in the staged member offsets for a group of short sequences (whose key rows are
+// its query rows). Rows past a tile's tokens are left as loaded; their scores are masked.
+
+struct RotJob {
+  uint8_t* tile;
+  uint64_t* full;
+  uint64_t* ready;
+  uint32_t phase;
+  uint32_t pos;
+  bool row_ok;
+  float mul;
+};
 
 template <bool BF16>
-__device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int s, int t) {
-  SlotBars& B = meta->bars[s];
-  uint32_t it = 0;
-  Ring q, k;
+__device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
+  Bars& B = meta->bars;
+  const int lane = t & 31;
+  const uint32_t tbl0 = smem_u32(smem + kOffTbl + t * 2 * kRowTblBytes);
+  const uint8_t* tblp = smem + kOffTbl + t * 2 * kRowTblBytes;
+  uint32_t it = 0, qn0 = 0, qn1 = 0;
+  Ring k;
   bool bad = false;
   for (;;) {
     const uint32_t mb = it & 1u;
     bad |= !wait_bar(meta, p.ctl, &B.item_full[mb], (it >> 1) & 1u, p.timeout_ns);
     bad = __any_sync(0xffffffffu, bad);
     if (bad) break;
-    const ItemBox bx = meta->box[s][mb];
+    const ItemBox& bx = meta->box[mb];
+    const bool valid = bx.valid != 0, has_b = bx.has_b != 0;
+    const TileRec ra = bx.a, rb = bx.b;
+    const Stream sm = stream_of(bx);
+    // stage the member offsets of A and B (a group needs them to find each row's sequence)
+    uint32_t* off_a = meta->cu_rot[mb][0];
+    uint32_t* off_b = meta->cu_rot[mb][1];
+    if (valid) {
+      stage_cu(p, ra, off_a, t, 128);
+      if (has_b) stage_cu(p, rb, off_b, t, 128);
+    }
     __syncwarp();
-    if ((t & 31) == 0) mbar_arrive(smem_u32(&B.item_empty[mb]));
+    if (lane == 0) {
+      mbar_arrive(smem_u32(&B.item_empty[mb]));
+      if (valid) mbar_arrive(smem_u32(&B.cu_rot[mb]));
+    }
     ++it;
-    if (!bx.valid) break;
-    const TileRec rec = bx.rec;
-    const uint32_t piece_start = __ldg(p.cu + rec.seq);
-    // positions of this thread's two query rows (for a group tile, also of its two key rows)
-    const uint32_t pos0 = t < static_cast<int>(rec.rows) ? position_of(p, rec, rec.q0 + t, piece_start) : 0u;
-    const uint32_t pos1 = t + 64 < static_cast<int>(rec.rows) ? position_of(p, rec, rec.q0 + t + 64, piece_start) : 0u;
+    if (!valid) break;
+    bad |= !wait_bar(meta, p.ctl, &B.cu_rot[mb], ((it - 1) >> 1) & 1u, p.timeout_ns);
+    bad = __any_sync(0xffffffffu, bad);
+    if (bad) break;
 
+    // positions of row t of Q_A and Q_B (for a group also of its key row t)
+    const bool qok_a = t < static_cast<int>(ra.rows);
+    const bool qok_b = has_b && t < static_cast<int>(rb.rows);
+    uint32_t qpos_a = 0u, qpos_b = 0u;
+    if (qok_a) {
+      uint32_t ss, se;
+      seq_bounds(p, ra, off_a, ra.q0 + t, ss, se);
+      qpos_a = ra.q0 + t - ss;
+    }
+    if (qok_b) {
+      uint32_t ss, se;
+      seq_bounds(p, rb, off_b, rb.q0 + t, ss, se);
+      qpos_b = rb.q0 + t - ss;
+    }
+    const uint32_t start_a = off_a[0], start_b = has_b ? off_b[0] : 0u;
+    const bool group_a = ra.kind != 0, group_b = rb.kind != 0;
+    const uint32_t nq = has_b ? 2u : 1u;
+    const uint32_t njobs = nq + sm.n;
+    const uint32_t kbase = k.n;
+
+    // job i: its tile, barriers and phase, and this thread's row position
+    auto job_of = [&](uint32_t i) -> RotJob {
+      RotJob jb;
+      if (i < nq) {
+        const bool xb = i == 1;
+        const uint32_t qn = xb ? qn1 : qn0;
+        const uint32_t qb = qn & 1u;
+        const int x = xb ? 1 : 0;
+        jb.tile = q_tile(smem, x, qb);
+        jb.full = &B.q_full[x][qb];
+        jb.ready = &B.q_ready[x][qb];
+        jb.phase = (qn >> 1) & 1u;
+        jb.pos = xb ? qpos_b : qpos_a;
+        jb.row_ok = xb ? qok_b : qok_a;
+        jb.mul = p.scale;
+      } else {
+        const uint32_t j = i - nq;
+        const StreamTile tile = stream_tile(sm, j);
+        const uint32_t kn = kbase + j;
+        const uint32_t st = kn % kKStages;
+        jb.tile = k_tile(smem, st);
+        jb.full = &B.k_full[st];
+        jb.ready = &B.k_ready[st];
+        jb.phase = (kn / kKStages) & 1u;
+        jb.row_ok = static_cast<uint32_t>(t) < tile.nkeys;
+        const bool group = tile.from_b ? group_b : group_a;
+        if (!jb.row_ok)
+          jb.pos = 0u;
+        else if (group)
+          jb.pos = tile.from_b ? qpos_b : qpos_a;  // a group's key rows are its query rows
+        else
+          jb.pos = tile.j0 + t - (tile.from_b ? start_b : start_a);
+        jb.mul = 1.0f;
+      }
+      return jb;
+    };
+
+    // job i's table rows go to buffer i & 1
+    {
+      const RotJob j0 = job_of(0);
+      if (j0.row_ok) fetch_table_row(p, tbl0, j0.pos, t);
+      cp_async_commit();
+      if (njobs > 1) {
+        const RotJob j1 = job_of(1);
+        if (j1.row_ok) fetch_table_row(p, tbl0 + kRowTblBytes, j1.pos, t);
+      }
+      cp_async_commit();
+    }
 #pragma unroll 1
-    for (uint32_t job = 0; job <= rec.ktiles; ++job) {
-      const bool isq = job == 0;
-      const uint32_t j = job - 1;
-      const uint32_t nrows = isq ? rec.rows : tile_keys(rec, j);
-      const uint32_t base = isq ? 0u : rec.k0 + j * kBC - piece_start;
-      const uint32_t st = isq ? q.stage(2) : k.stage(kKStages);
-      const uint32_t ph = isq ? q.phase(2) : k.phase(kKStages);
-      uint64_t* full = isq ? &B.q_full[st] : &B.k_full[st];
-      uint64_t* ready = isq ? &B.q_ready[st] : &B.k_ready[st];
-      uint8_t* tile = isq ? slot_q(smem, s, st) : slot_k(smem, s, st);
-      const float mul = isq ? p.scale : 1.0f;
-      // table positions of the two rows (row 0 of the tables for rows past the tile)
-      auto pos_of = [&](int r, uint32_t qp) -> uint32_t {
-        if (r >= static_cast<int>(nrows)) return 0u;
-        return (isq || rec.kind != 0) ? qp : base + r;
-      };
-      const uint32_t kp1 = pos_of(t + 64, pos1);
-      RopeRow cur = load_rope_row(p.cos_t, p.sin_t, pos_of(t, pos0));
-      bad |= !wait_bar(meta, p.ctl, full, ph, p.timeout_ns);
+    for (uint32_t i = 0; i < njobs; ++i) {
+      const RotJob jb = job_of(i);
+      cp_async_wait1();  // job i's rows have landed (job i + 1's may still be in flight)
+      bad |= !wait_bar(meta, p.ctl, jb.full, jb.phase, p.timeout_ns);
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
-#pragma unroll 1
-      for (int rr = 0; rr < 2; ++rr) {
-        const RopeRow nxt = load_rope_row(p.cos_t, p.sin_t, rr == 0 ? kp1 : 0u);
-        const int r = t + 64 * rr;
-        if (r < static_cast<int>(nrows)) rope_row_sw128<BF16>(tile, r, cur, mul);
-        cur = nxt;
-      }
+      if (jb.row_ok) rope_row<BF16>(jb.tile, t, tblp + (i & 1u) * kRowTblBytes, t, jb.mul);
       fence_proxy_async_smem();
       __syncwarp();
-      if ((t & 31) == 0) mbar_arrive(smem_u32(ready));
-      if (isq)
-        ++q.n;
-      else
-        ++k.n;
+      if (lane == 0) mbar_arrive(smem_u32(jb.ready));
+      // the buffer of job i is free: job i + 2's rows go there
+      if (i + 2 < njobs) {
+        const RotJob jn = job_of(i + 2);
+        if (jn.row_ok) fetch_table_row(p, tbl0 + (i & 1u) * kRowTblBytes, jn.pos, t);
+      }
+      cp_async_commit();
     }
+    cp_async_wait0();
     if (bad) break;
+    ++qn0;
+    if (has_b) ++qn1;
+    k.n += sm.n;
   }
-  if (bad && (t & 31) == 0) raise_abort(meta, p.ctl);
+  cp_async_wait0();
+  if (bad && lane == 0) raise_abort(meta, p.ctl);
 }
 
 // ------------------------------------------------------------------------------------
-// softmax warpgroup of one slot (128 threads; thread <-> query row <-> TMEM lane)
+// softmax warpgroup of query tile X (128 threads; thread <-> query row <-> TMEM lane)
 //
 // Each warp signals the MMA issuer on its own (barriers of count 4: after the warp's TMEM
 // accesses are fenced, lane 0 arrives), so warps never wait for one another; a failed wait
@@ -477,54 +704,71 @@ __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int s, int t
 // together.
 
 template <bool BF16>
-__device__ void softmax_wg(const Params& p, Meta* meta, int s, uint32_t tmem) {
-  SlotBars& B = meta->bars[s];
+__device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
+  Bars& B = meta->bars;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int r = (warp & 3) * 32 + lane;
   const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  const uint32_t tS = tmem + lane_addr + s * 256 + kColS;
-  const uint32_t tP = tmem + lane_addr + s * 256 + kColP;
-  const uint32_t tO = tmem + lane_addr + s * 256 + kColO;
+  const uint32_t tS = tmem + lane_addr + col_s(x);
+  const uint32_t tP = tmem + lane_addr + col_p(x);
+  const uint32_t tO = tmem + lane_addr + col_o(x);
   const int64_t hd = static_cast<int64_t>(p.H) * kD;
 
-  uint32_t it = 0, sf = 0, pvd = 0;
+  uint32_t it = 0, sf = 0, pvd = 0, used = 0;
   bool bad = false;
   for (;;) {
     const uint32_t mb = it & 1u;
     bad |= !wait_bar(meta, p.ctl, &B.item_full[mb], (it >> 1) & 1u, p.timeout_ns);
     bad = __any_sync(0xffffffffu, bad);
     if (bad) break;
-    const ItemBox bx = meta->box[s][mb];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&B.item_empty[mb]));
-    ++it;
-    if (!bx.valid) break;
-    const TileRec rec = bx.rec;
+    const ItemBox& bx = meta->box[mb];
+    const bool valid = bx.valid != 0;
+    const bool mine = valid && (x == 0 || bx.has_b);
+    const TileRec rec = x == 0 ? bx.a : bx.b;
     const int h = bx.head;
+    // this query tile's stream tiles [jlo, jhi): tile j holds keys [j0, j0 + nkeys) with
+    // j0 = kbase + 128 (j - jlo) and nkeys = min(128, kend - j0)
+    const uint32_t jlo = x == 0 ? 0u : bx.b0, jhi = x == 0 ? bx.a1 : bx.b1;
+    const uint32_t kbase = (x == 0 || bx.shared) ? bx.a.k0 + jlo * kBC : bx.b.k0;
+    const uint32_t kend = bx.shared ? bx.end : rec.k0 + rec.nk;
+    uint32_t* off = meta->cu_sm[x][used & 1u];
+    if (mine) stage_cu(p, rec, off, r, 128);
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(smem_u32(&B.item_empty[mb]));
+      if (mine) mbar_arrive(smem_u32(&B.cu_sm[x][used & 1u]));
+    }
+    ++it;
+    if (!valid) break;
+    if (!mine) continue;
+    bad |= !wait_bar(meta, p.ctl, &B.cu_sm[x][used & 1u], (used >> 1) & 1u, p.timeout_ns);
+    ++used;
+    bad = __any_sync(0xffffffffu, bad);
+    if (bad) break;
 
-    // this thread's query row and its visible key interval [lo, hi)
+    // this thread's query row and its visible key interval [lo, hi) (tokens < 2^31)
     const bool row_ok = r < static_cast<int>(rec.rows);
-    const uint32_t a = rec.q0 + r;
-    int64_t lo = 0, hi = 0;
+    const int a = static_cast<int>(rec.q0) + r;
+    int lo = 0, hi = 0;
     if (row_ok) {
-      const uint32_t sq = rec.kind == 0 ? rec.seq : seq_of_token(p.cu, rec.seq, rec.nseq, a);
-      const int64_t ss = __ldg(p.cu + sq), se = __ldg(p.cu + sq + 1);
-      lo = ss;
-      hi = se;
+      uint32_t ss, se;
+      seq_bounds(p, rec, off, static_cast<uint32_t>(a), ss, se);
+      lo = static_cast<int>(ss);
+      hi = static_cast<int>(se);
       if (p.window > 0) {
-        lo = max(ss, static_cast<int64_t>(a) - p.window);
-        hi = min(se, static_cast<int64_t>(a) + p.window + 1);
+        lo = max(lo, a - p.window);
+        hi = static_cast<int>(min(static_cast<int64_t>(hi), static_cast<int64_t>(a) + p.window + 1));
       }
     }
 
     float m_ref = kNeg, l = 0.f;
-    for (uint32_t j = 0; j < rec.ktiles; ++j) {
-      const uint32_t j0 = rec.k0 + j * kBC;
-      const uint32_t nkeys = tile_keys(rec, j);
+    for (uint32_t j = jlo; j < jhi; ++j) {
+      const int j0 = static_cast<int>(kbase + (j - jlo) * kBC);
+      const int nkeys = min(kBC, static_cast<int>(kend) - j0);
 
       // this row of S (columns past the tile's keys hold stale values; they are masked)
-      bad |= !wait_bar(meta, p.ctl, &B.s_full, sf & 1u, p.timeout_ns);
+      bad |= !wait_bar(meta, p.ctl, &B.s_full[x], sf & 1u, p.timeout_ns);
       ++sf;
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
@@ -534,13 +778,11 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int s, uint32_t tmem) {
       tmem_ld64(tS + 64, *reinterpret_cast<float(*)[64]>(sv + 64));
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&B.s_consumed));
+      if (lane == 0) mbar_arrive(smem_u32(&B.s_consumed[x]));
 
       // visible columns [c_lo, c_hi); every other column weighs zero
-      const int c_lo = static_cast<int>(
-          min(max(lo - static_cast<int64_t>(j0), static_cast<int64_t>(0)), static_cast<int64_t>(128)));
-      const int c_hi = static_cast<int>(
-          min(max(hi - static_cast<int64_t>(j0), static_cast<int64_t>(0)), static_cast<int64_t>(nkeys)));
+      const int c_lo = min(max(lo - j0, 0), 128);
+      const int c_hi = min(max(hi - j0, 0), nkeys);
       const bool full = __all_sync(0xffffffffu, c_lo == 0 && c_hi == 128);
       if (!full) {
 #pragma unroll
@@ -573,8 +815,8 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int s, uint32_t tmem) {
       uint32_t pp[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float2 x = __ffma2_rn(make_float2(sv[2 * c], sv[2 * c + 1]), c2, nm2);
-        const float2 e = make_float2(ex2(x.x), ex2(x.y));
+        const float2 xx = __ffma2_rn(make_float2(sv[2 * c], sv[2 * c + 1]), c2, nm2);
+        const float2 e = make_float2(ex2(xx.x), ex2(xx.y));
         acc[c & 3] = __fadd2_rn(acc[c & 3], e);
         pp[c] = Elem<BF16>::pack(e.x, e.y);
       }
@@ -582,8 +824,8 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int s, uint32_t tmem) {
       l += accs.x + accs.y;
 
       // once the previous PV has read P and written O: O rescale (rare), then P
-      if (j > 0) {
-        bad |= !wait_bar(meta, p.ctl, &B.pv_done, pvd & 1u, p.timeout_ns);
+      if (j > jlo) {
+        bad |= !wait_bar(meta, p.ctl, &B.pv_done[x], pvd & 1u, p.timeout_ns);
         ++pvd;
         bad = __any_sync(0xffffffffu, bad);
         if (bad) break;
@@ -605,12 +847,12 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int s, uint32_t tmem) {
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&B.p_ready));
+      if (lane == 0) mbar_arrive(smem_u32(&B.p_ready[x]));
     }
     if (bad) break;
 
     // epilogue: out = O / l, lse = m + ln l
-    bad |= !wait_bar(meta, p.ctl, &B.pv_done, pvd & 1u, p.timeout_ns);
+    bad |= !wait_bar(meta, p.ctl, &B.pv_done[x], pvd & 1u, p.timeout_ns);
     ++pvd;
     bad = __any_sync(0xffffffffu, bad);
     if (bad) break;
@@ -633,12 +875,11 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int s, uint32_t tmem) {
   if (bad && lane == 0) raise_abort(meta, p.ctl);
 }
 
-
 }  // namespace
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, Params p) {
+pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -648,30 +889,35 @@ pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, Params p) {
 
   if (tid == 0) {
     tma_prefetch_desc(&tmap_qkv);
-    for (int s = 0; s < kSlots; ++s) {
-      SlotBars& B = meta->bars[s];
-      for (int k = 0; k < 2; ++k) {
-        mbar_init(smem_u32(&B.item_full[k]), 1);
-        mbar_init(smem_u32(&B.item_empty[k]), kItemConsumers);
-        mbar_init(smem_u32(&B.q_full[k]), 1);
-        mbar_init(smem_u32(&B.q_ready[k]), kRotThreads / 32);
-        mbar_init(smem_u32(&B.q_empty[k]), 1);
+    Bars& B = meta->bars;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&B.item_full[i]), 1);
+      mbar_init(smem_u32(&B.item_empty[i]), kItemConsumers);
+      mbar_init(smem_u32(&B.cu_rot[i]), 4);
+      for (int x = 0; x < 2; ++x) {
+        mbar_init(smem_u32(&B.q_full[x][i]), 1);
+        mbar_init(smem_u32(&B.q_ready[x][i]), 4);
+        mbar_init(smem_u32(&B.q_empty[x][i]), 1);
+        mbar_init(smem_u32(&B.cu_sm[x][i]), 4);
       }
-      for (int k = 0; k < kKStages; ++k) {
-        mbar_init(smem_u32(&B.k_full[k]), 1);
-        mbar_init(smem_u32(&B.k_ready[k]), kRotThreads / 32);
-        mbar_init(smem_u32(&B.k_empty[k]), 1);
-      }
-      for (int k = 0; k < kVStages; ++k) {
-        mbar_init(smem_u32(&B.v_full[k]), 1);
-        mbar_init(smem_u32(&B.v_empty[k]), 1);
-      }
-      mbar_init(smem_u32(&B.s_full), 1);
-      mbar_init(smem_u32(&B.s_consumed), 4);
-      mbar_init(smem_u32(&B.p_ready), 4);
-      mbar_init(smem_u32(&B.pv_done), 1);
-      mbar_init(smem_u32(&B.drain), 1);
     }
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(smem_u32(&B.k_full[i]), 1);
+      mbar_init(smem_u32(&B.k_ready[i]), 4);
+      mbar_init(smem_u32(&B.k_empty[i]), 2);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(smem_u32(&B.v_full[i]), 1);
+      mbar_init(smem_u32(&B.v_empty[i]), 2);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&B.s_full[x]), 1);
+      mbar_init(smem_u32(&B.s_consumed[x]), 4);
+      mbar_init(smem_u32(&B.p_ready[x]), 4);
+      mbar_init(smem_u32(&B.pv_done[x]), 1);
+    }
+    mbar_init(smem_u32(&B.drain[0]), 1);
+    mbar_init(smem_u32(&B.drain[1]), 1);
     meta->abort = 0;
     fence_mbar_init();
   }
@@ -683,24 +929,23 @@ pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, Params p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = meta->tmem;
-  const unsigned int n_items = __ldcg(&p.ctl->ntiles) * static_cast<unsigned int>(p.H);
+  const unsigned int n_items = (__ldcg(&p.ctl->ntiles) + 1u) / 2u * static_cast<unsigned int>(p.H);
 
   // Register split (warpgroup-wide): the launch gives 512 x 128 = 65536 registers; the
-  // producer / MMA warpgroup drops to 48, the rotation warpgroup to 112, and the two softmax
-  // warpgroups rise to 168: 128 x 48 + 128 x 112 + 256 x 168 = 63488, within the launch.
+  // producer / MMA warpgroup drops to 80, the rotation warpgroup to 64, and the two softmax
+  // warpgroups rise to 184: 128 x 80 + 128 x 64 + 256 x 184 = 65536.
   if (warp < kWarpRot) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory");
-    if (warp < kWarpMma) {
-      if (lane == 0) producer(&tmap_qkv, p, smem, meta, warp, n_items);
-    } else {
-      if (lane == 0) mma_issuer(p, smem, meta, warp - kWarpMma, tmem, BF16);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    if (warp == kWarpProd) {
+      if (lane == 0) producer(&tmap_qkv, p, smem, meta, n_items);
+    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+      if (lane == 0) mma_issuer(p, smem, meta, tmem, BF16, warp - kWarpMma);
     }
   } else if (warp < kWarpSm) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
-    const int s = (warp - kWarpRot) >> 1;
-    rotator<BF16>(p, smem, meta, s, tid - (kWarpRot + 2 * s) * 32);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
+    rotator<BF16>(p, smem, meta, tid - kWarpRot * 32);
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
     softmax_wg<BF16>(p, meta, (warp - kWarpSm) >> 2, tmem);
   }
 
@@ -723,7 +968,7 @@ cudaError_t attend_tc_prepare() {
 }
 
 // Host side: one launch of `grid` persistent CTAs (one per SM: each holds all 512 TMEM
-// columns and about 225 KB of shared memory).
+// columns and about 210 KB of shared memory).
 cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
                              const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
                              long long T, int window, float scale, unsigned long long timeout_ns, int grid,
