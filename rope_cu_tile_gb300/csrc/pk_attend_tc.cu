@@ -302,7 +302,7 @@ __device__ __forceinline__ void rope_row(uint8_t* tile, int r, const uint8_t* tb
   using E = Elem<BF16>;
   uint8_t* row = tile + r * 128;
   const int sw = r & 7, tw = t & 7;
-#pragma unroll
+#pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     const uint4 x1 = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
     const uint4 x2 = *reinterpret_cast<const uint4*>(row + (((c + 4) ^ sw) << 4));
@@ -773,33 +773,37 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
       tc_fence_after();
-      float sv[128];
-      tmem_ld64(tS, *reinterpret_cast<float(*)[64]>(sv));
-      tmem_ld64(tS + 64, *reinterpret_cast<float(*)[64]>(sv + 64));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&B.s_consumed[x]));
 
       // visible columns [c_lo, c_hi); every other column weighs zero
       const int c_lo = min(max(lo - j0, 0), 128);
       const int c_hi = min(max(hi - j0, 0), nkeys);
       const bool full = __all_sync(0xffffffffu, c_lo == 0 && c_hi == 128);
-      if (!full) {
+
+      // Two passes over the row in halves of 64 columns, each reading its half from tensor
+      // memory (the loops stay rolled: a small code footprint for the warps that share an
+      // SM sub-partition). Pass 1: the row max.
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[64];
+        tmem_ld64(tS + 64 * hh, v);
+        if (!full) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c < c_lo || c >= c_hi) sv[c] = -INFINITY;
+          for (int c = 0; c < 64; ++c)
+            if (static_cast<unsigned>(c + 64 * hh - c_lo) >= static_cast<unsigned>(c_hi - c_lo)) v[c] = -INFINITY;
+        }
+        float mk[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mk[k] = fmax3(v[k], v[4 + k], v[8 + k]);
+#pragma unroll
+        for (int c = 12; c < 60; c += 8) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mk[k] = fmax3(mk[k], v[c + k], v[c + 4 + k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mk[k] = fmaxf(mk[k], v[60 + k]);
+        mx = fmax3(mx, fmax3(mk[0], mk[1], mk[2]), mk[3]);
       }
-      // row max: eight independent chains, then a tree
-      float mk[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mk[k] = fmax3(sv[k], sv[8 + k], sv[16 + k]);
-#pragma unroll
-      for (int c = 24; c < 128; c += 16) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mk[k] = (c + 8 + k < 128) ? fmax3(mk[k], sv[c + k], sv[c + 8 + k]) : fmaxf(mk[k], sv[c + k]);
-      }
-      const float mx = fmaxf(fmax3(mk[0], mk[1], mk[2]), fmax3(fmax3(mk[3], mk[4], mk[5]), mk[6], mk[7]));
       const float m_new = fmaxf(m_ref, mx);
       const bool grow = (m_new - m_ref) * kLog2e > kRescale;
       float alpha = 1.f;
@@ -811,39 +815,59 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
       const float mb2 = m_ref * kLog2e;
       const float2 c2 = make_float2(kLog2e, kLog2e);
       const float2 nm2 = make_float2(-mb2, -mb2);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t pp[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float2 xx = __ffma2_rn(make_float2(sv[2 * c], sv[2 * c + 1]), c2, nm2);
-        const float2 e = make_float2(ex2(xx.x), ex2(xx.y));
-        acc[c & 3] = __fadd2_rn(acc[c & 3], e);
-        pp[c] = Elem<BF16>::pack(e.x, e.y);
-      }
-      const float2 accs = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-      l += accs.x + accs.y;
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 
-      // once the previous PV has read P and written O: O rescale (rare), then P
-      if (j > jlo) {
-        bad |= !wait_bar(meta, p.ctl, &B.pv_done[x], pvd & 1u, p.timeout_ns);
-        ++pvd;
-        bad = __any_sync(0xffffffffu, bad);
-        if (bad) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, grow)) {
+      // Pass 2: probabilities of each half, written to P (the first once the previous PV
+      // has read P and written O, after the O rescale that a grown max asks for).
 #pragma unroll 1
-          for (int hh = 0; hh < 2; ++hh) {
-            float ov[32];
-            tmem_ld32(tO + 32 * hh, ov);
-            uint32_t ou[32];
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[64];
+        tmem_ld64(tS + 64 * hh, v);
+        if (hh == 1) {
+          // every S column of this tile is read: the next S may be issued
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&B.s_consumed[x]));
+        }
+        if (!full) {
 #pragma unroll
-            for (int d = 0; d < 32; ++d) ou[d] = __float_as_uint(ov[d] * alpha);
-            tmem_st32(tO + 32 * hh, ou);
+          for (int c = 0; c < 64; ++c)
+            if (static_cast<unsigned>(c + 64 * hh - c_lo) >= static_cast<unsigned>(c_hi - c_lo)) v[c] = -INFINITY;
+        }
+        uint32_t pp[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float2 xx = __ffma2_rn(make_float2(v[2 * c], v[2 * c + 1]), c2, nm2);
+          const float2 e = make_float2(ex2(xx.x), ex2(xx.y));
+          if (c & 1)
+            acc1 = __fadd2_rn(acc1, e);
+          else
+            acc0 = __fadd2_rn(acc0, e);
+          pp[c] = Elem<BF16>::pack(e.x, e.y);
+        }
+        if (hh == 0 && j > jlo) {
+          bad |= !wait_bar(meta, p.ctl, &B.pv_done[x], pvd & 1u, p.timeout_ns);
+          ++pvd;
+          bad = __any_sync(0xffffffffu, bad);
+          if (bad) break;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+            for (int oh = 0; oh < 2; ++oh) {
+              float ov[32];
+              tmem_ld32(tO + 32 * oh, ov);
+              uint32_t ou[32];
+#pragma unroll
+              for (int d = 0; d < 32; ++d) ou[d] = __float_as_uint(ov[d] * alpha);
+              tmem_st32(tO + 32 * oh, ou);
+            }
           }
         }
+        tmem_st32(tP + 32 * hh, pp);
       }
-      tmem_st32(tP, pp);
-      tmem_st32(tP + 32, pp + 32);
+      if (bad) break;
+      const float2 accs = __fadd2_rn(acc0, acc1);
+      l += accs.x + accs.y;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
