@@ -223,7 +223,8 @@ struct Params {
   int H;
   long long T;
   int window;
-  float scale;
+  float q_mul;  // multiplies the rotated q (the scale when it is not positive, else 1)
+  float s_mul;  // multiplies the scores in the softmax (the scale when it is positive, else 1)
   unsigned long long timeout_ns;
 };
 
@@ -293,13 +294,44 @@ __device__ __forceinline__ void fetch_table_row(const Params& p, uint32_t buf, u
   }
 }
 
-// Rotate and multiply by `mul` row r of a 128-byte-swizzled 64-column tile in place:
-// y[u] = x[u] c - x[u+32] s, y[u+32] = x[u] s + x[u+32] c, in fp32 straight from the 16-bit
-// operands. Elements u and u + 32 are logical 16-byte chunks c and c + 4, stored at chunks
-// (c ^ (r & 7)) and ((c + 4) ^ (r & 7)); the table row is in `tbl` as fetch_table_row left it.
+// Rotation of one 16-byte chunk pair: x1 holds elements u .. u+7 of the first half of a
+// row, x2 the matching elements u+32 .. u+39, tc / ts the cos / sin table values of the
+// same u; y1 = x1 c - x2 s, y2 = x1 s + x2 c in fp32 from the 16-bit operands, times `mul`
+// when SCALED.
+template <bool BF16, bool SCALED>
+__device__ __forceinline__ void rope_chunk(const uint4& x1, const uint4& x2, const uint4& tc, const uint4& ts,
+                                           float mul, uint4& y1o, uint4& y2o) {
+  using E = Elem<BF16>;
+  const uint32_t a[4] = {x1.x, x1.y, x1.z, x1.w};
+  const uint32_t b[4] = {x2.x, x2.y, x2.z, x2.w};
+  const uint32_t cc[4] = {tc.x, tc.y, tc.z, tc.w};
+  const uint32_t ss[4] = {ts.x, ts.y, ts.z, ts.w};
+  uint32_t y1[4], y2[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float lo1 = E::fma_lo(a[k], cc[k], -E::fma_lo(b[k], ss[k], 0.f));
+    float hi1 = E::fma_hi(a[k], cc[k], -E::fma_hi(b[k], ss[k], 0.f));
+    float lo2 = E::fma_lo(a[k], ss[k], E::fma_lo(b[k], cc[k], 0.f));
+    float hi2 = E::fma_hi(a[k], ss[k], E::fma_hi(b[k], cc[k], 0.f));
+    if (SCALED) {
+      lo1 *= mul;
+      hi1 *= mul;
+      lo2 *= mul;
+      hi2 *= mul;
+    }
+    y1[k] = E::pack(lo1, hi1);
+    y2[k] = E::pack(lo2, hi2);
+  }
+  y1o = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+  y2o = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+}
+
+// Rotate (and multiply by `mul` unless it is 1) row r of a 128-byte-swizzled 64-column tile
+// in place. Elements u and u + 32 are logical 16-byte chunks c and c + 4, stored at chunks
+// (c ^ (r & 7)) and ((c + 4) ^ (r & 7)); the table row is in `tbl` as fetch_table_row left
+// it. Two chunk pairs per step, all their loads issued before the arithmetic.
 template <bool BF16>
 __device__ __forceinline__ void rope_row(uint8_t* tile, int r, const uint8_t* tbl, int t, float mul) {
-  using E = Elem<BF16>;
   uint8_t* row = tile + r * 128;
   const int sw = r & 7, tw = t & 7;
 #pragma unroll 1
@@ -308,22 +340,13 @@ __device__ __forceinline__ void rope_row(uint8_t* tile, int r, const uint8_t* tb
     const uint4 x2 = *reinterpret_cast<const uint4*>(row + (((c + 4) ^ sw) << 4));
     const uint4 tc = *reinterpret_cast<const uint4*>(tbl + ((c ^ tw) << 4));
     const uint4 ts = *reinterpret_cast<const uint4*>(tbl + (((c + 4) ^ tw) << 4));
-    const uint32_t a[4] = {x1.x, x1.y, x1.z, x1.w};
-    const uint32_t b[4] = {x2.x, x2.y, x2.z, x2.w};
-    const uint32_t cc[4] = {tc.x, tc.y, tc.z, tc.w};
-    const uint32_t ss[4] = {ts.x, ts.y, ts.z, ts.w};
-    uint32_t y1[4], y2[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float lo1 = E::fma_lo(a[k], cc[k], -E::fma_lo(b[k], ss[k], 0.f));
-      const float hi1 = E::fma_hi(a[k], cc[k], -E::fma_hi(b[k], ss[k], 0.f));
-      const float lo2 = E::fma_lo(a[k], ss[k], E::fma_lo(b[k], cc[k], 0.f));
-      const float hi2 = E::fma_hi(a[k], ss[k], E::fma_hi(b[k], cc[k], 0.f));
-      y1[k] = E::pack(lo1 * mul, hi1 * mul);
-      y2[k] = E::pack(lo2 * mul, hi2 * mul);
-    }
-    *reinterpret_cast<uint4*>(row + ((c ^ sw) << 4)) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
-    *reinterpret_cast<uint4*>(row + (((c + 4) ^ sw) << 4)) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+    uint4 y1, y2;
+    if (mul == 1.0f)
+      rope_chunk<BF16, false>(x1, x2, tc, ts, mul, y1, y2);
+    else
+      rope_chunk<BF16, true>(x1, x2, tc, ts, mul, y1, y2);
+    *reinterpret_cast<uint4*>(row + ((c ^ sw) << 4)) = y1;
+    *reinterpret_cast<uint4*>(row + (((c + 4) ^ sw) << 4)) = y2;
   }
 }
 
@@ -633,7 +656,7 @@ __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
         jb.phase = (qn >> 1) & 1u;
         jb.pos = xb ? qpos_b : qpos_a;
         jb.row_ok = xb ? qok_b : qok_a;
-        jb.mul = p.scale;
+        jb.mul = p.q_mul;
       } else {
         const uint32_t j = i - nq;
         const StreamTile tile = stream_tile(sm, j);
@@ -714,6 +737,8 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
   const uint32_t tP = tmem + lane_addr + col_p(x);
   const uint32_t tO = tmem + lane_addr + col_o(x);
   const int64_t hd = static_cast<int64_t>(p.H) * kD;
+  // raw scores s weigh ex2(s k2 - m k2): k2 folds the score scale into the base change
+  const float k2 = p.s_mul * kLog2e;
 
   uint32_t it = 0, sf = 0, pvd = 0, used = 0;
   bool bad = false;
@@ -762,7 +787,7 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
       }
     }
 
-    float m_ref = kNeg, l = 0.f;
+    float m_ref = kNeg, l = 0.f;  // running max of the raw scores, and the row sum
     for (uint32_t j = jlo; j < jhi; ++j) {
       const int j0 = static_cast<int>(kbase + (j - jlo) * kBC);
       const int nkeys = min(kBC, static_cast<int>(kend) - j0);
@@ -805,15 +830,15 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
         mx = fmax3(mx, fmax3(mk[0], mk[1], mk[2]), mk[3]);
       }
       const float m_new = fmaxf(m_ref, mx);
-      const bool grow = (m_new - m_ref) * kLog2e > kRescale;
+      const bool grow = (m_new - m_ref) * k2 > kRescale;
       float alpha = 1.f;
       if (grow) {
-        alpha = ex2((m_ref - m_new) * kLog2e);
+        alpha = ex2((m_ref - m_new) * k2);
         l *= alpha;
         m_ref = m_new;
       }
-      const float mb2 = m_ref * kLog2e;
-      const float2 c2 = make_float2(kLog2e, kLog2e);
+      const float mb2 = m_ref * k2;
+      const float2 c2 = make_float2(k2, k2);
       const float2 nm2 = make_float2(-mb2, -mb2);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 
@@ -893,7 +918,7 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
                             Elem<BF16>::pack(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv),
                             Elem<BF16>::pack(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
                             Elem<BF16>::pack(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
-      p.lse[static_cast<int64_t>(h) * p.T + a] = m_ref + lg2(l) * kLn2;
+      p.lse[static_cast<int64_t>(h) * p.T + a] = (m_ref * k2 + lg2(l)) * kLn2;
     }
   }
   if (bad && lane == 0) raise_abort(meta, p.ctl);
@@ -1008,7 +1033,10 @@ cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos
   p.H = H;
   p.T = T;
   p.window = window;
-  p.scale = scale;
+  // a positive scale is applied to the scores in the softmax (the row max of the raw
+  // scores is then the max of the scaled ones); any other scale multiplies q
+  p.q_mul = scale > 0.0f ? 1.0f : scale;
+  p.s_mul = scale > 0.0f ? scale : 1.0f;
   p.timeout_ns = timeout_ns;
   const uint32_t smem = attend_tc_smem_bytes();
   if (bf16)
