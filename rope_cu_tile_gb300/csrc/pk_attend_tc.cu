@@ -977,32 +977,33 @@ pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_c
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = meta->tmem;
-  const unsigned int n_items = (__ldcg(&p.ctl->ntiles) + 1u) / 2u * static_cast<unsigned int>(p.H);
 
   // Register split (warpgroup-wide): the launch gives 512 x 128 = 65536 registers; the
   // producer / MMA warpgroup drops to 80, the rotation warpgroup to 64, and the two softmax
   // warpgroups rise to 184: 128 x 80 + 128 x 64 + 256 x 184 = 65536.
   if (warp < kWarpRot) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    // (each role reads what it needs after its own register change: nothing computed
+    // before the split stays live across it)
     if (warp == kWarpProd) {
-      if (lane == 0) producer(&tmap_qkv, p, smem, meta, n_items);
+      if (lane == 0)
+        producer(&tmap_qkv, p, smem, meta, (__ldcg(&p.ctl->ntiles) + 1u) / 2u * static_cast<unsigned int>(p.H));
     } else if (warp == kWarpMma || warp == kWarpMma + 1) {
-      if (lane == 0) mma_issuer(p, smem, meta, tmem, BF16, warp - kWarpMma);
+      if (lane == 0) mma_issuer(p, smem, meta, meta->tmem, BF16, warp - kWarpMma);
     }
   } else if (warp < kWarpSm) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
     rotator<BF16>(p, smem, meta, tid - kWarpRot * 32);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
-    softmax_wg<BF16>(p, meta, (warp - kWarpSm) >> 2, tmem);
+    softmax_wg<BF16>(p, meta, (warp - kWarpSm) >> 2, meta->tmem);
   }
 
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(meta->tmem, kTmemCols);
   }
 }
 
