@@ -986,8 +986,11 @@ pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_c
     // (each role reads what it needs after its own register change: nothing computed
     // before the split stays live across it)
     if (warp == kWarpProd) {
-      if (lane == 0)
+      if (lane == 0) {
+        // the records and the work counter come from the scheduler launched just before
+        griddep_wait();
         producer(&tmap_qkv, p, smem, meta, (__ldcg(&p.ctl->ntiles) + 1u) / 2u * static_cast<unsigned int>(p.H));
+      }
     } else if (warp == kWarpMma || warp == kWarpMma + 1) {
       if (lane == 0) mma_issuer(p, smem, meta, meta->tmem, BF16, warp - kWarpMma);
     }
@@ -1013,8 +1016,15 @@ uint32_t attend_tc_smem_bytes() { return kSmemUsed + 1024; }
 cudaError_t attend_tc_prepare() {
   const int smem = static_cast<int>(attend_tc_smem_bytes());
   cudaError_t e = cudaFuncSetAttribute(pk_attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(pk_attend_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pk_attend_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pk_attend_tc_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pk_attend_tc_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
 }
 
 // Host side: one launch of `grid` persistent CTAs (one per SM: each holds all 512 TMEM
@@ -1039,12 +1049,20 @@ cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos
   p.q_mul = scale > 0.0f ? 1.0f : scale;
   p.s_mul = scale > 0.0f ? scale : 1.0f;
   p.timeout_ns = timeout_ns;
-  const uint32_t smem = attend_tc_smem_bytes();
-  if (bf16)
-    pk_attend_tc_kernel<true><<<grid, kThreads, smem, stream>>>(tmap, p);
-  else
-    pk_attend_tc_kernel<false><<<grid, kThreads, smem, stream>>>(tmap, p);
-  return cudaGetLastError();
+  // programmatic stream serialization: the CTAs set up (barriers, tensor memory) while the
+  // scheduler finishes; the producer waits for the scheduler before it reads the records
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = attend_tc_smem_bytes();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (bf16) return cudaLaunchKernelEx(&cfg, pk_attend_tc_kernel<true>, tmap, p);
+  return cudaLaunchKernelEx(&cfg, pk_attend_tc_kernel<false>, tmap, p);
 }
 
 }  // namespace pk

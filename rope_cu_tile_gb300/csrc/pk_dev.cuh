@@ -52,6 +52,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start while the previous kernel of the stream runs; griddep_wait blocks until that
+// kernel has completed and its memory operations are visible (a no-op without a
+// dependency). griddep_launch_dependents lets the next kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -18,6 +18,7 @@ namespace pk {
 cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, TileRec* tiles, long long cap,
                             Ctl* ctl, cudaStream_t stream);
 cudaError_t attend_tc_prepare();
+cudaError_t schedule_prepare();
 cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
                              const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
                              long long T, int window, float scale, unsigned long long timeout_ns, int grid,
@@ -99,7 +100,7 @@ int device_info(int dev, DeviceInfo** out) {
   }
   if (!di.supported) return PK_ERR_UNSUPPORTED;
   if (!di.attrs_set) {
-    if (attend_tc_prepare() != cudaSuccess) return PK_ERR_CUDA;
+    if (attend_tc_prepare() != cudaSuccess || schedule_prepare() != cudaSuccess) return PK_ERR_CUDA;
     di.attrs_set = true;
   }
   *out = &di;

@@ -31,6 +31,7 @@ namespace pk {
 cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, TileRec* tiles, long long cap,
                             Ctl* ctl, cudaStream_t stream);
 cudaError_t attend_tc_prepare();
+cudaError_t schedule_prepare();
 cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
                              const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
                              long long T, int window, float scale, unsigned long long timeout_ns, int grid,
@@ -75,7 +76,7 @@ int setup_device(int dev, Setup** out) {
     s.supported = prop.major == 10 && prop.minor == 3;
     s.sms = prop.multiProcessorCount;
     if (s.supported) {
-      if (attend_tc_prepare() != cudaSuccess) return PK_ERR_CUDA;
+      if (attend_tc_prepare() != cudaSuccess || schedule_prepare() != cudaSuccess) return PK_ERR_CUDA;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PK_ERR_CUDA;
       s.scratch = static_cast<unsigned char*>(p);

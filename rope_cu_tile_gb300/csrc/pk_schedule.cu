@@ -15,8 +15,8 @@
 // (i) a piece of the long sequence that covers the granule's first token, (ii) the group
 // of short sequences starting in it, (iii) the first piece of a long sequence starting in
 // it (a long sequence starting in a granule is the last one starting there, since it runs
-// past the granule's end). One block of threads takes contiguous runs of granules, counts,
-// scans, then writes.
+// past the granule's end). One block of threads stages cu in shared memory (when it fits),
+// takes contiguous runs of granules, counts, scans, then writes.
 #include "pk_dev.cuh"
 
 namespace pk {
@@ -24,16 +24,21 @@ namespace pk {
 namespace {
 
 constexpr int kSchedThreads = 1024;
+// cu is staged in shared memory when it has at most this many entries (192 KB); longer lists
+// are searched in global memory
+constexpr int kStageMax = 48 * 1024;
 
-struct GranuleTiles {
-  int n;
-  TileRec rec[3];
+// cu as the caller's array in global memory (read-only path)
+struct GlobalCu {
+  const uint32_t* p;
 };
-
-__device__ __forceinline__ uint32_t ld_cu(const uint32_t* cu, uint32_t i) { return __ldg(cu + i); }
+__device__ __forceinline__ uint32_t ld_cu(GlobalCu cu, uint32_t i) { return __ldg(cu.p + i); }
+// cu as the staged copy in shared memory
+__device__ __forceinline__ uint32_t ld_cu(const uint32_t* cu, uint32_t i) { return cu[i]; }
 
 // first index s in [0, n) with cu[s] >= v, or n
-__device__ __forceinline__ uint32_t lower_bound_cu(const uint32_t* cu, uint32_t n, uint64_t v) {
+template <class CuPtr>
+__device__ __forceinline__ uint32_t lower_bound_cu(CuPtr cu, uint32_t n, uint64_t v) {
   uint32_t lo = 0, hi = n;
   while (lo < hi) {
     const uint32_t mid = (lo + hi) >> 1;
@@ -43,7 +48,8 @@ __device__ __forceinline__ uint32_t lower_bound_cu(const uint32_t* cu, uint32_t 
 }
 
 // first index s in [0, n) with cu[s] > v, or n
-__device__ __forceinline__ uint32_t upper_bound_cu(const uint32_t* cu, uint32_t n, uint64_t v) {
+template <class CuPtr>
+__device__ __forceinline__ uint32_t upper_bound_cu(CuPtr cu, uint32_t n, uint64_t v) {
   uint32_t lo = 0, hi = n;
   while (lo < hi) {
     const uint32_t mid = (lo + hi) >> 1;
@@ -52,7 +58,8 @@ __device__ __forceinline__ uint32_t upper_bound_cu(const uint32_t* cu, uint32_t 
   return lo;
 }
 
-__device__ __forceinline__ TileRec piece(const uint32_t* cu, uint32_t s, uint32_t i0, int window) {
+template <class CuPtr>
+__device__ __forceinline__ TileRec piece(CuPtr cu, uint32_t s, uint32_t i0, int window) {
   const uint32_t start = ld_cu(cu, s), end = ld_cu(cu, s + 1);
   const uint32_t L = end - start;
   TileRec r;
@@ -73,11 +80,10 @@ __device__ __forceinline__ TileRec piece(const uint32_t* cu, uint32_t s, uint32_
   return r;
 }
 
-// The records whose first query token falls in granule b, in increasing q0.
-__device__ GranuleTiles granule_tiles(const uint32_t* cu, uint32_t S, uint64_t T, int window,
-                                      uint64_t b) {
-  GranuleTiles g;
-  g.n = 0;
+// Calls emit(record) for each record whose first query token falls in granule b, in
+// increasing q0 (at most three; no array, so nothing goes to local memory).
+template <class CuPtr, class Emit>
+__device__ __forceinline__ void granule_visit(CuPtr cu, uint32_t S, int window, uint64_t b, Emit&& emit) {
   const uint64_t G0 = b * kGrain, G1 = G0 + kGrain;
   // (i) the sequence holding token G0, if it started earlier and is long
   {
@@ -86,7 +92,7 @@ __device__ GranuleTiles granule_tiles(const uint32_t* cu, uint32_t S, uint64_t T
       const uint64_t start = ld_cu(cu, sc), end = ld_cu(cu, sc + 1);
       if (start < G0 && end - start > static_cast<uint64_t>(kShort)) {
         const uint64_t i0 = ((G0 - start + kBR - 1) / kBR) * kBR;
-        if (start + i0 < end && start + i0 < G1) g.rec[g.n++] = piece(cu, sc, static_cast<uint32_t>(i0), window);
+        if (start + i0 < end && start + i0 < G1) emit(piece(cu, sc, static_cast<uint32_t>(i0), window));
       }
     }
   }
@@ -110,44 +116,25 @@ __device__ GranuleTiles granule_tiles(const uint32_t* cu, uint32_t S, uint64_t T
         r.nseq = m_end - s_lo;
         r.kind = 1;
         r.ktiles = (rows + kBC - 1) / kBC;
-        g.rec[g.n++] = r;
+        emit(r);
       }
     }
-    if (last_long) g.rec[g.n++] = piece(cu, last, 0, window);
+    if (last_long) emit(piece(cu, last, 0, window));
   }
-  (void)T;
-  return g;
 }
 
-}  // namespace
-
-__global__ void __launch_bounds__(kSchedThreads)
-pk_schedule_kernel(const uint32_t* __restrict__ cu, int S, long long T, int window,
-                   TileRec* __restrict__ tiles, long long cap, Ctl* ctl) {
-  __shared__ int s_bad;
-  __shared__ uint32_t s_warp[kSchedThreads / 32];
+// Count, scan and write the records, reading cu through `cu` (the staged shared copy or the
+// caller's array; the body is instantiated for each so that loads use their own space).
+template <class CuPtr>
+__device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int window, TileRec* __restrict__ tiles,
+                                              long long cap, Ctl* ctl, uint32_t* s_warp) {
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
-  if (tid == 0) {
-    s_bad = (ld_cu(cu, 0) != 0u) || (static_cast<long long>(ld_cu(cu, S)) != T);
-  }
-  __syncthreads();
-  for (int s = tid; s < S; s += nthr)
-    if (ld_cu(cu, s + 1) < ld_cu(cu, s)) s_bad = 1;
-  __syncthreads();
-  if (s_bad) {
-    if (tid == 0) {
-      ctl->ntiles = 0;
-      ctl->next = 0;
-      set_status(ctl, kErrBadCu);
-    }
-    return;
-  }
   const uint64_t NB = (static_cast<uint64_t>(T) + kGrain - 1) / kGrain;
   const uint64_t per = (NB + nthr - 1) / nthr;
   const uint64_t b0 = min(NB, per * tid), b1 = min(NB, b0 + per);
   uint32_t count = 0;
-  for (uint64_t b = b0; b < b1; ++b) count += granule_tiles(cu, S, T, window, b).n;
+  for (uint64_t b = b0; b < b1; ++b) granule_visit(cu, S, window, b, [&](const TileRec&) { ++count; });
 
   // exclusive scan of the per-thread counts
   const int lane = tid & 31, warp = tid >> 5;
@@ -174,11 +161,15 @@ pk_schedule_kernel(const uint32_t* __restrict__ cu, int S, long long T, int wind
   const uint32_t total = s_warp[nthr / 32 - 1];
 
   uint32_t at = base;
-  for (uint64_t b = b0; b < b1; ++b) {
-    const GranuleTiles g = granule_tiles(cu, S, T, window, b);
-    for (int k = 0; k < g.n; ++k, ++at)
-      if (at < static_cast<uint64_t>(cap)) tiles[at] = g.rec[k];
-  }
+  for (uint64_t b = b0; b < b1; ++b)
+    granule_visit(cu, S, window, b, [&](const TileRec& r) {
+      if (at < static_cast<uint64_t>(cap)) {
+        uint4* d = reinterpret_cast<uint4*>(tiles + at);
+        d[0] = make_uint4(r.q0, r.rows, r.k0, r.nk);
+        d[1] = make_uint4(r.seq, r.nseq, r.kind, r.ktiles);
+      }
+      ++at;
+    });
   if (tid == 0) {
     if (total > static_cast<uint64_t>(cap)) {
       ctl->ntiles = 0;
@@ -190,9 +181,62 @@ pk_schedule_kernel(const uint32_t* __restrict__ cu, int S, long long T, int wind
   }
 }
 
+}  // namespace
+
+__global__ void __launch_bounds__(kSchedThreads)
+pk_schedule_kernel(const uint32_t* __restrict__ cu_g, int S, long long T, int window,
+                   TileRec* __restrict__ tiles, long long cap, Ctl* ctl) {
+  extern __shared__ uint32_t s_cu[];
+  __shared__ int s_bad;
+  __shared__ uint32_t s_warp[kSchedThreads / 32];
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  // the attention kernel may start its set-up now; it reads the records only after this
+  // grid has completed (griddep_wait)
+  griddep_launch_dependents();
+  const bool staged = S + 1 <= kStageMax;
+  if (tid == 0) s_bad = 0;
+  if (staged) {
+    for (int s = tid; s <= S; s += nthr) s_cu[s] = __ldg(cu_g + s);
+    __syncthreads();
+    if (tid == 0 && (s_cu[0] != 0u || static_cast<long long>(s_cu[S]) != T)) s_bad = 1;
+    for (int s = tid; s < S; s += nthr)
+      if (s_cu[s + 1] < s_cu[s]) s_bad = 1;
+  } else {
+    __syncthreads();
+    if (tid == 0 && (__ldg(cu_g) != 0u || static_cast<long long>(__ldg(cu_g + S)) != T)) s_bad = 1;
+    for (int s = tid; s < S; s += nthr)
+      if (__ldg(cu_g + s + 1) < __ldg(cu_g + s)) s_bad = 1;
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) {
+      ctl->ntiles = 0;
+      ctl->next = 0;
+      set_status(ctl, kErrBadCu);
+    }
+    return;
+  }
+  if (staged)
+    schedule_body(static_cast<const uint32_t*>(s_cu), S, T, window, tiles, cap, ctl, s_warp);
+  else
+    schedule_body(GlobalCu{cu_g}, S, T, window, tiles, cap, ctl, s_warp);
+}
+
+// The carve-out matches the attention kernel's (all shared memory), so that the SMs need
+// no reconfiguration between the two kernels of a call.
+cudaError_t schedule_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(pk_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kStageMax * static_cast<int>(sizeof(uint32_t)));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(pk_schedule_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, TileRec* tiles, long long cap,
                             Ctl* ctl, cudaStream_t stream) {
-  pk_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(cu, S, T, window, tiles, cap, ctl);
+  const size_t smem = S + 1 <= kStageMax ? static_cast<size_t>(S + 1) * sizeof(uint32_t) : 0;
+  pk_schedule_kernel<<<1, kSchedThreads, smem, stream>>>(cu, S, T, window, tiles, cap, ctl);
   return cudaGetLastError();
 }
 
