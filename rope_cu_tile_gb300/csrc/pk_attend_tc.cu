@@ -40,7 +40,7 @@ namespace pk {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kKStages = 4;
+constexpr int kKStages = 4;  // a power of two (the rotation warps step the stage with a mask)
 constexpr int kVStages = 3;
 constexpr int kWarpProd = 0;
 constexpr int kWarpMma = 1;  // warps 1 (A), 2 (B)
@@ -570,21 +570,14 @@ __device__ void mma_issuer(const Params& p, uint8_t* smem, Meta* meta, uint32_t 
 // ------------------------------------------------------------------------------------
 // rotation warpgroup (128 threads; thread t rotates row t of every tile)
 //
-// Jobs of an item, in order: Q_A, Q_B (when B is a record), then K(0) .. K(n - 1). The
-// table rows of job i + 1 are in flight (cp.async) while job i is rotated. A row's position
-// is its token minus the start of its sequence: one subtraction for a piece of a sequence, a
-// search in the staged member offsets for a group of short sequences (whose key rows are
-// its query rows). Rows past a tile's tokens are left as loaded; their scores are masked.
-
-struct RotJob {
-  uint8_t* tile;
-  uint64_t* full;
-  uint64_t* ready;
-  uint32_t phase;
-  uint32_t pos;
-  bool row_ok;
-  float mul;
-};
+// Per item: Q_A, Q_B (when B is a record), then the key stream K(0) .. K(n - 1), each as
+// soon as it lands. A row's position is its token minus the start of its sequence: one
+// subtraction for a piece of a sequence, a search in the staged member offsets for a group
+// of short sequences (whose key rows are its query rows). The table rows of the next job
+// are in flight (cp.async) while the current one is rotated. Ring stage, phase and
+// positions advance step by step: the per-job bookkeeping is a few instructions, since this
+// warpgroup's time goes into dependent chains. Rows past a tile's tokens are left as
+// loaded; their scores are masked.
 
 template <bool BF16>
 __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
@@ -593,7 +586,8 @@ __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
   const uint32_t tbl0 = smem_u32(smem + kOffTbl + t * 2 * kRowTblBytes);
   const uint8_t* tblp = smem + kOffTbl + t * 2 * kRowTblBytes;
   uint32_t it = 0, qn0 = 0, qn1 = 0;
-  Ring k;
+  uint32_t kst = 0, kph = 0;  // K ring stage and phase of the next K tile
+  uint32_t buf = 0;           // table buffer of the next job
   bool bad = false;
   for (;;) {
     const uint32_t mb = it & 1u;
@@ -636,83 +630,93 @@ __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
       seq_bounds(p, rb, off_b, rb.q0 + t, ss, se);
       qpos_b = rb.q0 + t - ss;
     }
-    const uint32_t start_a = off_a[0], start_b = has_b ? off_b[0] : 0u;
-    const bool group_a = ra.kind != 0, group_b = rb.kind != 0;
-    const uint32_t nq = has_b ? 2u : 1u;
-    const uint32_t njobs = nq + sm.n;
-    const uint32_t kbase = k.n;
 
-    // job i: its tile, barriers and phase, and this thread's row position
-    auto job_of = [&](uint32_t i) -> RotJob {
-      RotJob jb;
-      if (i < nq) {
-        const bool xb = i == 1;
-        const uint32_t qn = xb ? qn1 : qn0;
-        const uint32_t qb = qn & 1u;
-        const int x = xb ? 1 : 0;
-        jb.tile = q_tile(smem, x, qb);
-        jb.full = &B.q_full[x][qb];
-        jb.ready = &B.q_ready[x][qb];
-        jb.phase = (qn >> 1) & 1u;
-        jb.pos = xb ? qpos_b : qpos_a;
-        jb.row_ok = xb ? qok_b : qok_a;
-        jb.mul = p.q_mul;
-      } else {
-        const uint32_t j = i - nq;
-        const StreamTile tile = stream_tile(sm, j);
-        const uint32_t kn = kbase + j;
-        const uint32_t st = kn % kKStages;
-        jb.tile = k_tile(smem, st);
-        jb.full = &B.k_full[st];
-        jb.ready = &B.k_ready[st];
-        jb.phase = (kn / kKStages) & 1u;
-        jb.row_ok = static_cast<uint32_t>(t) < tile.nkeys;
-        const bool group = tile.from_b ? group_b : group_a;
-        if (!jb.row_ok)
-          jb.pos = 0u;
-        else if (group)
-          jb.pos = tile.from_b ? qpos_b : qpos_a;  // a group's key rows are its query rows
-        else
-          jb.pos = tile.j0 + t - (tile.from_b ? start_b : start_a);
-        jb.mul = 1.0f;
-      }
-      return jb;
+    // row t of key tile j of the stream: segment A holds tiles [0, a1) (all of them for a
+    // shared stream), segment B the rest; within a segment, tile j starts at token
+    // k0 + 128 (j - j_first), its keys end at kend, and a piece's row position is the token
+    // minus the sequence start (a group's is its query row's)
+    const uint32_t seg_a_end = sm.shared ? sm.n : sm.a1;
+    const uint32_t a_kend = sm.shared ? sm.end : sm.a_k0 + sm.a_nk;
+    const uint32_t b_kend = sm.b_k0 + sm.b_nk;
+    const int32_t a_pbase = ra.kind != 0 ? 0 : static_cast<int32_t>(sm.a_k0 + t) - static_cast<int32_t>(off_a[0]);
+    const int32_t b_pbase = (!has_b || rb.kind != 0) ? 0 : static_cast<int32_t>(sm.b_k0 + t) - static_cast<int32_t>(off_b[0]);
+    auto krow = [&](uint32_t j, uint32_t& pos) -> bool {
+      const bool inb = j >= seg_a_end;
+      const uint32_t jj = inb ? j - seg_a_end : j;
+      const uint32_t j0 = (inb ? sm.b_k0 : sm.a_k0) + jj * kBC;
+      const bool ok = static_cast<uint32_t>(t) < (inb ? b_kend : a_kend) - j0;
+      const bool grp = inb ? rb.kind != 0 : ra.kind != 0;
+      pos = !ok ? 0u : grp ? (inb ? qpos_b : qpos_a)
+                          : static_cast<uint32_t>((inb ? b_pbase : a_pbase) + static_cast<int32_t>(jj * kBC));
+      return ok;
     };
 
-    // job i's table rows go to buffer i & 1
+    const uint32_t nq = has_b ? 2u : 1u;
+    const uint32_t njobs = nq + sm.n;
+    // the first job's table rows
     {
-      const RotJob j0 = job_of(0);
-      if (j0.row_ok) fetch_table_row(p, tbl0, j0.pos, t);
-      cp_async_commit();
-      if (njobs > 1) {
-        const RotJob j1 = job_of(1);
-        if (j1.row_ok) fetch_table_row(p, tbl0 + kRowTblBytes, j1.pos, t);
-      }
+      const bool ok0 = qok_a;
+      if (ok0) fetch_table_row(p, tbl0 + buf * kRowTblBytes, qpos_a, t);
       cp_async_commit();
     }
 #pragma unroll 1
     for (uint32_t i = 0; i < njobs; ++i) {
-      const RotJob jb = job_of(i);
-      cp_async_wait1();  // job i's rows have landed (job i + 1's may still be in flight)
-      bad |= !wait_bar(meta, p.ctl, jb.full, jb.phase, p.timeout_ns);
-      bad = __any_sync(0xffffffffu, bad);
-      if (bad) break;
-      if (jb.row_ok) rope_row<BF16>(jb.tile, t, tblp + (i & 1u) * kRowTblBytes, t, jb.mul);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(jb.ready));
-      // the buffer of job i is free: job i + 2's rows go there
-      if (i + 2 < njobs) {
-        const RotJob jn = job_of(i + 2);
-        if (jn.row_ok) fetch_table_row(p, tbl0 + (i & 1u) * kRowTblBytes, jn.pos, t);
+      // this job
+      const bool isq = i < nq;
+      const bool xb = i == 1 && has_b;
+      uint32_t pos_i;
+      bool ok;
+      uint8_t* tile;
+      uint64_t* full;
+      uint64_t* ready;
+      uint32_t phase;
+      if (isq) {
+        const uint32_t qn = xb ? qn1 : qn0;
+        const uint32_t qb = qn & 1u;
+        const int x = xb ? 1 : 0;
+        tile = q_tile(smem, x, qb);
+        full = &B.q_full[x][qb];
+        ready = &B.q_ready[x][qb];
+        phase = (qn >> 1) & 1u;
+        ok = xb ? qok_b : qok_a;
+      } else {
+        tile = k_tile(smem, kst);
+        full = &B.k_full[kst];
+        ready = &B.k_ready[kst];
+        phase = kph;
+        ok = krow(i - nq, pos_i);
+      }
+      // the next job's table rows into the other buffer
+      if (i + 1 < njobs) {
+        uint32_t pos_n = 0;
+        bool ok_n;
+        if (i + 1 < nq) {
+          ok_n = qok_b;
+          pos_n = qpos_b;
+        } else {
+          ok_n = krow(i + 1 - nq, pos_n);
+        }
+        if (ok_n) fetch_table_row(p, tbl0 + (buf ^ 1u) * kRowTblBytes, pos_n, t);
       }
       cp_async_commit();
+      cp_async_wait1();  // this job's rows have landed (the next one's may still be in flight)
+      bad |= !wait_bar(meta, p.ctl, full, phase, p.timeout_ns);
+      bad = __any_sync(0xffffffffu, bad);
+      if (bad) break;
+      if (ok) rope_row<BF16>(tile, t, tblp + buf * kRowTblBytes, t, isq ? p.q_mul : 1.0f);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(ready));
+      buf ^= 1u;
+      if (!isq) {
+        kst = (kst + 1) & (kKStages - 1);
+        if (kst == 0) kph ^= 1u;
+      }
     }
     cp_async_wait0();
     if (bad) break;
     ++qn0;
     if (has_b) ++qn1;
-    k.n += sm.n;
   }
   cp_async_wait0();
   if (bad && lane == 0) raise_abort(meta, p.ctl);

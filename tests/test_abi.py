@@ -17,7 +17,8 @@ def declared_functions():
     for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
         if not h.endswith(".h"):
             continue
-        text = open(os.path.join(ROOT, "include", h)).read()
+        with open(os.path.join(ROOT, "include", h)) as f:
+            text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         names += re.findall(r"\b(pk_\w+)\s*\(", text)
     return sorted(set(names))

@@ -132,3 +132,39 @@ def test_deterministic(pk):
     o1, l1 = run(pk, wl, inputs=inputs)
     o2, l2 = run(pk, wl, inputs=inputs)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ------------------------------------------------------------------------------------------
+# paths of the tensor-core kernel that the workloads above do not reach
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("scale", [1.0, 0.05, -0.125, 0.0])
+def test_scales(pk, orc, dtype, scale):
+    """A positive scale is applied to the scores in the softmax, any other multiplies q. The
+    inputs' spread is chosen so that the scaled scores keep unit spread (as at scale 1/8 with
+    unit inputs): the rotated q and k are rounded to the input type for the tensor cores, and
+    larger scores would carry that rounding past the stated tolerances at any scale."""
+    sigma = (1.0 / (8.0 * abs(scale))) ** 0.5 if scale != 0.0 else 1.0
+    wl = synth.make_lens_workload("scale", [130, 40, 5, 260], dtype, H=2, window=0, seed=11, scale=scale,
+                                  sigma=sigma)
+    _check(pk, orc, wl)
+
+
+@pytest.mark.parametrize("window", [0, 2])
+def test_group_with_many_members(pk, orc, window):
+    """A group of short sequences with more member offsets than the kernel stages in shared
+    memory (empty sequences share a granule without limit): rows find their sequence in cu."""
+    lens = [3] + [0] * 100 + [5] + [0] * 50 + [7, 2] + [0] * 20 + [40, 200]
+    wl = synth.make_lens_workload("members", lens, "bf16", H=2, window=window, seed=12)
+    sched = orc.schedule(wl.cu, window)
+    assert int(sched[:, 5].max()) > 66  # nseq of the group
+    _check(pk, orc, wl)
+
+
+@pytest.mark.parametrize("lens", [[129], [129, 129], [127, 300, 5], [640, 64, 640]], ids=str)
+def test_pairs(pk, orc, lens):
+    """Odd and even record counts, pieces sharing a key stream, a stream that ends mid-pair."""
+    for window in (0, 100):
+        wl = synth.make_lens_workload("pairs", lens, "bf16", H=3, window=window, seed=len(lens))
+        _check(pk, orc, wl)
