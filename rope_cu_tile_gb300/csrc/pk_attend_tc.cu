@@ -813,25 +813,24 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
       // SM sub-partition). Pass 1: the row max.
       float mx = -INFINITY;
 #pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        float v[64];
-        tmem_ld64(tS + 64 * hh, v);
+      for (int qq = 0; qq < 4; ++qq) {
+        float v[32];
+        tmem_ld32(tS + 32 * qq, v);
         if (!full) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (static_cast<unsigned>(c + 64 * hh - c_lo) >= static_cast<unsigned>(c_hi - c_lo)) v[c] = -INFINITY;
+          for (int c = 0; c < 32; ++c)
+            if (static_cast<unsigned>(c + 32 * qq - c_lo) >= static_cast<unsigned>(c_hi - c_lo)) v[c] = -INFINITY;
         }
-        float mk[4];
+        float m0 = fmax3(v[0], v[1], v[2]), m1 = fmax3(v[3], v[4], v[5]), m2 = fmax3(v[6], v[7], v[8]),
+              m3 = fmax3(v[9], v[10], v[11]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mk[k] = fmax3(v[k], v[4 + k], v[8 + k]);
-#pragma unroll
-        for (int c = 12; c < 60; c += 8) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mk[k] = fmax3(mk[k], v[c + k], v[c + 4 + k]);
+        for (int c = 12; c < 28; c += 8) {
+          m0 = fmax3(m0, v[c], v[c + 1]);
+          m1 = fmax3(m1, v[c + 2], v[c + 3]);
+          m2 = fmax3(m2, v[c + 4], v[c + 5]);
+          m3 = fmax3(m3, v[c + 6], v[c + 7]);
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mk[k] = fmaxf(mk[k], v[60 + k]);
-        mx = fmax3(mx, fmax3(mk[0], mk[1], mk[2]), mk[3]);
+        mx = fmax3(mx, fmax3(m0, m1, v[28]), fmax3(fmax3(m2, m3, v[29]), v[30], v[31]));
       }
       const float m_new = fmaxf(m_ref, mx);
       const bool grow = (m_new - m_ref) * k2 > kRescale;
