@@ -48,10 +48,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of the attention kernel per launch from an ncu capture, valid only while the
 # kernel source has the recorded hash (otherwise reported as null).
 NCU_TRAFFIC = {  # {config_name: (sha1 of pk_attend_tc.cu at capture, bytes per launch)}
-    "global": ("19b0bd4848cf9e360dc615859b20c185255ce7b1", 84934656),
-    "local": ("19b0bd4848cf9e360dc615859b20c185255ce7b1", 429214720),
-    "long": ("19b0bd4848cf9e360dc615859b20c185255ce7b1", 1069248768),
-    "short": ("19b0bd4848cf9e360dc615859b20c185255ce7b1", 386051328),
+    "global": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 83713280),
+    "local": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 428753152),
+    "long": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 1068222976),
+    "short": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 384914688),
 }
 
 
