@@ -133,8 +133,25 @@ __device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int 
   const uint64_t NB = (static_cast<uint64_t>(T) + kGrain - 1) / kGrain;
   const uint64_t per = (NB + nthr - 1) / nthr;
   const uint64_t b0 = min(NB, per * tid), b1 = min(NB, b0 + per);
+  // one granule per thread (T <= 64 x threads): its records stay in registers from the count
+  // to the write; otherwise they are enumerated twice
+  const bool single = per <= 1;
+  TileRec g0{}, g1{}, g2{};
   uint32_t count = 0;
-  for (uint64_t b = b0; b < b1; ++b) granule_visit(cu, S, window, b, [&](const TileRec&) { ++count; });
+  if (single) {
+    if (b0 < b1)
+      granule_visit(cu, S, window, b0, [&](const TileRec& r) {
+        if (count == 0)
+          g0 = r;
+        else if (count == 1)
+          g1 = r;
+        else
+          g2 = r;
+        ++count;
+      });
+  } else {
+    for (uint64_t b = b0; b < b1; ++b) granule_visit(cu, S, window, b, [&](const TileRec&) { ++count; });
+  }
 
   // exclusive scan of the per-thread counts
   const int lane = tid & 31, warp = tid >> 5;
@@ -161,15 +178,21 @@ __device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int 
   const uint32_t total = s_warp[nthr / 32 - 1];
 
   uint32_t at = base;
-  for (uint64_t b = b0; b < b1; ++b)
-    granule_visit(cu, S, window, b, [&](const TileRec& r) {
-      if (at < static_cast<uint64_t>(cap)) {
-        uint4* d = reinterpret_cast<uint4*>(tiles + at);
-        d[0] = make_uint4(r.q0, r.rows, r.k0, r.nk);
-        d[1] = make_uint4(r.seq, r.nseq, r.kind, r.ktiles);
-      }
-      ++at;
-    });
+  auto put = [&](const TileRec& r) {
+    if (at < static_cast<uint64_t>(cap)) {
+      uint4* d = reinterpret_cast<uint4*>(tiles + at);
+      d[0] = make_uint4(r.q0, r.rows, r.k0, r.nk);
+      d[1] = make_uint4(r.seq, r.nseq, r.kind, r.ktiles);
+    }
+    ++at;
+  };
+  if (single) {
+    if (count > 0) put(g0);
+    if (count > 1) put(g1);
+    if (count > 2) put(g2);
+  } else {
+    for (uint64_t b = b0; b < b1; ++b) granule_visit(cu, S, window, b, put);
+  }
   if (tid == 0) {
     if (total > static_cast<uint64_t>(cap)) {
       ctl->ntiles = 0;
