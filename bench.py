@@ -55,6 +55,18 @@ NCU_TRAFFIC = {  # {config_name: (sha1 of pk_attend_tc.cu at capture, bytes per 
 }
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's); x itself at one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def kernel_source_hash() -> str:
     p = os.path.join(ROOT, "rope_cu_tile_gb300", "csrc", "pk_attend_tc.cu")
     return hashlib.sha1(open(p, "rb").read()).hexdigest()
@@ -237,11 +249,9 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
     ms = ev0.elapsed_time(ev1)
     if pk.last_status(stream) != 0:
         raise RuntimeError("device error during timed steps")
+    ms = max_over_ranks(ms, world)
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
@@ -304,11 +314,7 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
     f1.record(s_out)
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1) / e_steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
 
     return {"ms_per_step": ms / steps, "attend_ms": attend_ms / max(calls, 1),
             "schedule_ms": sched_ms / max(calls, 1), "calls": calls, "flops": flops, "bytes": abytes,
