@@ -40,6 +40,14 @@
  *     alignment, launch) are returned at once and nothing is launched. Errors found by
  *     the device (a malformed cu, a wait that ran out of time) are recorded in the
  *     stream's status word, read by pk_last_status(). The kernels never trap.
+ *
+ * Environment (read by the library, for tests and debugging):
+ *   PK_TIMEOUT_MS          bound of every pipeline wait inside the kernels (default 2000);
+ *                          read at the first call of the process.
+ *   PK_DEBUG_SKIP_ARRIVE=1 test hook of the bf16 / fp16 path, read at every call: the
+ *                          producer of each CTA withholds its first work-item hand-off, so
+ *                          the call ends with PK_ERR_TIMEOUT after one wait bound and writes
+ *                          no valid output; later calls without it are unaffected.
  */
 #ifndef PK_H
 #define PK_H

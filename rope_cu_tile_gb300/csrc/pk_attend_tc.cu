@@ -33,6 +33,8 @@
 // CTA's abort flag, which every other wait watches; the producer then waits (bounded)
 // for its copies in flight, the MMA issuer for its MMAs, and the CTA frees its tensor
 // memory and returns.
+#include <cstdlib>
+
 #include "pk_dev.cuh"
 
 namespace pk {
@@ -226,6 +228,7 @@ struct Params {
   float q_mul;  // multiplies the rotated q (the scale when it is not positive, else 1)
   float s_mul;  // multiplies the scores in the softmax (the scale when it is positive, else 1)
   unsigned long long timeout_ns;
+  int skip_first_item_arrive;  // test hook: the producer withholds its first item hand-off
 };
 
 // The member sequence offsets cu[rec.seq .. rec.seq + rec.nseq] of a record, copied by the
@@ -405,7 +408,9 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, uint8_t* smem
     bx.b0 = b0;
     bx.b1 = b1;
     bx.end = end;
-    mbar_arrive(smem_u32(&B.item_full[mb]));
+    // (the test hook leaves the consumers waiting: their bounded waits time out and the CTA
+    // unwinds with PK_ERR_TIMEOUT)
+    if (!(p.skip_first_item_arrive && it == 0)) mbar_arrive(smem_u32(&B.item_full[mb]));
     ++it;
 
     // Q_X into its next buffer once the item two back has issued its last S_X
@@ -1052,6 +1057,13 @@ cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos
   p.q_mul = scale > 0.0f ? 1.0f : scale;
   p.s_mul = scale > 0.0f ? scale : 1.0f;
   p.timeout_ns = timeout_ns;
+  // test hook for the bounded waits (PK_DEBUG_SKIP_ARRIVE=1): every CTA's producer withholds
+  // its first work-item hand-off, so the consumers' waits run out and the call ends with
+  // PK_ERR_TIMEOUT in the stream's status word; nothing faults and the context stays usable
+  {
+    const char* e = std::getenv("PK_DEBUG_SKIP_ARRIVE");
+    p.skip_first_item_arrive = (e && e[0] == '1') ? 1 : 0;
+  }
   // programmatic stream serialization: the CTAs set up (barriers, tensor memory) while the
   // scheduler finishes; the producer waits for the scheduler before it reads the records
   cudaLaunchConfig_t cfg = {};

@@ -134,3 +134,49 @@ def test_constant_values(pk):
     wl.qkv = qkv
     o, _ = run(pk, wl)
     assert max_err(o, want) <= TOL["f16"][0]
+
+
+_STALL_SCRIPT = r"""
+import json, os, sys
+sys.path.insert(0, os.environ["ROOT"]); sys.path.insert(0, os.path.join(os.environ["ROOT"], "tests"))
+import numpy as np, torch
+import rope_cu_tile_gb300 as pk
+import synth
+from gpu_util import device_inputs, out_to_f64
+from oracle import get
+pk.load()
+wl = synth.make_lens_workload("stall", [300, 40, 129], "bf16", H=2, window=0, seed=9)
+qkv, cos, sin, cu = device_inputs(wl)
+os.environ["PK_DEBUG_SKIP_ARRIVE"] = "1"
+pk.attend(qkv, cos, sin, cu, wl.H, 0, wl.scale)
+torch.cuda.synchronize()
+stalled = pk.last_status()
+del os.environ["PK_DEBUG_SKIP_ARRIVE"]
+out, lse = pk.attend(qkv, cos, sin, cu, wl.H, 0, wl.scale)
+torch.cuda.synchronize()
+after = pk.last_status()
+want_o, want_l = get().attend(wl.qkv, wl.cos, wl.sin, wl.cu, wl.H, 0, wl.scale, "bf16")
+eo = float(np.max(np.abs(out_to_f64(out) - want_o)))
+el = float(np.max(np.abs(lse.cpu().numpy().astype(np.float64) - want_l)))
+print(json.dumps({"stalled": stalled, "after": after, "eo": eo, "el": el}))
+"""
+
+
+def test_withheld_hand_off_times_out_and_the_context_stays_usable():
+    """A producer that withholds its first work-item hand-off (test hook): every consumer's
+    bounded wait runs out, the call ends with PK_ERR_TIMEOUT in the status word, and the next
+    call on the same context is correct. Nothing traps, faults or hangs."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, ROOT=root, PK_TIMEOUT_MS="100")
+    env.pop("PK_DEBUG_SKIP_ARRIVE", None)
+    p = subprocess.run([sys.executable, "-c", _STALL_SCRIPT], env=env, capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-3000:]
+    r = json.loads(p.stdout.strip().splitlines()[-1])
+    assert r["stalled"] == 6, r  # PK_ERR_TIMEOUT
+    assert r["after"] == 0, r
+    assert r["eo"] <= TOL["bf16"][0] and r["el"] <= TOL["bf16"][1], r
