@@ -23,15 +23,19 @@
 //        K and V tiles (128-byte swizzle, straight from the strided qkv), K two tiles ahead
 //        of V; warps 1, 2: MMA issuers of A, B (one lane each): per stream tile j,
 //        S_X(j) = Q_X K(j)^T when X uses j, then O_X += P_X(j-1) V(j-1); warp 3 idle.
-//   WG1  rotation: thread t rotates (and for Q scales) row t of every Q and K tile in
-//        shared memory as soon as it lands, from table rows it prefetched with cp.async.
-//   WG2, WG3  softmax of A, B: thread r owns query row r. It reads its S row from TMEM,
-//        masks it by the row's visible key interval, keeps a running max (O is rescaled
-//        only when the max grows by more than a factor 2^8), writes P to TMEM, and at the
-//        end of the item writes out = O / l and lse = m + ln l.
+//   WG1  rotation: thread t rotates row t of every Q and K tile in shared memory as soon
+//        as it lands, from table rows it prefetched with cp.async (q is multiplied by the
+//        scale here only when the scale is not positive).
+//   WG2, WG3  softmax of A, B: thread r owns query row r. It reads its S row from TMEM
+//        twice (the row max by quarters, then the probabilities by halves), masks it by the
+//        row's visible key interval, applies a positive scale inside exp2, keeps a running
+//        max (O is rescaled only when the max grows by more than a factor 2^8), writes P to
+//        TMEM, and at the end of the item writes out = O / l and lse = m + ln l.
+// The loops of the rotation and softmax roles stay rolled: the four code streams sharing
+// an SM sub-partition run out of instruction cache when they are unrolled.
 // Every wait is bounded. A wait that times out records PK_ERR_TIMEOUT and raises the
 // CTA's abort flag, which every other wait watches; the producer then waits (bounded)
-// for its copies in flight, the MMA issuer for its MMAs, and the CTA frees its tensor
+// for its copies in flight, the MMA issuers for their MMAs, and the CTA frees its tensor
 // memory and returns.
 #include <cstdlib>
 
