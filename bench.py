@@ -46,8 +46,8 @@ L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic of the attention kernel per launch from an ncu capture, valid only while the
-# kernel source has the recorded hash (otherwise reported as null).
-NCU_TRAFFIC = {  # {config_name: (sha1 of pk_attend_tc.cu at capture, bytes per launch)}
+# kernel's sources have the recorded hash (kernel_source_hash; otherwise reported as null).
+NCU_TRAFFIC = {  # {config_name: (kernel_source_hash() at capture, bytes per launch)}
     "global": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 83713280),
     "local": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 428753152),
     "long": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 1068222976),
@@ -68,8 +68,13 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 def kernel_source_hash() -> str:
-    p = os.path.join(ROOT, "rope_cu_tile_gb300", "csrc", "pk_attend_tc.cu")
-    return hashlib.sha1(open(p, "rb").read()).hexdigest()
+    """sha1 over what the attention kernel is built from: its source, the device header and
+    the build flags."""
+    h = hashlib.sha1()
+    for rel in (("csrc", "pk_attend_tc.cu"), ("csrc", "pk_dev.cuh"), ("build.py",)):
+        with open(os.path.join(ROOT, "rope_cu_tile_gb300", *rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def load_peaks():
