@@ -48,6 +48,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of the attention kernel per launch from an ncu capture, valid only while the
 # kernel's sources have the recorded hash (kernel_source_hash; otherwise reported as null).
 NCU_TRAFFIC = {  # {config_name: (kernel_source_hash() at capture, bytes per launch)}
+    "global": ("7beb5d3ca726e91a76d52ad3c285a88966a60a76", 83515136),
+    "local": ("7beb5d3ca726e91a76d52ad3c285a88966a60a76", 428199936),
+    "long": ("7beb5d3ca726e91a76d52ad3c285a88966a60a76", 1068990976),
+    "short": ("7beb5d3ca726e91a76d52ad3c285a88966a60a76", 384982528),
+}
     "global": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 83713280),
     "local": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 428753152),
     "long": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 1068222976),
