@@ -53,11 +53,6 @@ NCU_TRAFFIC = {  # {config_name: (kernel_source_hash() at capture, bytes per lau
     "long": ("7beb5d3ca726e91a76d52ad3c285a88966a60a76", 1068990976),
     "short": ("7beb5d3ca726e91a76d52ad3c285a88966a60a76", 384982528),
 }
-    "global": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 83713280),
-    "local": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 428753152),
-    "long": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 1068222976),
-    "short": ("05eb62dd99e51e1ae21492cbc736f030cbbe52c8", 384914688),
-}
 
 
 def max_over_ranks(x: float, world: int) -> float:
