@@ -25,8 +25,10 @@
  * `window` = 0 lets every key of the sequence through (the pages' "0: every key").
  *
  * Precision: bf16 and fp16 inputs are multiplied on the tensor cores (tcgen05, fp32
- * accumulation) after rotation in fp32; the probabilities are rounded to the input type
- * before the product with v. fp32 inputs are computed in fp32 on the CUDA cores.
+ * accumulation) after rotation in fp32 (the rotated q and k are rounded to the input type);
+ * a positive scale multiplies the fp32 scores, any other scale the rotated q; the
+ * probabilities are rounded to the input type before the product with v. fp32 inputs are
+ * computed in fp32 on the CUDA cores.
  *
  * Conventions for every entry point below:
  *   - All array pointers are DEVICE pointers of the current CUDA device; the caller owns
