@@ -37,7 +37,9 @@
  *   - The library keeps, per (device, stream), a small workspace it allocates on first use
  *     and grows when a larger T arrives (tile records and a control word); pk_release()
  *     frees all of them. Calls on one stream are ordered; calls on different streams use
- *     different workspaces.
+ *     different workspaces. A call may be captured in a CUDA graph once an earlier,
+ *     uncaptured call on the same stream has allocated a workspace large enough for T;
+ *     a captured call that would have to allocate returns PK_ERR_CAPTURE, nothing launched.
  *   - Return value: PK_OK, or an error code below. Errors found on the host (arguments,
  *     alignment, launch) are returned at once and nothing is launched. Errors found by
  *     the device (a malformed cu, a wait that ran out of time) are recorded in the
@@ -73,7 +75,9 @@ enum pk_status {
     PK_ERR_TIMEOUT = 6,      /* device: a pipeline wait exceeded its bound; results invalid */
     PK_ERR_NOMEM = 7,        /* workspace allocation failed */
     PK_ERR_INTERNAL = 8,     /* device: schedule exceeded its capacity (a library bug) */
-    PK_ERR_TOO_LARGE = 9     /* pk_attend_noalloc: T above PK_NOALLOC_MAX_T */
+    PK_ERR_TOO_LARGE = 9,    /* pk_attend_noalloc: T above PK_NOALLOC_MAX_T */
+    PK_ERR_CAPTURE = 10      /* the stream is being captured and its workspace would have to
+                                be allocated or grown: make one uncaptured call first */
 };
 
 enum pk_dtype { PK_F32 = 0, PK_BF16 = 1, PK_F16 = 2 };

@@ -23,7 +23,7 @@ PK_F32, PK_BF16, PK_F16 = 0, 1, 2
 STATUS = {
     0: "PK_OK", 1: "PK_ERR_ARG", 2: "PK_ERR_ALIGN", 3: "PK_ERR_CUDA", 4: "PK_ERR_UNSUPPORTED",
     5: "PK_ERR_BAD_CU", 6: "PK_ERR_TIMEOUT", 7: "PK_ERR_NOMEM", 8: "PK_ERR_INTERNAL",
-    9: "PK_ERR_TOO_LARGE",
+    9: "PK_ERR_TOO_LARGE", 10: "PK_ERR_CAPTURE",
 }
 NOALLOC_MAX_T = 1048576
 

@@ -114,6 +114,12 @@ int workspace(int dev, cudaStream_t stream, int64_t cap, Workspace** out) {
     *out = &ws;
     return PK_OK;
   }
+  cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap_status) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_CUDA;
+  }
+  if (cap_status != cudaStreamCaptureStatusNone) return PK_ERR_CAPTURE;
   int carried = 0;
   if (ws.base) {
     // keep the sticky status across the move

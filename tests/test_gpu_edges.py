@@ -180,3 +180,53 @@ def test_withheld_hand_off_times_out_and_the_context_stays_usable():
     assert r["stalled"] == 6, r  # PK_ERR_TIMEOUT
     assert r["after"] == 0, r
     assert r["eo"] <= TOL["bf16"][0] and r["el"] <= TOL["bf16"][1], r
+
+
+def test_cuda_graph_capture(pk, orc):
+    """After a first call has set up the stream's workspace, a call captured in a CUDA graph
+    (both kernels, the attention kernel's programmatic launch included) replays correctly."""
+    import torch
+
+    wl = synth.make_lens_workload("graph", [200, 7, 129, 64], "bf16", H=2, window=0, seed=13)
+    qkv, cos, sin, cu = device_inputs(wl)
+    s = torch.cuda.Stream()
+    out = torch.empty((wl.T, wl.H * 64), dtype=qkv.dtype, device="cuda")
+    lse = torch.empty((wl.H, wl.T), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(s):
+        pk.attend(qkv, cos, sin, cu, wl.H, 0, wl.scale, out=out, lse=lse, stream=s)
+    torch.cuda.synchronize()
+    out.fill_(0)
+    lse.fill_(0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pk.attend(qkv, cos, sin, cu, wl.H, 0, wl.scale, out=out, lse=lse, stream=s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert pk.last_status(s) == 0
+    want_o, want_l = orc.attend(wl.qkv, wl.cos, wl.sin, wl.cu, wl.H, 0, wl.scale, "bf16")
+    assert max_err(out_to_f64(out), want_o) <= TOL["bf16"][0]
+    assert max_err(lse.cpu().numpy().astype(np.float64), want_l) <= TOL["bf16"][1]
+
+
+def test_capture_that_would_allocate_is_refused(pk):
+    """A captured call whose stream has no workspace yet returns PK_ERR_CAPTURE and launches
+    nothing; the capture itself stays valid and replays the rest of its work."""
+    import torch
+
+    wl = synth.make_lens_workload("graph-fresh", [130, 5], "bf16", H=1, window=0, seed=14)
+    qkv, cos, sin, cu = device_inputs(wl)
+    out = torch.full((wl.T, wl.H * 64), 7.0, dtype=qkv.dtype, device="cuda")
+    lse = torch.zeros((wl.H, wl.T), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    pk.release()  # no stream has a workspace now
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        lse.fill_(3.0)
+        with pytest.raises(pk.PKError) as err:
+            pk.attend(qkv, cos, sin, cu, wl.H, 0, wl.scale, out=out, lse=lse, stream=s)
+    assert err.value.code == 10  # PK_ERR_CAPTURE
+    g.replay()
+    torch.cuda.synchronize()
+    assert bool((lse == 3.0).all()) and bool((out == 7.0).all())
