@@ -118,9 +118,9 @@ int pk_attend_dt(int dtype, const void *qkv, const void *cos, const void *sin,
  * 128-row piece of one sequence and 1 for a group of short sequences, ktiles =
  * ceil(nk/128)). Synchronizes `stream` and writes the record count to *nt (host pointer).
  * Returns PK_ERR_BAD_CU for a malformed cu (then *nt = 0), PK_ERR_ARG when cap is too small.
- * The rule (packed.rs fn layout for sequences longer than 64 tokens; grouping of short
- * sequences by the 64-token granule their first token falls in) is stated in full in the
- * oracle that checks it.
+ * The rule (packed.rs fn layout for sequences longer than 64 tokens; short sequences packed
+ * greedily into groups of at most 128 rows within 1024-token windows) is stated in full in
+ * the oracle that checks it.
  */
 int pk_schedule(const uint32_t *cu, int S, int64_t T, int window, uint32_t *tiles, int64_t cap,
                 int64_t *nt, struct CUstream_st *stream);
@@ -153,7 +153,7 @@ int pk_profile_stop(double *schedule_ms, double *attend_ms, int *calls);
  * a plugin whose enqueue step may not allocate, an application whose pool allocator owns
  * the device) or that cannot afford the synchronization a cudaMalloc brings use this call
  * instead: it allocates nothing, and runs the same kernels on a scratch area compiled into
- * the library (a static __device__ array of about 1.5 MB, present on every GPU that loads
+ * the library (a static __device__ array of about 4 MB, present on every GPU that loads
  * the library until the process exits).
  *   - dtype: enum pk_dtype; the other arguments as pk_attend.
  *   - T at most PK_NOALLOC_MAX_T tokens; larger T returns PK_ERR_TOO_LARGE, nothing launched.

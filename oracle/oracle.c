@@ -21,7 +21,8 @@
  * sequences, the tile records the library's device scheduler must reproduce bit for bit.
  * Its first part is packed.rs fn layout (each sequence cut into BR-row tiles at rows
  * 0, BR, 2BR, ...) with the key range clipped to the window (fn attend, key-range
- * clipping); its second part packs runs of short sequences into one tile.
+ * clipping); its second part packs short sequences greedily into tiles of at most BR
+ * rows.
  *
  * Inputs may be given in fp64, fp32, bf16 (bit patterns) or fp16 (bit patterns); every
  * value is widened to fp64 exactly before use.
@@ -389,14 +390,19 @@ int oracle_attend_rows(const void *qkv, int dt, const void *cosb, const void *si
  *   kind      0: a BR-row piece of one sequence; 1: a group of whole short sequences
  *   ktiles    ceil(nk / BC)
  * Constants: BR = BC = 128 rows per tile; a sequence is short when its length is at most
- * SHORT = 64; short (and empty) sequences whose first token falls in the same GRAIN = 64
- * token granule [64 b, 64 b + 64) form one group (at most 63 + 64 = 127 rows).
+ * SHORT = 64. Short (and empty) sequences are grouped within WIN = 1024-token windows
+ * [1024 w, 1024 w + 1024), a sequence belonging to the window of its first token: taken in
+ * order, they are packed greedily -- a group takes the next sequence while that sequence is
+ * short, belongs to the group's window and keeps the group within BR rows; anything else
+ * closes it (a group of empty sequences only has no rows and gives no record).
  * Records are listed by increasing q0.
  */
 #define SCH_BR 128
 #define SCH_BC 128
 #define SCH_SHORT 64
-#define SCH_GRAIN 64
+#define SCH_WIN 1024
+/* capacity unit: at most 3 records per 64 tokens (plus one) */
+#define SCH_CAP_UNIT 64
 
 static int64_t emit(uint32_t *tiles, int64_t cap, int64_t nt, int64_t q0, int64_t rows, int64_t k0,
                     int64_t k1, int64_t seq, int64_t nseq, int kind) {
@@ -423,25 +429,32 @@ int oracle_schedule(const uint32_t *cu, int S, int64_t T, int window, uint32_t *
     *nt_out = 0;
     if (window < 0 || check_cu(cu, S, T)) return -1;
     int64_t nt = 0;
-    /* the open group of short sequences: granule, first member, last member */
-    int64_t g_b = -1, g_first = -1, g_last = -1;
+    /* the open group of short sequences: window, first member, last member */
+    int64_t g_w = -1, g_first = -1, g_last = -1;
     for (int s = 0; s <= S; s++) {
         int64_t start = s < S ? cu[s] : T;
         int64_t L = s < S ? (int64_t)cu[s + 1] - cu[s] : 0;
         int is_short = s < S && L <= SCH_SHORT;
-        int64_t b = start / SCH_GRAIN;
+        int64_t w = start / SCH_WIN;
         /* close the open group when this sequence does not join it */
-        if (g_b >= 0 && !(is_short && b == g_b)) {
+#if ORACLE_MUTANT == 10
+        int joins = g_w >= 0 && is_short && w == g_w && start + L - cu[g_first] <= SCH_BR + 1; /* planted */
+#elif ORACLE_MUTANT == 11
+        int joins = g_w >= 0 && is_short && start + L - cu[g_first] <= SCH_BR;  /* planted: no window */
+#else
+        int joins = g_w >= 0 && is_short && w == g_w && start + L - cu[g_first] <= SCH_BR;
+#endif
+        if (g_w >= 0 && !joins) {
             int64_t q0 = cu[g_first];
             int64_t rows = (int64_t)cu[g_last + 1] - q0;
             if (rows > 0)
                 nt = emit(tiles, cap, nt, q0, rows, q0, q0 + rows, g_first, g_last - g_first + 1, 1);
-            g_b = -1;
+            g_w = -1;
         }
         if (s == S) break;
         if (is_short) {
-            if (g_b < 0) {
-                g_b = b;
+            if (g_w < 0) {
+                g_w = w;
                 g_first = s;
             }
             g_last = s;
@@ -473,4 +486,4 @@ int oracle_schedule(const uint32_t *cu, int S, int64_t T, int window, uint32_t *
 }
 
 /* an upper bound on the number of records for T tokens (what a caller should allocate) */
-int64_t oracle_schedule_cap(int64_t T) { return 3 * ((T + SCH_GRAIN - 1) / SCH_GRAIN) + 1; }
+int64_t oracle_schedule_cap(int64_t T) { return 3 * ((T + SCH_CAP_UNIT - 1) / SCH_CAP_UNIT) + 1; }

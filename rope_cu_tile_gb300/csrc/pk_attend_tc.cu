@@ -89,7 +89,7 @@ struct Bars {
 
 // Member sequence offsets of an item's records, staged by the rotation warpgroup (A's and
 // B's) and by each softmax warpgroup (its own record's).
-constexpr int kCuStage = kShort + 2;
+constexpr int kCuStage = kBR + 2;  // a group of up to 128 non-empty sequences
 struct Meta {
   Bars bars;
   ItemBox box[2];
@@ -100,6 +100,7 @@ struct Meta {
 };
 
 constexpr uint32_t kSmemUsed = kOffMeta + sizeof(Meta);
+static_assert(kSmemUsed + 1024 <= 227u * 1024u, "fits the 227 KB a block may use");
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns of query tile X
 __host__ __device__ constexpr uint32_t col_s(int x) { return 128u * x; }

@@ -14,7 +14,23 @@ constexpr int kHalf = 32;      // rotary pairs (u, u + 32)
 constexpr int kBR = 128;       // query rows per tile (one tcgen05 M=128 tile)
 constexpr int kBC = 128;       // keys per key tile
 constexpr int kShort = 64;     // sequences of at most this length are grouped
-constexpr int kGrain = 64;     // grouping granule in tokens
+constexpr int kWin = 1024;     // grouping window in tokens (groups never cross one)
+// schedule capacity: pieces <= T/64 (a long sequence has at least 65 tokens), groups <=
+// T/64 plus one per run of short sequences (two consecutive groups of a run hold more than
+// 128 rows), runs <= long sequences + windows: at most 3 records per kCapUnit tokens, plus one
+constexpr int kCapUnit = 64;
+// Records whose first query token falls in one window: records of at least 65 rows start
+// 65 apart (16), last pieces of at most 64 rows (the sequence holding the window's first
+// token, plus one per long sequence starting in it: 17), groups of at most 64 rows closed by
+// an overflow (each followed by a larger group: at most 16) or by a long sequence or the
+// window's end (17): 66 at most. The scheduler's single walk writes a warp's records to
+// slots of this many per window, then copies them into place.
+constexpr int kWinCap = 72;
+constexpr int kSchedWarps = 32;  // warps of the scheduler's block
+// staging slots (records) the scheduler needs for T tokens
+__host__ __device__ constexpr long long schedule_stage_records(long long T) {
+  return ((T + kWin - 1) / kWin + kSchedWarps - 1) / kSchedWarps * kSchedWarps * kWinCap;
+}
 constexpr int kRec = 8;        // uint32 per tile record
 
 // Tile record, written by the scheduler (8 x uint32, 32 bytes).

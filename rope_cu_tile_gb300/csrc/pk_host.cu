@@ -16,7 +16,7 @@
 namespace pk {
 
 cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, TileRec* tiles, long long cap,
-                            Ctl* ctl, cudaStream_t stream);
+                            TileRec* stage, Ctl* ctl, cudaStream_t stream);
 cudaError_t attend_tc_prepare();
 cudaError_t schedule_prepare();
 cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
@@ -29,13 +29,15 @@ cudaError_t attend_f32_launch(const float* qkv, const float* cos_t, const float*
 
 namespace {
 
-int64_t schedule_capacity(int64_t T) { return 3 * ((T + kGrain - 1) / kGrain) + 1; }
+int64_t schedule_capacity(int64_t T) { return 3 * ((T + kCapUnit - 1) / kCapUnit) + 1; }
 
 struct Workspace {
   void* base = nullptr;
   Ctl* ctl = nullptr;
-  TileRec* tiles = nullptr;
+  TileRec* tiles = nullptr;  // cap records
+  TileRec* stage = nullptr;  // the scheduler's staging slots
   int64_t cap = 0;
+  int64_t room = 0;  // tokens the workspace is sized for
 };
 
 struct DeviceInfo {
@@ -107,10 +109,11 @@ int device_info(int dev, DeviceInfo** out) {
   return PK_OK;
 }
 
-// the workspace of (dev, stream) with room for `cap` records (caller holds g_mu)
-int workspace(int dev, cudaStream_t stream, int64_t cap, Workspace** out) {
+// the workspace of (dev, stream) sized for T tokens: the records and the scheduler's staging
+// slots (caller holds g_mu)
+int workspace(int dev, cudaStream_t stream, int64_t T, Workspace** out) {
   Workspace& ws = g_ws[std::make_pair(dev, stream)];
-  if (ws.base && ws.cap >= cap) {
+  if (ws.base && ws.room >= T) {
     *out = &ws;
     return PK_OK;
   }
@@ -129,9 +132,10 @@ int workspace(int dev, cudaStream_t stream, int64_t cap, Workspace** out) {
     cudaFree(ws.base);
     ws = Workspace();
   }
-  int64_t want = cap < 4096 ? 4096 : cap;
-  want = want + want / 4;  // headroom against regrowth
-  const size_t bytes = sizeof(Ctl) + static_cast<size_t>(want) * sizeof(TileRec);
+  int64_t room = T < 65536 ? 65536 : T;
+  room = room + room / 4;  // headroom against regrowth
+  const int64_t cap = schedule_capacity(room), stage = schedule_stage_records(room);
+  const size_t bytes = sizeof(Ctl) + static_cast<size_t>(cap + stage) * sizeof(TileRec);
   void* p = nullptr;
   if (cudaMalloc(&p, bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -147,7 +151,9 @@ int workspace(int dev, cudaStream_t stream, int64_t cap, Workspace** out) {
   ws.base = p;
   ws.ctl = static_cast<Ctl*>(p);
   ws.tiles = reinterpret_cast<TileRec*>(static_cast<char*>(p) + sizeof(Ctl));
-  ws.cap = want;
+  ws.stage = ws.tiles + cap;
+  ws.cap = cap;
+  ws.room = room;
   *out = &ws;
   return PK_OK;
 }
@@ -168,7 +174,7 @@ int check_args(int dtype, const void* qkv, const void* cos, const void* sin, con
 
 int launch_schedule(const uint32_t* cu, int S, int64_t T, int window, Workspace* ws, cudaStream_t stream) {
   return schedule_launch(cu, S, static_cast<long long>(T), window, ws->tiles, static_cast<long long>(ws->cap),
-                         ws->ctl, stream) == cudaSuccess
+                         ws->stage, ws->ctl, stream) == cudaSuccess
              ? PK_OK
              : PK_ERR_CUDA;
 }
@@ -187,7 +193,7 @@ int attend(int dtype, const void* qkv, const void* cos, const void* sin, const u
   DeviceInfo* di = nullptr;
   if ((rc = device_info(dev, &di)) != PK_OK) return rc;
   Workspace* ws = nullptr;
-  if ((rc = workspace(dev, stream, schedule_capacity(T), &ws)) != PK_OK) return rc;
+  if ((rc = workspace(dev, stream, T, &ws)) != PK_OK) return rc;
   cudaEvent_t* ev = nullptr;
   if (g_prof.on && g_prof.dev == dev && g_prof.used < g_prof.cap) ev = g_prof.ev + 3 * g_prof.used++;
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return PK_ERR_CUDA;
@@ -277,7 +283,7 @@ int pk_schedule(const uint32_t* cu, int S, int64_t T, int window, uint32_t* tile
   int rc = device_info(dev, &di);
   if (rc != PK_OK) return rc;
   Workspace* ws = nullptr;
-  if ((rc = workspace(dev, stream, schedule_capacity(T), &ws)) != PK_OK) return rc;
+  if ((rc = workspace(dev, stream, T, &ws)) != PK_OK) return rc;
   if ((rc = launch_schedule(cu, S, T, window, ws, stream)) != PK_OK) return rc;
   Ctl ctl;
   if (cudaMemcpyAsync(&ctl, ws->ctl, sizeof ctl, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||

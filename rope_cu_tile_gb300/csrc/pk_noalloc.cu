@@ -8,7 +8,7 @@
 // own pool allocator owns the device), or code on a path where a cudaMalloc would
 // synchronize the device at the wrong moment. This entry point runs the same scheduler and
 // attention kernels on a scratch area that lives in the library image itself: a file-scope
-// static __device__ array sized for T <= PK_NOALLOC_MAX_T tokens (about 1.5 MB, held by
+// static __device__ array sized for T <= PK_NOALLOC_MAX_T tokens (about 4 MB, held by
 // every GPU that loads the library until the process exits).
 //
 // It calls no cudaMalloc, cudaFree or other allocating routine. Its first call on a device
@@ -29,7 +29,7 @@
 namespace pk {
 
 cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, TileRec* tiles, long long cap,
-                            Ctl* ctl, cudaStream_t stream);
+                            TileRec* stage, Ctl* ctl, cudaStream_t stream);
 cudaError_t attend_tc_prepare();
 cudaError_t schedule_prepare();
 cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
@@ -43,11 +43,12 @@ cudaError_t attend_f32_launch(const float* qkv, const float* cos_t, const float*
 namespace {
 
 constexpr long long kNoallocMaxT = PK_NOALLOC_MAX_T;
-constexpr long long kNoallocCap = 3 * ((kNoallocMaxT + kGrain - 1) / kGrain) + 1;
-constexpr size_t kScratchBytes = sizeof(Ctl) + static_cast<size_t>(kNoallocCap) * sizeof(TileRec);
+constexpr long long kNoallocCap = 3 * ((kNoallocMaxT + kCapUnit - 1) / kCapUnit) + 1;
+constexpr long long kNoallocStage = schedule_stage_records(kNoallocMaxT);
+constexpr size_t kScratchBytes = sizeof(Ctl) + static_cast<size_t>(kNoallocCap + kNoallocStage) * sizeof(TileRec);
 
-// The scratch area: the control block, then the tile records. Zero at load time; each call
-// clears the control block before use.
+// The scratch area: the control block, the tile records, then the scheduler's staging slots.
+// Zero at load time; each call clears the control block before use.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -138,10 +139,11 @@ extern "C" int pk_attend_noalloc(int dtype, const void* qkv, const void* cos, co
   if (rc != PK_OK) return rc;
   Ctl* ctl = reinterpret_cast<Ctl*>(s->scratch);
   TileRec* tiles = reinterpret_cast<TileRec*>(s->scratch + sizeof(Ctl));
+  TileRec* stage = tiles + kNoallocCap;
 
   // the control block starts each call at zero (the last call's counter and status stay in it)
   if (cudaMemsetAsync(ctl, 0, sizeof(Ctl), st) != cudaSuccess) return PK_ERR_CUDA;
-  if (schedule_launch(cu, S, static_cast<long long>(T), window, tiles, kNoallocCap, ctl, st) != cudaSuccess)
+  if (schedule_launch(cu, S, static_cast<long long>(T), window, tiles, kNoallocCap, stage, ctl, st) != cudaSuccess)
     return PK_ERR_CUDA;
   cudaError_t e;
   if (dtype == PK_F32) {

@@ -5,25 +5,27 @@
 //   - a sequence longer than kShort tokens is cut into 128-row pieces at rows 0, 128, ...
 //     (fn layout); a piece's keys are the whole sequence, or with a window w the rows
 //     [max(start, q0 - w), min(end, q0 + rows + w)) -- the union of its rows' windows;
-//   - sequences of at most kShort tokens (empty ones included) whose first token falls in
-//     the same kGrain-token granule form one group tile whose queries and keys are all of
-//     their rows (at most 63 + 64 = 127 rows);
+//   - sequences of at most kShort tokens (empty ones included) are grouped within
+//     kWin-token windows, a sequence belonging to the window of its first token: in order,
+//     a group takes the next sequence while that one is short, belongs to the group's
+//     window and keeps the group within 128 rows (greedy packing); a group tile's queries
+//     and keys are all of its rows, and a group of empty sequences only gives no record;
 //   - records are listed by increasing first query token.
 //
-// The device computes this in parallel over granules: every record's first query token
-// falls in exactly one granule [64 b, 64 b + 64), and a granule holds at most three:
-// (i) a piece of the long sequence that covers the granule's first token, (ii) the group
-// of short sequences starting in it, (iii) the first piece of a long sequence starting in
-// it (a long sequence starting in a granule is the last one starting there, since it runs
-// past the granule's end). One block of threads stages cu in shared memory (when it fits),
-// takes contiguous runs of granules, counts, scans, then writes.
+// The device computes this in parallel over windows: every record's first query token
+// falls in exactly one window [kWin w, kWin w + kWin), which holds (i) the pieces of the
+// long sequence that covers the window's first token, if it started earlier, then (ii) the
+// records of the sequences starting in it, found by one walk over them. One block of
+// threads stages cu in shared memory (when it fits); each warp walks a contiguous run of
+// windows (its lanes test 32 candidate group members at once and write pieces side by
+// side), counts, the warps' counts are scanned, then the warps walk again to write.
 #include "pk_dev.cuh"
 
 namespace pk {
 
 namespace {
 
-constexpr int kSchedThreads = 1024;
+constexpr int kSchedThreads = 32 * kSchedWarps;
 // cu is staged in shared memory when it has at most this many entries (192 KB); longer lists
 // are searched in global memory
 constexpr int kStageMax = 48 * 1024;
@@ -35,28 +37,6 @@ struct GlobalCu {
 __device__ __forceinline__ uint32_t ld_cu(GlobalCu cu, uint32_t i) { return __ldg(cu.p + i); }
 // cu as the staged copy in shared memory
 __device__ __forceinline__ uint32_t ld_cu(const uint32_t* cu, uint32_t i) { return cu[i]; }
-
-// first index s in [0, n) with cu[s] >= v, or n
-template <class CuPtr>
-__device__ __forceinline__ uint32_t lower_bound_cu(CuPtr cu, uint32_t n, uint64_t v) {
-  uint32_t lo = 0, hi = n;
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi) >> 1;
-    if (static_cast<uint64_t>(ld_cu(cu, mid)) < v) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
-
-// first index s in [0, n) with cu[s] > v, or n
-template <class CuPtr>
-__device__ __forceinline__ uint32_t upper_bound_cu(CuPtr cu, uint32_t n, uint64_t v) {
-  uint32_t lo = 0, hi = n;
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi) >> 1;
-    if (static_cast<uint64_t>(ld_cu(cu, mid)) <= v) lo = mid + 1; else hi = mid;
-  }
-  return lo;
-}
 
 template <class CuPtr>
 __device__ __forceinline__ TileRec piece(CuPtr cu, uint32_t s, uint32_t i0, int window) {
@@ -80,126 +60,182 @@ __device__ __forceinline__ TileRec piece(CuPtr cu, uint32_t s, uint32_t i0, int 
   return r;
 }
 
-// Calls emit(record) for each record whose first query token falls in granule b, in
-// increasing q0 (at most three; no array, so nothing goes to local memory).
-template <class CuPtr, class Emit>
-__device__ __forceinline__ void granule_visit(CuPtr cu, uint32_t S, int window, uint64_t b, Emit&& emit) {
-  const uint64_t G0 = b * kGrain, G1 = G0 + kGrain;
-  // (i) the sequence holding token G0, if it started earlier and is long
-  {
-    const uint32_t sc = upper_bound_cu(cu, S + 1, G0) - 1;  // largest s with cu[s] <= G0
-    if (sc < S) {
-      const uint64_t start = ld_cu(cu, sc), end = ld_cu(cu, sc + 1);
-      if (start < G0 && end - start > static_cast<uint64_t>(kShort)) {
-        const uint64_t i0 = ((G0 - start + kBR - 1) / kBR) * kBR;
-        if (start + i0 < end && start + i0 < G1) emit(piece(cu, sc, static_cast<uint32_t>(i0), window));
-      }
+// The record sink of a warp's walk: every lane calls it with the same arguments, and the
+// write position stays warp-uniform.
+struct WriteSink {
+  TileRec* tiles;
+  uint64_t cap;
+  uint32_t at;
+  __device__ __forceinline__ void put(uint32_t i, const TileRec& r) const {
+    if (i < cap) {
+      uint4* d = reinterpret_cast<uint4*>(tiles + i);
+      d[0] = make_uint4(r.q0, r.rows, r.k0, r.nk);
+      d[1] = make_uint4(r.seq, r.nseq, r.kind, r.ktiles);
     }
   }
-  // sequences whose first token falls in [G0, G1)
-  const uint32_t s_lo = lower_bound_cu(cu, S, G0);
-  const uint32_t s_hi = lower_bound_cu(cu, S, G1);
-  if (s_lo < s_hi) {
-    const uint32_t last = s_hi - 1;
-    const bool last_long = ld_cu(cu, last + 1) - ld_cu(cu, last) > static_cast<uint32_t>(kShort);
-    const uint32_t m_end = last_long ? last : s_hi;  // members [s_lo, m_end)
-    if (m_end > s_lo) {
-      const uint32_t q0 = ld_cu(cu, s_lo);
-      const uint32_t rows = ld_cu(cu, m_end) - q0;
-      if (rows > 0) {
-        TileRec r;
-        r.q0 = q0;
-        r.rows = rows;
-        r.k0 = q0;
-        r.nk = rows;
-        r.seq = s_lo;
-        r.nseq = m_end - s_lo;
-        r.kind = 1;
-        r.ktiles = (rows + kBC - 1) / kBC;
-        emit(r);
-      }
+  // k pieces of sequence s at rows i0, i0 + 128, ...: lane l writes pieces l, l + 32, ...
+  template <class CuPtr>
+  __device__ __forceinline__ void pieces(CuPtr cu, uint32_t s, uint32_t i0, uint32_t k, int window, int lane) {
+    for (uint32_t i = lane; i < k; i += 32) put(at + i, piece(cu, s, i0 + i * kBR, window));
+    at += k;
+  }
+  __device__ __forceinline__ void group(uint32_t s, uint32_t e, uint32_t c0, uint32_t ce, int lane) {
+    if (lane == 0) {
+      TileRec r;
+      r.q0 = c0;
+      r.rows = ce - c0;
+      r.k0 = c0;
+      r.nk = ce - c0;
+      r.seq = s;
+      r.nseq = e - s;
+      r.kind = 1;
+      r.ktiles = (r.rows + kBC - 1) / kBC;
+      put(at, r);
     }
-    if (last_long) emit(piece(cu, last, 0, window));
+    ++at;
+  }
+};
+
+// First index i in [lo, hi) with cu[i] >= v (strict: cu[i] > v), or hi, found by the
+// lanes of a warp together: each round splits [lo, hi) into 32 blocks, tests the last entry
+// of each, and keeps the first block whose test holds (a 32-way search: about three
+// dependent loads for 32K entries). Called by every lane with the same arguments.
+template <class CuPtr>
+__device__ __forceinline__ uint32_t warp_search(CuPtr cu, uint32_t lo, uint32_t hi, uint64_t v, bool strict,
+                                                int lane) {
+  while (lo < hi) {
+    const uint32_t step = (hi - lo + 31) / 32;
+    const uint64_t end = static_cast<uint64_t>(lo) + static_cast<uint64_t>(lane + 1) * step;
+    const uint32_t q = static_cast<uint32_t>(min(end, static_cast<uint64_t>(hi))) - 1;  // last of block `lane`
+    bool pred = false;
+    if (static_cast<uint64_t>(lo) + static_cast<uint64_t>(lane) * step < hi) {
+      const uint64_t c = ld_cu(cu, q);
+      pred = strict ? c > v : c >= v;
+    }
+    const unsigned int m = __ballot_sync(0xffffffffu, pred);
+    if (m == 0u) return hi;
+    const uint32_t k = static_cast<uint32_t>(__ffs(m) - 1);
+    const uint32_t qk = static_cast<uint32_t>(min(static_cast<uint64_t>(lo) + static_cast<uint64_t>(k + 1) * step,
+                                                  static_cast<uint64_t>(hi))) - 1;
+    lo += k * step;  // the answer is in [lo + k step, qk], and qk holds
+    hi = qk;
+  }
+  return hi;
+}
+
+// One warp walks window w = [kWin w, kWin w + kWin) and hands its records to the sink in
+// increasing q0. The sequences starting in the window are read 32 at a time (lane l holds
+// sequence base + l); groups are closed with ballots over those registers.
+template <class CuPtr, class Sink>
+__device__ __forceinline__ void window_visit(CuPtr cu, uint32_t S, int window, uint64_t w, int lane, Sink& sink) {
+  const uint64_t W0 = w * kWin, W1 = W0 + kWin;
+  const uint32_t s_lo = warp_search(cu, 0u, S, W0, false, lane);  // first sequence starting at or after W0
+  const uint32_t s_hi = warp_search(cu, s_lo, S, W1, false, lane);
+  // (i) the pieces in this window of the long sequence holding token W0, if it started
+  // earlier: the last sequence starting before W0, when the next one starts after W0
+  if (s_lo > 0 && (s_lo == S || ld_cu(cu, s_lo) > W0)) {
+    const uint32_t sc = s_lo - 1;
+    const uint64_t start = ld_cu(cu, sc), end = ld_cu(cu, sc + 1);
+    if (end - start > static_cast<uint64_t>(kShort)) {
+      const uint64_t i0 = ((W0 - start + kBR - 1) / kBR) * kBR;
+      const uint64_t lim = min(end, W1) - start;  // pieces start below lim
+      if (i0 < lim)
+        sink.pieces(cu, sc, static_cast<uint32_t>(i0), static_cast<uint32_t>((lim - i0 + kBR - 1) / kBR), window, lane);
+    }
+  }
+  // (ii) the sequences starting in [W0, W1), in order
+  bool open = false;    // a group is open: first member gs, first token g0
+  uint32_t gs = 0, g0 = 0;
+  for (uint32_t base = s_lo; base < s_hi; base += 32) {
+    const uint32_t j = base + static_cast<uint32_t>(lane);
+    const bool valid = j < s_hi;
+    const uint32_t cj = j <= S ? ld_cu(cu, j) : 0u;       // cu[j]
+    const uint32_t cj1 = valid ? ld_cu(cu, j + 1) : 0u;   // cu[j + 1]
+    const bool is_long = valid && cj1 - cj > static_cast<uint32_t>(kShort);
+    const unsigned int longs = __ballot_sync(0xffffffffu, is_long);
+    uint32_t p = base;  // the next sequence of this chunk not yet placed
+    while (p < s_hi && p < base + 32) {
+      const uint32_t off = p - base;
+      if (open) {
+        // the open group takes p, p + 1, ... until one is outside the window, long, or ends
+        // past g0 + 128
+        const bool stop = lane >= static_cast<int>(off) && (!valid || is_long || cj1 - g0 > static_cast<uint32_t>(kBR));
+        const unsigned int ends = __ballot_sync(0xffffffffu, stop);
+        if (ends == 0u) break;  // it runs into the next chunk
+        const uint32_t e_off = static_cast<uint32_t>(__ffs(ends) - 1);
+        const uint32_t ce = __shfl_sync(0xffffffffu, cj, static_cast<int>(e_off));  // cu[e]
+        if (ce > g0) sink.group(gs, base + e_off, g0, ce, lane);
+        open = false;
+        p = base + e_off;
+        continue;
+      }
+      if ((longs >> off) & 1u) {
+        // a long sequence: its pieces that start in this window
+        const uint32_t c0 = __shfl_sync(0xffffffffu, cj, static_cast<int>(off));
+        const uint32_t c1 = __shfl_sync(0xffffffffu, cj1, static_cast<int>(off));
+        const uint64_t lim = min(static_cast<uint64_t>(c1), W1) - c0;
+        sink.pieces(cu, p, 0u, static_cast<uint32_t>((lim + kBR - 1) / kBR), window, lane);
+        ++p;
+        continue;
+      }
+      // a short sequence opens a group
+      open = true;
+      gs = p;
+      g0 = __shfl_sync(0xffffffffu, cj, static_cast<int>(off));
+      ++p;
+    }
+  }
+  // a group still open at the window's last sequence ends there
+  if (open) {
+    const uint32_t ce = ld_cu(cu, s_hi);
+    if (ce > g0) sink.group(gs, s_hi, g0, ce, lane);
   }
 }
 
-// Count, scan and write the records, reading cu through `cu` (the staged shared copy or the
+// Walk, scan and place the records, reading cu through `cu` (the staged shared copy or the
 // caller's array; the body is instantiated for each so that loads use their own space).
+// Warp k takes a contiguous run of windows and writes their records, in order, to its own
+// staging slots; the warps' counts are scanned and each warp copies its run into place, so
+// the runs follow in q0 order.
 template <class CuPtr>
 __device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int window, TileRec* __restrict__ tiles,
-                                              long long cap, Ctl* ctl, uint32_t* s_warp) {
+                                              long long cap, TileRec* __restrict__ stage, Ctl* ctl,
+                                              uint32_t* s_warp) {
   const int tid = threadIdx.x;
-  const int nthr = blockDim.x;
-  const uint64_t NB = (static_cast<uint64_t>(T) + kGrain - 1) / kGrain;
-  const uint64_t per = (NB + nthr - 1) / nthr;
-  const uint64_t b0 = min(NB, per * tid), b1 = min(NB, b0 + per);
-  // one granule per thread (T <= 64 x threads): its records stay in registers from the count
-  // to the write; otherwise they are enumerated twice
-  const bool single = per <= 1;
-  TileRec g0{}, g1{}, g2{};
-  uint32_t count = 0;
-  if (single) {
-    if (b0 < b1)
-      granule_visit(cu, S, window, b0, [&](const TileRec& r) {
-        if (count == 0)
-          g0 = r;
-        else if (count == 1)
-          g1 = r;
-        else
-          g2 = r;
-        ++count;
-      });
-  } else {
-    for (uint64_t b = b0; b < b1; ++b) granule_visit(cu, S, window, b, [&](const TileRec&) { ++count; });
-  }
-
-  // exclusive scan of the per-thread counts
   const int lane = tid & 31, warp = tid >> 5;
-  uint32_t incl = count;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) s_warp[warp] = incl;
+  const uint64_t NB = (static_cast<uint64_t>(T) + kWin - 1) / kWin;
+  const uint64_t per = (NB + kSchedWarps - 1) / kSchedWarps;
+  const uint64_t b0 = min(NB, per * warp), b1 = min(NB, b0 + per);
+  const uint64_t slots = per * kWinCap;
+  WriteSink st{stage + static_cast<uint64_t>(warp) * slots, slots, 0u};
+  for (uint64_t b = b0; b < b1; ++b) window_visit(cu, static_cast<uint32_t>(S), window, b, lane, st);
+  const uint32_t count = st.at;
+
+  // exclusive scan of the per-warp counts (the block barriers also make the staged records
+  // visible to every lane)
+  if (lane == 0) s_warp[warp] = count;
   __syncthreads();
   if (warp == 0) {
-    const int nw = nthr / 32;
-    uint32_t x = lane < nw ? s_warp[lane] : 0u;
+    uint32_t x = lane < kSchedWarps ? s_warp[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t v = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += v;
     }
-    if (lane < nw) s_warp[lane] = x;  // inclusive over warps
+    if (lane < kSchedWarps) s_warp[lane] = x;  // inclusive
   }
   __syncthreads();
-  const uint32_t base = (warp ? s_warp[warp - 1] : 0u) + incl - count;
-  const uint32_t total = s_warp[nthr / 32 - 1];
-
-  uint32_t at = base;
-  auto put = [&](const TileRec& r) {
-    if (at < static_cast<uint64_t>(cap)) {
-      uint4* d = reinterpret_cast<uint4*>(tiles + at);
-      d[0] = make_uint4(r.q0, r.rows, r.k0, r.nk);
-      d[1] = make_uint4(r.seq, r.nseq, r.kind, r.ktiles);
-    }
-    ++at;
-  };
-  if (single) {
-    if (count > 0) put(g0);
-    if (count > 1) put(g1);
-    if (count > 2) put(g2);
-  } else {
-    for (uint64_t b = b0; b < b1; ++b) granule_visit(cu, S, window, b, put);
+  const uint32_t total = s_warp[kSchedWarps - 1];
+  const uint32_t base = warp ? s_warp[warp - 1] : 0u;
+  const bool fits = count <= slots && total <= static_cast<uint64_t>(cap);
+  if (fits) {
+    const uint4* src = reinterpret_cast<const uint4*>(stage + static_cast<uint64_t>(warp) * slots);
+    uint4* dst = reinterpret_cast<uint4*>(tiles + base);
+    for (uint32_t i = lane; i < 2 * count; i += 32) dst[i] = src[i];
   }
+  if (!fits && lane == 0) set_status(ctl, kErrInternal);
   if (tid == 0) {
-    if (total > static_cast<uint64_t>(cap)) {
-      ctl->ntiles = 0;
-      set_status(ctl, kErrInternal);
-    } else {
-      ctl->ntiles = total;
-    }
+    ctl->ntiles = total <= static_cast<uint64_t>(cap) ? total : 0u;
     ctl->next = 0;
   }
 }
@@ -208,10 +244,10 @@ __device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int 
 
 __global__ void __launch_bounds__(kSchedThreads)
 pk_schedule_kernel(const uint32_t* __restrict__ cu_g, int S, long long T, int window,
-                   TileRec* __restrict__ tiles, long long cap, Ctl* ctl) {
+                   TileRec* __restrict__ tiles, long long cap, TileRec* __restrict__ stage, Ctl* ctl) {
   extern __shared__ uint32_t s_cu[];
   __shared__ int s_bad;
-  __shared__ uint32_t s_warp[kSchedThreads / 32];
+  __shared__ uint32_t s_warp[kSchedWarps];
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
   // the attention kernel may start its set-up now; it reads the records only after this
@@ -220,7 +256,15 @@ pk_schedule_kernel(const uint32_t* __restrict__ cu_g, int S, long long T, int wi
   const bool staged = S + 1 <= kStageMax;
   if (tid == 0) s_bad = 0;
   if (staged) {
-    for (int s = tid; s <= S; s += nthr) s_cu[s] = __ldg(cu_g + s);
+    // eight loads in flight per thread
+    for (int s0 = tid; s0 <= S; s0 += 8 * nthr) {
+      uint32_t v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = s0 + k * nthr <= S ? __ldg(cu_g + s0 + k * nthr) : 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (s0 + k * nthr <= S) s_cu[s0 + k * nthr] = v[k];
+    }
     __syncthreads();
     if (tid == 0 && (s_cu[0] != 0u || static_cast<long long>(s_cu[S]) != T)) s_bad = 1;
     for (int s = tid; s < S; s += nthr)
@@ -241,9 +285,9 @@ pk_schedule_kernel(const uint32_t* __restrict__ cu_g, int S, long long T, int wi
     return;
   }
   if (staged)
-    schedule_body(static_cast<const uint32_t*>(s_cu), S, T, window, tiles, cap, ctl, s_warp);
+    schedule_body(static_cast<const uint32_t*>(s_cu), S, T, window, tiles, cap, stage, ctl, s_warp);
   else
-    schedule_body(GlobalCu{cu_g}, S, T, window, tiles, cap, ctl, s_warp);
+    schedule_body(GlobalCu{cu_g}, S, T, window, tiles, cap, stage, ctl, s_warp);
 }
 
 // The carve-out matches the attention kernel's (all shared memory), so that the SMs need
@@ -256,10 +300,11 @@ cudaError_t schedule_prepare() {
                               cudaSharedmemCarveoutMaxShared);
 }
 
+// `stage` holds schedule_stage_records(T) records of scratch.
 cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, TileRec* tiles, long long cap,
-                            Ctl* ctl, cudaStream_t stream) {
+                            TileRec* stage, Ctl* ctl, cudaStream_t stream) {
   const size_t smem = S + 1 <= kStageMax ? static_cast<size_t>(S + 1) * sizeof(uint32_t) : 0;
-  pk_schedule_kernel<<<1, kSchedThreads, smem, stream>>>(cu, S, T, window, tiles, cap, ctl);
+  pk_schedule_kernel<<<1, kSchedThreads, smem, stream>>>(cu, S, T, window, tiles, cap, stage, ctl);
   return cudaGetLastError();
 }
 

@@ -322,11 +322,15 @@ def pin_widen(orc) -> list[str]:
 
 BR = 128
 SHORT = 64
-GRAIN = 64
+WIN = 1024
 
 
 def schedule_failures(tiles: np.ndarray, cu: np.ndarray, window: int) -> list[str]:
-    """Properties that fix the schedule's records uniquely."""
+    """Properties that fix the schedule's records uniquely: the rows partition [0, T) in
+    order; long sequences are cut at rows 0, 128, ...; short sequences are packed greedily,
+    window by window (a group starts where the previous record of its window's run ended
+    and stops only where the next sequence is long, belongs to another window or would
+    take it past 128 rows); every key range is the hull of its rows' visible keys."""
     fails = []
     cu = np.asarray(cu, dtype=np.int64)
     S = cu.shape[0] - 1
@@ -346,7 +350,10 @@ def schedule_failures(tiles: np.ndarray, cu: np.ndarray, window: int) -> list[st
         fails.append("rows outside [1, 128]")
     if np.any(kt != (nk + 127) // 128):
         fails.append("ktiles")
-    grains_seen = set()
+
+    def short_in(s, w):
+        return 0 <= s < S and lens[s] <= SHORT and int(cu[s]) // WIN == w
+
     for n in range(t.shape[0]):
         s0, ns = int(seq[n]), int(nseq[n])
         if not (0 <= s0 and s0 + ns <= S and ns >= 1):
@@ -354,19 +361,18 @@ def schedule_failures(tiles: np.ndarray, cu: np.ndarray, window: int) -> list[st
             continue
         if kind[n] == 1:
             members = range(s0, s0 + ns)
-            g = {int(cu[s]) // GRAIN for s in members}
-            if len(g) != 1 or any(lens[s] > SHORT for s in members):
+            w = int(cu[s0]) // WIN
+            if any(not short_in(s, w) for s in members):
                 fails.append("group members")
-            g = g.pop() if len(g) == 1 else -1
-            if g in grains_seen:
-                fails.append("two groups in one granule")
-            grains_seen.add(g)
             if int(cu[s0]) != q0[n] or int(cu[s0 + ns]) != q0[n] + rows[n]:
                 fails.append("group rows")
-            # maximal: the neighbours outside are not short members of the same granule
-            for s in (s0 - 1, s0 + ns):
-                if 0 <= s < S and lens[s] <= SHORT and int(cu[s]) // GRAIN == g:
-                    fails.append("group not maximal")
+            # greedy: the next sequence of the run would not fit ...
+            s1 = s0 + ns
+            if short_in(s1, w) and int(cu[s1 + 1]) - q0[n] <= BR:
+                fails.append("group not maximal")
+            # ... and the run's previous sequence closed the previous group
+            if short_in(s0 - 1, w) and not (n > 0 and kind[n - 1] == 1 and seq[n - 1] + nseq[n - 1] == s0):
+                fails.append("group does not start where the previous one ended")
         elif kind[n] == 0:
             if ns != 1 or lens[s0] <= SHORT:
                 fails.append("piece of a short sequence")
@@ -407,6 +413,16 @@ def schedule_cases():
     for k in range(6):
         lens = rng.integers(0, 300 if k % 2 else 40, size=int(rng.integers(1, 60)))
         cases.append((f"rand{k}", synth.cu_from_lens(lens), int(rng.choice([0, 1, 4, 64, 200]))))
+    # greedy packing at exactly 128 rows, and one row over
+    cases.append(("fill128", synth.cu_from_lens([64, 64, 1, 40, 40, 48, 1, 0, 127, 1]), 0))
+    # several windows of dense short sequences (groups close at window ends)
+    cases.append(("win_dense", synth.cu_from_lens(rng.integers(0, 20, size=400)), 0))
+    cases.append(("win_dense_w", synth.cu_from_lens(rng.integers(0, 20, size=400)), 5))
+    # a sequence and empty ones starting exactly at a window boundary, a short one straddling
+    # the next, a long one over several windows, single-token sequences (128-member groups)
+    edge = [1000, 24, 0, 0, 10, 1000, 20, 40, 3000] + [1] * 300 + [64] * 20
+    cases.append(("win_edges", synth.cu_from_lens(edge), 0))
+    cases.append(("win_edges_w", synth.cu_from_lens(edge), 100))
     return cases
 
 

@@ -154,11 +154,11 @@ def test_scales(pk, orc, dtype, scale):
 @pytest.mark.parametrize("window", [0, 2])
 def test_group_with_many_members(pk, orc, window):
     """A group of short sequences with more member offsets than the kernel stages in shared
-    memory (empty sequences share a granule without limit): rows find their sequence in cu."""
+    memory (a group takes any number of empty sequences): rows find their sequence in cu."""
     lens = [3] + [0] * 100 + [5] + [0] * 50 + [7, 2] + [0] * 20 + [40, 200]
     wl = synth.make_lens_workload("members", lens, "bf16", H=2, window=window, seed=12)
     sched = orc.schedule(wl.cu, window)
-    assert int(sched[:, 5].max()) > 66  # nseq of the group
+    assert int(sched[:, 5].max()) > 130  # nseq of the group: past the staged offsets
     _check(pk, orc, wl)
 
 

@@ -25,6 +25,8 @@ MUTANTS = {
     7: "keys used as values",
     8: "key range one short at the window's far edge",
     9: "key range one too wide at the window's near edge",
+    10: "group of short sequences one row over the tile",
+    11: "group of short sequences crossing its window",
 }
 
 
