@@ -26,10 +26,16 @@ constexpr int kCapUnit = 64;
 // window's end (17): 66 at most. The scheduler's single walk writes a warp's records to
 // slots of this many per window, then copies them into place.
 constexpr int kWinCap = 72;
-constexpr int kSchedWarps = 32;  // warps of the scheduler's block
+constexpr int kSchedWarps = 32;  // warps of each scheduler block
+constexpr int kSchedCtas = 4;    // blocks of the scheduler's cluster when one block has too few warps
+// blocks of the scheduler's one cluster for T tokens: one while a block has a warp per window
+__host__ __device__ constexpr int schedule_ctas(long long T) {
+  return (T + kWin - 1) / kWin <= kSchedWarps ? 1 : kSchedCtas;
+}
 // staging slots (records) the scheduler needs for T tokens
 __host__ __device__ constexpr long long schedule_stage_records(long long T) {
-  return ((T + kWin - 1) / kWin + kSchedWarps - 1) / kSchedWarps * kSchedWarps * kWinCap;
+  return ((T + kWin - 1) / kWin + kSchedWarps * schedule_ctas(T) - 1) / (kSchedWarps * schedule_ctas(T)) *
+         (kSchedWarps * schedule_ctas(T)) * kWinCap;
 }
 constexpr int kRec = 8;        // uint32 per tile record
 

@@ -19,7 +19,11 @@
 // threads stages cu in shared memory (when it fits); each warp walks a contiguous run of
 // windows (its lanes test 32 candidate group members at once and write pieces side by
 // side), counts, the warps' counts are scanned, then the warps walk again to write.
+#include <cooperative_groups.h>
+
 #include "pk_dev.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace pk {
 
@@ -194,47 +198,51 @@ __device__ __forceinline__ void window_visit(CuPtr cu, uint32_t S, int window, u
 
 // Walk, scan and place the records, reading cu through `cu` (the staged shared copy or the
 // caller's array; the body is instantiated for each so that loads use their own space).
-// Warp k takes a contiguous run of windows and writes their records, in order, to its own
-// staging slots; the warps' counts are scanned and each warp copies its run into place, so
-// the runs follow in q0 order.
+// The C blocks of the cluster (schedule_ctas) hold kSchedWarps warps each; global warp gw =
+// warp x C + rank takes a contiguous run of windows (so consecutive runs are spread over the
+// blocks) and writes their records, in order, to its own staging slots. The warps'
+// counts, exchanged through distributed shared memory, give each warp the position of its
+// run, which it then copies into place: the runs follow in q0 order.
 template <class CuPtr>
 __device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int window, TileRec* __restrict__ tiles,
                                               long long cap, TileRec* __restrict__ stage, Ctl* ctl,
-                                              uint32_t* s_warp) {
+                                              uint32_t* s_warp, cg::cluster_group& cluster) {
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster.block_rank(), C = cluster.num_blocks();
+  const uint32_t G = kSchedWarps * C;
+  const uint32_t gw = static_cast<uint32_t>(warp) * C + rank;
   const uint64_t NB = (static_cast<uint64_t>(T) + kWin - 1) / kWin;
-  const uint64_t per = (NB + kSchedWarps - 1) / kSchedWarps;
-  const uint64_t b0 = min(NB, per * warp), b1 = min(NB, b0 + per);
+  const uint64_t per = (NB + G - 1) / G;
+  const uint64_t b0 = min(NB, per * gw), b1 = min(NB, b0 + per);
   const uint64_t slots = per * kWinCap;
-  WriteSink st{stage + static_cast<uint64_t>(warp) * slots, slots, 0u};
+  WriteSink st{stage + static_cast<uint64_t>(gw) * slots, slots, 0u};
   for (uint64_t b = b0; b < b1; ++b) window_visit(cu, static_cast<uint32_t>(S), window, b, lane, st);
   const uint32_t count = st.at;
 
-  // exclusive scan of the per-warp counts (the block barriers also make the staged records
-  // visible to every lane)
+  // every warp's count, then this warp's position: the sum over the warps before it
   if (lane == 0) s_warp[warp] = count;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t x = lane < kSchedWarps ? s_warp[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += v;
-    }
-    if (lane < kSchedWarps) s_warp[lane] = x;  // inclusive
+  cluster.sync();  // (also orders the staged records before the copies below)
+  uint32_t before = 0, total = 0;
+  for (uint32_t k = lane; k < G; k += 32) {
+    const uint32_t v = cluster.map_shared_rank(s_warp, k % C)[k / C];
+    total += v;
+    if (k < gw) before += v;
   }
-  __syncthreads();
-  const uint32_t total = s_warp[kSchedWarps - 1];
-  const uint32_t base = warp ? s_warp[warp - 1] : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+  }
+  cluster.sync();  // no block leaves while another still reads its counts
   const bool fits = count <= slots && total <= static_cast<uint64_t>(cap);
   if (fits) {
-    const uint4* src = reinterpret_cast<const uint4*>(stage + static_cast<uint64_t>(warp) * slots);
-    uint4* dst = reinterpret_cast<uint4*>(tiles + base);
+    const uint4* src = reinterpret_cast<const uint4*>(stage + static_cast<uint64_t>(gw) * slots);
+    uint4* dst = reinterpret_cast<uint4*>(tiles + before);
     for (uint32_t i = lane; i < 2 * count; i += 32) dst[i] = src[i];
   }
   if (!fits && lane == 0) set_status(ctl, kErrInternal);
-  if (tid == 0) {
+  if (rank == 0 && tid == 0) {
     ctl->ntiles = total <= static_cast<uint64_t>(cap) ? total : 0u;
     ctl->next = 0;
   }
@@ -242,12 +250,15 @@ __device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int 
 
 }  // namespace
 
+// One cluster of schedule_ctas(T) blocks. Every block stages cu (when it fits) and checks it;
+// a malformed cu sends all of them out before the first cluster barrier.
 __global__ void __launch_bounds__(kSchedThreads)
 pk_schedule_kernel(const uint32_t* __restrict__ cu_g, int S, long long T, int window,
                    TileRec* __restrict__ tiles, long long cap, TileRec* __restrict__ stage, Ctl* ctl) {
   extern __shared__ uint32_t s_cu[];
   __shared__ int s_bad;
   __shared__ uint32_t s_warp[kSchedWarps];
+  cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
   // the attention kernel may start its set-up now; it reads the records only after this
@@ -277,7 +288,7 @@ pk_schedule_kernel(const uint32_t* __restrict__ cu_g, int S, long long T, int wi
   }
   __syncthreads();
   if (s_bad) {
-    if (tid == 0) {
+    if (cluster.block_rank() == 0 && tid == 0) {
       ctl->ntiles = 0;
       ctl->next = 0;
       set_status(ctl, kErrBadCu);
@@ -285,9 +296,9 @@ pk_schedule_kernel(const uint32_t* __restrict__ cu_g, int S, long long T, int wi
     return;
   }
   if (staged)
-    schedule_body(static_cast<const uint32_t*>(s_cu), S, T, window, tiles, cap, stage, ctl, s_warp);
+    schedule_body(static_cast<const uint32_t*>(s_cu), S, T, window, tiles, cap, stage, ctl, s_warp, cluster);
   else
-    schedule_body(GlobalCu{cu_g}, S, T, window, tiles, cap, stage, ctl, s_warp);
+    schedule_body(GlobalCu{cu_g}, S, T, window, tiles, cap, stage, ctl, s_warp, cluster);
 }
 
 // The carve-out matches the attention kernel's (all shared memory), so that the SMs need
@@ -304,8 +315,25 @@ cudaError_t schedule_prepare() {
 cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, TileRec* tiles, long long cap,
                             TileRec* stage, Ctl* ctl, cudaStream_t stream) {
   const size_t smem = S + 1 <= kStageMax ? static_cast<size_t>(S + 1) * sizeof(uint32_t) : 0;
-  pk_schedule_kernel<<<1, kSchedThreads, smem, stream>>>(cu, S, T, window, tiles, cap, stage, ctl);
-  return cudaGetLastError();
+  const int ctas = schedule_ctas(T);
+  if (ctas == 1) {
+    // a lone block is a cluster of one without the cluster launch
+    pk_schedule_kernel<<<1, kSchedThreads, smem, stream>>>(cu, S, T, window, tiles, cap, stage, ctl);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.blockDim = dim3(kSchedThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ctas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pk_schedule_kernel, cu, S, T, window, tiles, cap, stage, ctl);
 }
 
 }  // namespace pk

@@ -29,6 +29,12 @@ def _sched_cases():
         lens += [L, 1, L]
     cases.append(("boundaries", synth.cu_from_lens(lens), 0))
     cases.append(("boundaries_w", synth.cu_from_lens(lens), 100))
+    # more sequences than the scheduler stages in shared memory (cu read from global memory),
+    # over enough windows for a cluster of scheduler blocks, with 128-member groups
+    rng = np.random.default_rng(77)
+    cases.append(("many_tiny", synth.cu_from_lens(rng.integers(0, 4, size=60000)), 0))
+    cases.append(("many_tiny_mixed", synth.cu_from_lens(
+        np.where(rng.random(52000) < 0.01, rng.integers(65, 600, size=52000), rng.integers(0, 3, size=52000))), 3))
     return cases
 
 
