@@ -33,6 +33,9 @@ constexpr int kSchedThreads = 32 * kSchedWarps;
 // cu is staged in shared memory when it has at most this many entries (192 KB); longer lists
 // are searched in global memory
 constexpr int kStageMax = 48 * 1024;
+// dynamic shared memory the scheduler may use: staged cu, then (when they fit) the record
+// slots of the block's warps
+constexpr int kSchedSmem = 200 * 1024;
 
 // cu as the caller's array in global memory (read-only path)
 struct GlobalCu {
@@ -205,8 +208,8 @@ __device__ __forceinline__ void window_visit(CuPtr cu, uint32_t S, int window, u
 // run, which it then copies into place: the runs follow in q0 order.
 template <class CuPtr>
 __device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int window, TileRec* __restrict__ tiles,
-                                              long long cap, TileRec* __restrict__ stage, Ctl* ctl,
-                                              uint32_t* s_warp, cg::cluster_group& cluster) {
+                                              long long cap, TileRec* __restrict__ stage, TileRec* smem_slots,
+                                              Ctl* ctl, uint32_t* s_warp, cg::cluster_group& cluster) {
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster.block_rank(), C = cluster.num_blocks();
@@ -216,16 +219,21 @@ __device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int 
   const uint64_t per = (NB + G - 1) / G;
   const uint64_t b0 = min(NB, per * gw), b1 = min(NB, b0 + per);
   const uint64_t slots = per * kWinCap;
-  WriteSink st{stage + static_cast<uint64_t>(gw) * slots, slots, 0u};
+  // this warp's slots: in shared memory when the launch found room, else in the workspace
+  TileRec* mine = smem_slots ? smem_slots + static_cast<uint64_t>(warp) * slots : stage + static_cast<uint64_t>(gw) * slots;
+  WriteSink st{mine, slots, 0u};
   for (uint64_t b = b0; b < b1; ++b) window_visit(cu, static_cast<uint32_t>(S), window, b, lane, st);
   const uint32_t count = st.at;
 
   // every warp's count, then this warp's position: the sum over the warps before it
   if (lane == 0) s_warp[warp] = count;
-  cluster.sync();  // (also orders the staged records before the copies below)
+  if (C == 1)
+    __syncthreads();  // (also orders the staged records before the copies below)
+  else
+    cluster.sync();
   uint32_t before = 0, total = 0;
   for (uint32_t k = lane; k < G; k += 32) {
-    const uint32_t v = cluster.map_shared_rank(s_warp, k % C)[k / C];
+    const uint32_t v = C == 1 ? s_warp[k] : cluster.map_shared_rank(s_warp, k % C)[k / C];
     total += v;
     if (k < gw) before += v;
   }
@@ -234,10 +242,10 @@ __device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int 
     before += __shfl_xor_sync(0xffffffffu, before, o);
     total += __shfl_xor_sync(0xffffffffu, total, o);
   }
-  cluster.sync();  // no block leaves while another still reads its counts
+  if (C > 1) cluster.sync();  // no block leaves while another still reads its counts
   const bool fits = count <= slots && total <= static_cast<uint64_t>(cap);
   if (fits) {
-    const uint4* src = reinterpret_cast<const uint4*>(stage + static_cast<uint64_t>(gw) * slots);
+    const uint4* src = reinterpret_cast<const uint4*>(mine);
     uint4* dst = reinterpret_cast<uint4*>(tiles + before);
     for (uint32_t i = lane; i < 2 * count; i += 32) dst[i] = src[i];
   }
@@ -254,8 +262,11 @@ __device__ __forceinline__ void schedule_body(CuPtr cu, int S, long long T, int 
 // a malformed cu sends all of them out before the first cluster barrier.
 __global__ void __launch_bounds__(kSchedThreads)
 pk_schedule_kernel(const uint32_t* __restrict__ cu_g, int S, long long T, int window,
-                   TileRec* __restrict__ tiles, long long cap, TileRec* __restrict__ stage, Ctl* ctl) {
-  extern __shared__ uint32_t s_cu[];
+                   TileRec* __restrict__ tiles, long long cap, TileRec* __restrict__ stage, Ctl* ctl,
+                   unsigned int slots_at) {
+  extern __shared__ __align__(16) uint32_t s_cu[];
+  // record slots in shared memory past the staged cu (slots_at bytes in), or none
+  TileRec* smem_slots = slots_at ? reinterpret_cast<TileRec*>(reinterpret_cast<char*>(s_cu) + slots_at) : nullptr;
   __shared__ int s_bad;
   __shared__ uint32_t s_warp[kSchedWarps];
   cg::cluster_group cluster = cg::this_cluster();
@@ -296,16 +307,17 @@ pk_schedule_kernel(const uint32_t* __restrict__ cu_g, int S, long long T, int wi
     return;
   }
   if (staged)
-    schedule_body(static_cast<const uint32_t*>(s_cu), S, T, window, tiles, cap, stage, ctl, s_warp, cluster);
+    schedule_body(static_cast<const uint32_t*>(s_cu), S, T, window, tiles, cap, stage, smem_slots, ctl, s_warp,
+                  cluster);
   else
-    schedule_body(GlobalCu{cu_g}, S, T, window, tiles, cap, stage, ctl, s_warp, cluster);
+    schedule_body(GlobalCu{cu_g}, S, T, window, tiles, cap, stage, smem_slots, ctl, s_warp, cluster);
 }
 
 // The carve-out matches the attention kernel's (all shared memory), so that the SMs need
 // no reconfiguration between the two kernels of a call.
 cudaError_t schedule_prepare() {
   cudaError_t e = cudaFuncSetAttribute(pk_schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kStageMax * static_cast<int>(sizeof(uint32_t)));
+                                       kSchedSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(pk_schedule_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                               cudaSharedmemCarveoutMaxShared);
@@ -314,11 +326,18 @@ cudaError_t schedule_prepare() {
 // `stage` holds schedule_stage_records(T) records of scratch.
 cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, TileRec* tiles, long long cap,
                             TileRec* stage, Ctl* ctl, cudaStream_t stream) {
-  const size_t smem = S + 1 <= kStageMax ? static_cast<size_t>(S + 1) * sizeof(uint32_t) : 0;
   const int ctas = schedule_ctas(T);
+  // staged cu (when it fits), then the block's record slots (when they fit too)
+  const size_t cu_bytes = S + 1 <= kStageMax ? (static_cast<size_t>(S + 1) * sizeof(uint32_t) + 15) / 16 * 16 : 0;
+  const long long nb = (T + kWin - 1) / kWin;
+  const long long per = (nb + kSchedWarps * ctas - 1) / (kSchedWarps * ctas);
+  const size_t slot_bytes = static_cast<size_t>(kSchedWarps) * per * kWinCap * sizeof(TileRec);
+  const bool in_smem = cu_bytes + slot_bytes <= static_cast<size_t>(kSchedSmem);
+  const size_t smem = in_smem ? cu_bytes + slot_bytes : cu_bytes;
+  const unsigned int slots_at = in_smem ? static_cast<unsigned int>(cu_bytes) : 0u;
   if (ctas == 1) {
     // a lone block is a cluster of one without the cluster launch
-    pk_schedule_kernel<<<1, kSchedThreads, smem, stream>>>(cu, S, T, window, tiles, cap, stage, ctl);
+    pk_schedule_kernel<<<1, kSchedThreads, smem, stream>>>(cu, S, T, window, tiles, cap, stage, ctl, slots_at);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -333,7 +352,7 @@ cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pk_schedule_kernel, cu, S, T, window, tiles, cap, stage, ctl);
+  return cudaLaunchKernelEx(&cfg, pk_schedule_kernel, cu, S, T, window, tiles, cap, stage, ctl, slots_at);
 }
 
 }  // namespace pk

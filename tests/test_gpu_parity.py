@@ -35,6 +35,9 @@ def _sched_cases():
     cases.append(("many_tiny", synth.cu_from_lens(rng.integers(0, 4, size=60000)), 0))
     cases.append(("many_tiny_mixed", synth.cu_from_lens(
         np.where(rng.random(52000) < 0.01, rng.integers(65, 600, size=52000), rng.integers(0, 3, size=52000))), 3))
+    # enough windows that the scheduler's record slots live in the workspace, not in shared memory
+    cases.append(("many_windows", synth.cu_from_lens(
+        np.where(rng.random(3000) < 0.3, rng.integers(65, 500, size=3000), rng.integers(0, 30, size=3000))), 0))
     return cases
 
 
