@@ -48,10 +48,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic of the attention kernel per launch from an ncu capture, valid only while the
 # kernel's sources have the recorded hash (kernel_source_hash; otherwise reported as null).
 NCU_TRAFFIC = {  # {config_name: (kernel_source_hash() at capture, bytes per launch)}
-    "global": ("7beb5d3ca726e91a76d52ad3c285a88966a60a76", 83515136),
-    "local": ("7beb5d3ca726e91a76d52ad3c285a88966a60a76", 428199936),
-    "long": ("7beb5d3ca726e91a76d52ad3c285a88966a60a76", 1068990976),
-    "short": ("7beb5d3ca726e91a76d52ad3c285a88966a60a76", 384982528),
+    "global": ("0110f327a2d78257ece1d2667434f2585152c20c", 83526656),
+    "local": ("0110f327a2d78257ece1d2667434f2585152c20c", 428252160),
+    "long": ("0110f327a2d78257ece1d2667434f2585152c20c", 1068187648),
+    "short": ("0110f327a2d78257ece1d2667434f2585152c20c", 381117184),
 }
 
 
