@@ -52,6 +52,8 @@ class Oracle:
         L.oracle_attend_rows.restype = i32
         L.oracle_rope.argtypes = [vp, i32, i64, vp, vp, i32, vp]
         L.oracle_rope.restype = None
+        L.oracle_rope_qkv.argtypes = [vp, i32, vp, vp, i32, i64, vp, i32, i64, i32, i32, i32, i32, vp]
+        L.oracle_rope_qkv.restype = i32
         L.oracle_schedule.argtypes = [vp, i32, i64, i32, vp, i64, ctypes.POINTER(i64)]
         L.oracle_schedule.restype = i32
         L.oracle_schedule_cap.argtypes = [i64]
@@ -123,6 +125,25 @@ class Oracle:
         y = np.zeros(64, dtype=np.float64)
         self.lib.oracle_rope(xa.ctypes.data, dx, int(pos), c.ctypes.data, s.ctypes.data, dc,
                              y.ctypes.data)
+        return y
+
+    def rope_qkv(self, qkv, cos, sin, cu, H: int, dims: int, traditional: bool, inverse: bool,
+                 dtype: str = "f64", table_dtype: str = "f64"):
+        """The standalone rotation of every q and k head vector of qkv [T, 3 H 64] (v copied),
+        f64 [T, 3 H 64]; tables cos/sin [P, dims / 2]."""
+        cu = np.ascontiguousarray(cu, dtype=np.uint32)
+        S = cu.shape[0] - 1
+        T = int(cu[-1])
+        xa, dx = self._arr(np.asarray(qkv).reshape(T, 3 * H * 64) if T else np.zeros((0, 3 * H * 64)), dtype)
+        c, dc = self._arr(cos, table_dtype)
+        s, _ = self._arr(sin, table_dtype)
+        P = int(np.asarray(cos).shape[0])
+        y = np.zeros((T, 3 * H * 64), dtype=np.float64)
+        rc = self.lib.oracle_rope_qkv(xa.ctypes.data, dx, c.ctypes.data, s.ctypes.data, dc, P,
+                                      cu.ctypes.data, S, T, H, int(dims), int(bool(traditional)),
+                                      int(bool(inverse)), y.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_rope_qkv: bad arguments")
         return y
 
     def schedule(self, cu, window: int):

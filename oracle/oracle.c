@@ -381,6 +381,78 @@ int oracle_attend_rows(const void *qkv, int dt, const void *cosb, const void *si
 }
 
 /* ---------------------------------------------------------------------------------------
+ * the standalone rotation (the pages' rope op: the first `dims` features of a head vector
+ * rotated in pairs -- the two halves, or interleaved pairs ("traditional") -- forwards, or
+ * inversely for the gradient; kime's rope step applies it to the q and k of a packed qkv)
+ *
+ * For a head vector x (64 features) at in-sequence position p, with h = dims / 2 and table
+ * entries c_j = cos[p h + j], s_j = sin[p h + j] (tables of width h):
+ *   pair j < h: (a, b) = (j, j + h) for the halves, (2j, 2j + 1) for interleaved pairs
+ *   forward:  y_a = x_a c_j - x_b s_j,   y_b = x_a s_j + x_b c_j
+ *   inverse:  y_a = x_a c_j + x_b s_j,   y_b = x_b c_j - x_a s_j   (the transposed rotation)
+ *   features dims .. 63 are copied.
+ */
+static void rope_vector(const void *x, int dt, int64_t at, int64_t pos, const void *cosb, const void *sinb,
+                        int tdt, int dims, int traditional, int inverse, double *y) {
+    const int h = dims / 2;
+    for (int f = dims; f < HD; f++) y[f] = ld(x, dt, at + f);
+#if ORACLE_MUTANT == 14
+    for (int f = dims; f < HD; f++) y[f] = 0.0;                    /* planted: tail not copied */
+#endif
+    for (int j = 0; j < h; j++) {
+#if ORACLE_MUTANT == 13
+        int a = j, b = j + h;                                      /* planted: layout ignored */
+#else
+        int a = traditional ? 2 * j : j;
+        int b = traditional ? 2 * j + 1 : j + h;
+#endif
+        double c = ld(cosb, tdt, pos * h + j), sn = ld(sinb, tdt, pos * h + j);
+        double xa = ld(x, dt, at + a), xb = ld(x, dt, at + b);
+#if ORACLE_MUTANT == 12
+        int fwd = 1;                                               /* planted: direction ignored */
+#else
+        int fwd = !inverse;
+#endif
+        if (fwd) {
+            y[a] = xa * c - xb * sn;
+            y[b] = xa * sn + xb * c;
+        } else {
+            y[a] = xa * c + xb * sn;
+            y[b] = xb * c - xa * sn;
+        }
+    }
+}
+
+/*
+ * Every q and k head vector of qkv [T, 3 H 64] rotated at its token's in-sequence position
+ * (the token minus the start of its sequence in cu); v copied. y [T, 3 H 64] in f64.
+ * Returns 0, or -1 on bad arguments (dims odd or outside [2, 64], H < 1, malformed cu, a
+ * position at or past P table rows).
+ */
+int oracle_rope_qkv(const void *qkv, int dt, const void *cosb, const void *sinb, int tdt, int64_t P,
+                    const uint32_t *cu, int S, int64_t T, int H, int dims, int traditional, int inverse,
+                    double *y) {
+    if (H < 1 || dims < 2 || dims > HD || (dims & 1) || check_cu(cu, S, T)) return -1;
+    const int64_t W = 3LL * H * HD;
+    for (int sq = 0; sq < S; sq++) {
+        for (int64_t t = cu[sq]; t < (int64_t)cu[sq + 1]; t++) {
+            const int64_t pos = t - cu[sq];
+            if (pos >= P) return -1;
+            for (int part = 0; part < 3; part++)
+                for (int hh = 0; hh < H; hh++) {
+                    const int64_t at = t * W + (int64_t)part * H * HD + (int64_t)hh * HD;
+                    if (part == 2) {
+                        for (int f = 0; f < HD; f++) y[at + f] = ld(qkv, dt, at + f);
+                    } else {
+                        rope_vector(qkv, dt, at, pos, cosb, sinb, tdt, dims, traditional, inverse, y + at);
+                    }
+                }
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------------
  * the tile schedule
  *
  * Records of 8 uint32: {q0, rows, k0, nk, seq, nseq, kind, ktiles}

@@ -317,6 +317,84 @@ def pin_widen(orc) -> list[str]:
 
 
 # ----------------------------------------------------------------------------------------
+# standalone rotation (the rope op: halves or interleaved pairs, partial dims, inverse)
+
+
+def _angle_tables(P: int, h: int, rng) -> tuple[np.ndarray, np.ndarray]:
+    """cos/sin [P, h] of random angles in f64 (c^2 + s^2 = 1 to rounding)."""
+    th = rng.uniform(-np.pi, np.pi, size=(P, h))
+    return np.cos(th), np.sin(th)
+
+
+def pin_rope_op(orc) -> list[str]:
+    fails = []
+    rng = np.random.default_rng(11)
+    H = 2
+    lens = [7, 0, 12, 1]
+    cu = synth.cu_from_lens(lens)
+    T = int(cu[-1])
+    seq, pos = token_seq_pos(cu)
+    qkv = rng.standard_normal((T, 3 * H * 64))
+    # (a) all 64 features in halves, forwards: the pinned rotation of the attention path
+    c64, s64 = synth.rope_tables(16, 10000.0)
+    y = orc.rope_qkv(qkv, c64, s64, cu, H, 64, False, False)
+    for t in range(T):
+        for part in range(2):
+            for h in range(H):
+                a = part * H * 64 + h * 64
+                if not np.allclose(y[t, a:a + 64], orc.rope(qkv[t, a:a + 64], int(pos[t]), c64, s64),
+                                   rtol=0, atol=1e-13):
+                    fails.append("rope op: full halves differ from the attention path's rotation")
+    for dims in (64, 32, 6, 2):
+        h = dims // 2
+        ct, st = _angle_tables(16, h, rng)
+        for trad in (False, True):
+            fw = orc.rope_qkv(qkv, ct, st, cu, H, dims, trad, False)
+            back = orc.rope_qkv(fw, ct, st, cu, H, dims, trad, True)
+            # (b) the inverse undoes the forward rotation
+            if not np.allclose(back, qkv, rtol=0, atol=1e-12):
+                fails.append(f"rope op: inverse(forward) != x (dims {dims}, interleaved {trad})")
+            # (e) features past dims and all of v are copied exactly
+            qk = fw[:, :2 * H * 64].reshape(T, 2 * H, 64)
+            x_qk = qkv[:, :2 * H * 64].reshape(T, 2 * H, 64)
+            if not (np.array_equal(qk[..., dims:], x_qk[..., dims:]) and
+                    np.array_equal(fw[:, 2 * H * 64:], qkv[:, 2 * H * 64:])):
+                fails.append(f"rope op: untouched features changed (dims {dims})")
+            # (f) each pair keeps its length
+            ia = np.arange(h) * 2 if trad else np.arange(h)
+            ib = ia + 1 if trad else ia + h
+            n0 = x_qk[..., ia] ** 2 + x_qk[..., ib] ** 2
+            n1 = qk[..., ia] ** 2 + qk[..., ib] ** 2
+            if not np.allclose(n0, n1, rtol=1e-12, atol=1e-12):
+                fails.append(f"rope op: pair lengths changed (dims {dims}, interleaved {trad})")
+        # (d) interleaved pairs = halves after moving feature 2j to j and 2j + 1 to j + h
+        perm = np.arange(64)
+        perm[:dims] = np.concatenate([np.arange(h) * 2, np.arange(h) * 2 + 1])
+        xp = qkv.reshape(T, 3 * H, 64)[..., perm].reshape(T, -1)
+        tr = orc.rope_qkv(qkv, ct, st, cu, H, dims, True, False).reshape(T, 3 * H, 64)
+        hv = orc.rope_qkv(xp, ct, st, cu, H, dims, False, False).reshape(T, 3 * H, 64)
+        inv_perm = np.argsort(perm)
+        if not np.allclose(tr, hv[..., inv_perm], rtol=0, atol=1e-13):
+            fails.append(f"rope op: interleaved pairs are not the permuted halves (dims {dims})")
+    # (c) direction: the first feature of pair j turns towards the second (forwards) or away
+    dims, h = 8, 4
+    ct, st = _angle_tables(16, h, rng)
+    for trad in (False, True):
+        for j in range(h):
+            a = 2 * j if trad else j
+            b = a + 1 if trad else j + h
+            e = np.zeros((T, 3 * H * 64))
+            e[:, a] = 1.0
+            fw = orc.rope_qkv(e, ct, st, cu, H, dims, trad, False)
+            iv = orc.rope_qkv(e, ct, st, cu, H, dims, trad, True)
+            cj, sj = ct[pos, j], st[pos, j]
+            if not (np.allclose(fw[:, a], cj, atol=1e-15) and np.allclose(fw[:, b], sj, atol=1e-15) and
+                    np.allclose(iv[:, a], cj, atol=1e-15) and np.allclose(iv[:, b], -sj, atol=1e-15)):
+                fails.append(f"rope op: rotation direction (pair {j}, interleaved {trad})")
+    return list(dict.fromkeys(fails))
+
+
+# ----------------------------------------------------------------------------------------
 # schedule
 
 
@@ -436,7 +514,7 @@ def pin_schedule(orc) -> list[str]:
 
 
 ALL_PINS = (pin_sdpa, pin_rope, pin_closed_forms, pin_probabilities, pin_window_and_permutation,
-            pin_widen, pin_schedule)
+            pin_widen, pin_schedule, pin_rope_op)
 
 
 def all_failures(orc) -> list[str]:

@@ -27,6 +27,9 @@ MUTANTS = {
     9: "key range one too wide at the window's near edge",
     10: "group of short sequences one row over the tile",
     11: "group of short sequences crossing its window",
+    12: "rope op: inverse rotates forwards",
+    13: "rope op: interleaved layout ignored",
+    14: "rope op: features past dims not copied",
 }
 
 
