@@ -26,6 +26,7 @@ arm, on the same workload and metric.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -334,6 +335,52 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
             "nsets": nsets, "clocks": clk.summary(), "e2e_ms": e2e_ms, "h2d": int(h2d), "d2h": int(d2h)}
 
 
+def run_rope(wl, steps, warmup, dev_index, dims=64):
+    """The standalone rotation (pk_rope) over the workload's packed qkv, out of place: q and k
+    rotated, v copied. Algorithmic bytes: qkv read once and written once, plus the tables."""
+    import torch
+
+    import rope_cu_tile_gb300 as pk
+
+    pk.load()
+    dev = torch.device("cuda", dev_index)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    e = synth.elem_size(wl.dtype)
+    qkv0, _, _, cu = device_tensors(wl, torch, dev)
+    P = max(1, int(wl.lens.max()))
+    c, s = synth.rope_tables_dims(P, dims, wl.base)
+    cos = device_tensors(dataclasses.replace(wl, cos=synth.to_storage(c, wl.dtype)), torch, dev)[1]
+    sin = device_tensors(dataclasses.replace(wl, cos=synth.to_storage(s, wl.dtype)), torch, dev)[1]
+    qkv_bytes = wl.T * 3 * wl.H * 64 * e
+    abytes = 2 * qkv_bytes + 2 * P * (dims // 2) * e + 4 * (wl.S + 1)
+    nsets = max(1, min(8, int(np.ceil(3 * L2_BYTES / (2 * qkv_bytes))))) if 2 * qkv_bytes < 2 * L2_BYTES else 1
+    sets = [(qkv0 if k == 0 else qkv0.clone(), torch.empty_like(qkv0)) for k in range(nsets)]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    def step(i):
+        x, y = sets[i % nsets]
+        pk.rope(x, cos, sin, cu, wl.H, dims, False, False, out=y, status=status, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev_index) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(steps):
+                step(warmup + i)
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device error in pk_rope")
+    ms = ev0.elapsed_time(ev1) / steps
+    return {"ms": ms, "bytes": abytes, "nsets": nsets, "clocks": clk.summary(), "dims": dims}
+
+
 def roofline(wl, attend_ms, peaks, peak_src):
     flops, abytes = work(wl)
     t_bw = abytes / (peaks["hbm_gbs"] * 1e9)
@@ -363,6 +410,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="global", choices=list(synth.CONFIG_NAMES))
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--op", default="attend", choices=["attend", "rope"],
+                    help="attend: the attention path (default); rope: the standalone rotation")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -402,6 +451,26 @@ def main():
         print(json.dumps(line))
         return
 
+    if args.op == "rope":
+        if rank != 0:
+            return
+        r = run_rope(wl, args.steps, args.warmup, local)
+        peaks, psrc = load_peaks()
+        gbs = r["bytes"] / (r["ms"] * 1e-3) / 1e9
+        cfg.update({"op": "pk_rope (q and k rotated, v copied, out of place)", "dims": r["dims"],
+                    "algorithmic_mb": r["bytes"] / 1e6,
+                    "l2": f"rotating {r['nsets']} input/output sets" if r["nsets"] > 1 else "inputs larger than L2"})
+        cfg.pop("useful_gflop", None)
+        line = {"metric": "pk_rope: GB/s on 1 GB300; % of HBM roofline", "value": gbs, "unit": "GB/s",
+                "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+                "data": "synthetic", "config": cfg,
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gbs / peaks["hbm_gbs"], "peak_source": psrc, "traffic": None,
+                             "kernel": "pk_rope_kernel"},
+                "gpu_launches": args.steps, "clocks": r["clocks"]}
+        print(json.dumps(line))
+        return
     if world > 1:
         import torch.distributed as dist
         import torch

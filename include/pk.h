@@ -172,6 +172,34 @@ int pk_attend_noalloc(int dtype, const void *qkv, const void *cos, const void *s
                       const uint32_t *cu, int S, int64_t T, int H, int window, float scale,
                       void *out, float *lse, int *status, struct CUstream_st *stream);
 
+/*
+ * pk_rope -- the standalone rotary embedding of a packed qkv: the pages' rope op
+ * (hanzo-kernel fast ops, FastOp::Rope and its graph fallback), applied as kime's rope step
+ * applies it, to every q and k head vector of qkv.
+ *   - For a head vector x (64 features) of a token at in-sequence position p (the token minus
+ *     the start of its sequence in cu), with h = dims / 2, c_j = cos[p h + j], s_j = sin[p h + j]:
+ *     pair j < h is (j, j + h) (traditional = 0: the two halves) or (2j, 2j + 1)
+ *     (traditional != 0: interleaved pairs); forwards (inverse = 0)
+ *         y_a = x_a c_j - x_b s_j,  y_b = x_a s_j + x_b c_j,
+ *     inversely (inverse != 0, the transposed rotation: the gradient of the forward one)
+ *         y_a = x_a c_j + x_b s_j,  y_b = x_b c_j - x_a s_j;
+ *     features dims .. 63 are copied. Arithmetic in fp32, one rounding to the element type.
+ *   - dtype: enum pk_dtype, for x, y, cos and sin alike.
+ *   - x, y: device [T, 3 H 64] (q | k | v blocks, heads contiguous, as pk_attend's qkv). y may
+ *     be x (in place: v is left as it is); otherwise v is copied, and x and y must not overlap.
+ *     4-byte aligned (8-byte for PK_F32).
+ *   - cos, sin: device [P, dims / 2] tables; P >= the longest sequence. Element-aligned.
+ *   - cu, S, T: as pk_attend (device cu[S + 1], cu[0] = 0, non-decreasing, cu[S] = T).
+ *   - H in [1, PK_MAX_H]; dims even in [2, 64].
+ *   - status: optional device int (NULL: none), written in stream order: PK_OK, or
+ *     PK_ERR_BAD_CU when cu is malformed or a position reaches P (such tokens are skipped).
+ *   - Returns PK_OK or PK_ERR_ARG / PK_ERR_ALIGN / PK_ERR_UNSUPPORTED / PK_ERR_CUDA (nothing
+ *     launched). Asynchronous on `stream`; allocates nothing.
+ */
+int pk_rope(int dtype, const void *x, void *y, const void *cos, const void *sin, int64_t P,
+            const uint32_t *cu, int S, int64_t T, int H, int dims, int traditional, int inverse,
+            int *status, struct CUstream_st *stream);
+
 /* Text of a status code (static storage). */
 const char *pk_status_string(int status);
 

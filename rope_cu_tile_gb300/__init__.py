@@ -30,7 +30,7 @@ NOALLOC_MAX_T = 1048576
 # names declared in include/pk.h
 EXPORTS = ("pk_attend", "pk_attend_bf16", "pk_attend_f16", "pk_attend_f32", "pk_attend_dt",
            "pk_schedule", "pk_schedule_capacity", "pk_last_status", "pk_status_string",
-           "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop", "pk_attend_noalloc")
+           "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop", "pk_attend_noalloc", "pk_rope")
 
 _lib = None
 
@@ -60,6 +60,8 @@ def load(path: str | None = None):
     L.pk_attend_dt.restype = i32
     L.pk_attend_noalloc.argtypes = [i32] + sig[:11] + [vp, vp]
     L.pk_attend_noalloc.restype = i32
+    L.pk_rope.argtypes = [i32, vp, vp, vp, vp, i64, vp, i32, i64, i32, i32, i32, i32, vp, vp]
+    L.pk_rope.restype = i32
     L.pk_schedule.argtypes = [vp, i32, i64, i32, vp, i64, ctypes.POINTER(i64), vp]
     L.pk_schedule.restype = i32
     L.pk_schedule_capacity.argtypes = [i64]
@@ -106,6 +108,11 @@ def pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse
     """The allocation-free variant (see include/pk.h): for callers that cannot let the library
     cudaMalloc a workspace; `status` is an optional device pointer to one int."""
     return load().pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, status, stream)
+
+
+def pk_rope(dtype, x, y, cos, sin, P, cu, S, T, H, dims, traditional, inverse, status, stream) -> int:
+    """The standalone rotation of the q and k head vectors of a packed qkv (see include/pk.h)."""
+    return load().pk_rope(dtype, x, y, cos, sin, P, cu, S, T, H, dims, traditional, inverse, status, stream)
 
 
 def pk_schedule(cu, S, T, window, tiles, cap, stream):
@@ -167,6 +174,34 @@ def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=N
                       _stream_handle(stream))
     _check(rc, "pk_attend")
     return out, lse
+
+
+def rope(qkv, cos, sin, cu, H: int, dims: int = 64, traditional: bool = False, inverse: bool = False,
+         out=None, status=None, stream=None):
+    """qkv [T, 3*H*64] with the first `dims` features of every q and k head vector rotated at
+    their in-sequence positions (tables cos/sin [P, dims/2] in qkv's dtype); v copied. `out`
+    may be qkv itself (in place). `status`: optional int32 device tensor of one element."""
+    torch = _torch()
+    T = qkv.shape[0]
+    S = cu.shape[0] - 1
+    if qkv.dim() != 2 or qkv.shape[1] != 3 * H * 64:
+        raise ValueError("qkv must be [T, 3*H*64]")
+    if cos.dtype != qkv.dtype or sin.dtype != qkv.dtype or cos.shape != sin.shape:
+        raise TypeError("cos/sin must have qkv's dtype and one shape")
+    if cos.dim() != 2 or cos.shape[1] != dims // 2:
+        raise ValueError("cos/sin must be [P, dims/2]")
+    if cu.dtype not in (torch.int32, torch.uint32):
+        raise TypeError("cu must be int32 or uint32")
+    for t in (qkv, cos, sin, cu):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if out is None:
+        out = torch.empty_like(qkv)
+    rc = pk_rope(dtype_code(qkv), qkv.data_ptr(), out.data_ptr(), cos.data_ptr(), sin.data_ptr(),
+                 cos.shape[0], cu.data_ptr(), S, T, H, int(dims), int(bool(traditional)), int(bool(inverse)),
+                 status.data_ptr() if status is not None else None, _stream_handle(stream))
+    _check(rc, "pk_rope")
+    return out
 
 
 def schedule(cu, T: int, window: int, stream=None):

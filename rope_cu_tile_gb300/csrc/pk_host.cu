@@ -372,14 +372,15 @@ const char* pk_status_string(int status) {
   switch (status) {
     case PK_OK: return "ok";
     case PK_ERR_ARG: return "invalid argument";
-    case PK_ERR_ALIGN: return "pointer not aligned (qkv, cos, sin, out: 16 bytes; cu, lse: 4 bytes)";
+    case PK_ERR_ALIGN: return "pointer not aligned (see the entry point's alignment rules in pk.h)";
     case PK_ERR_CUDA: return "CUDA runtime or driver call failed";
     case PK_ERR_UNSUPPORTED: return "device is not sm_103 (GB300)";
-    case PK_ERR_BAD_CU: return "cu malformed: cu[0] != 0, decreasing, or cu[S] != T";
+    case PK_ERR_BAD_CU: return "cu malformed (cu[0] != 0, decreasing, or cu[S] != T), or a position past the tables";
     case PK_ERR_TIMEOUT: return "a device wait exceeded its bound; results invalid";
     case PK_ERR_NOMEM: return "workspace allocation failed";
     case PK_ERR_INTERNAL: return "schedule capacity exceeded (library bug)";
     case PK_ERR_TOO_LARGE: return "T exceeds PK_NOALLOC_MAX_T, the static scratch capacity of pk_attend_noalloc";
+    case PK_ERR_CAPTURE: return "stream capture would have to allocate the workspace: make one uncaptured call first";
     default: return "unknown status";
   }
 }

@@ -86,6 +86,15 @@ def rope_tables(p: int, base: float) -> tuple[np.ndarray, np.ndarray]:
     return np.cos(ang), np.sin(ang)
 
 
+def rope_tables_dims(p: int, dims: int, base: float) -> tuple[np.ndarray, np.ndarray]:
+    """cos/sin [p, dims/2] in float64 for a rotation of the first `dims` features:
+    angle(pos, j) = pos * base^(-2j/dims) (the rope op's default frequencies)."""
+    pos = np.arange(p, dtype=np.float64)[:, None]
+    j = np.arange(dims // 2, dtype=np.float64)[None, :]
+    ang = pos / np.power(base, 2.0 * j / dims)
+    return np.cos(ang), np.sin(ang)
+
+
 # ----------------------------------------------------------------------------------------
 # workloads
 

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(10):
+    for code in range(11):
         assert pk.status_string(code) != "unknown status"
     assert pk.status_string(99) == "unknown status"
     assert lib.pk_version() >= 100
@@ -76,6 +76,35 @@ def test_argument_checks_need_no_gpu(lib):
     assert lib.pk_schedule_capacity(0) == 1
     assert lib.pk_schedule_capacity(64) == 4
     assert lib.pk_schedule_capacity(65) == 7
+
+
+def test_rope_argument_checks_need_no_gpu(lib):
+    # pk_rope rejects bad arguments before any CUDA call
+    p = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1002)
+    null = ctypes.c_void_p(0)
+    args = dict(dtype=1, x=p, y=p, cos=p, sin=p, P=16, cu=p, S=1, T=5, H=2, dims=64, trad=0, inv=0,
+                status=null, stream=null)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return pk.pk_rope(a["dtype"], a["x"], a["y"], a["cos"], a["sin"], a["P"], a["cu"], a["S"], a["T"],
+                          a["H"], a["dims"], a["trad"], a["inv"], a["status"], a["stream"])
+
+    assert call(dtype=7) == 1
+    assert call(dims=0) == 1
+    assert call(dims=7) == 1         # odd
+    assert call(dims=66) == 1        # more than the head
+    assert call(H=0) == 1
+    assert call(S=-1) == 1
+    assert call(S=0) == 1            # T > 0 with no sequences
+    assert call(P=0) == 1
+    assert call(x=null) == 1
+    assert call(cos=null) == 1
+    assert call(x=odd) == 2          # a 16-bit word is 4 bytes
+    assert call(dtype=0, y=ctypes.c_void_p(0x1004)) == 2  # fp32 words are 8 bytes
+    assert call(T=0, S=0, x=null, y=null, cos=null, sin=null, cu=null) == 0  # nothing to do
 
 
 def test_schedule_capacity_matches_oracle(lib, orc):
