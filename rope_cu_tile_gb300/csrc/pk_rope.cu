@@ -13,7 +13,7 @@
 // is found once by a 32-way search and then followed). Lane l holds features 2l and 2l + 1 of
 // a head vector (one 4-byte word in 16 bits, 8 bytes in fp32), so a head vector is one
 // coalesced 128- or 256-byte access; the partner of a feature sits in another lane (halves) or
-// the same lane (interleaved pairs) and comes by shuffle. Head vectors are processed four at a
+// the same lane (interleaved pairs) and comes by shuffle. Head vectors are processed twelve at a
 // time so that several loads are in flight per warp. Arithmetic in fp32, one rounding to the
 // element type.
 #include <cuda_bf16.h>
@@ -27,7 +27,7 @@ namespace pk {
 namespace {
 
 constexpr int kRopeThreads = 256;
-constexpr int kRopeBatch = 4;  // head vectors in flight per warp
+constexpr int kRopeBatch = 12;  // head vectors in flight per warp (measured best of 4 to 24)
 
 // two elements of one lane as floats, and back
 template <int DT>
@@ -207,7 +207,15 @@ __global__ void __launch_bounds__(kRopeThreads) pk_rope_kernel(const RopeArgs a)
       }
     }
     if (a.copy_v)
-      for (int v = nqk; v < 3 * a.H; ++v) yr[v * 32 + lane] = xr[v * 32 + lane];
+      for (int v0 = nqk; v0 < 3 * a.H; v0 += kRopeBatch) {
+        Word w[kRopeBatch];
+#pragma unroll
+        for (int b = 0; b < kRopeBatch; ++b)
+          if (v0 + b < 3 * a.H) w[b] = xr[(v0 + b) * 32 + lane];
+#pragma unroll
+        for (int b = 0; b < kRopeBatch; ++b)
+          if (v0 + b < 3 * a.H) yr[(v0 + b) * 32 + lane] = w[b];
+      }
   }
 }
 
