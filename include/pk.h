@@ -173,6 +173,18 @@ int pk_attend_noalloc(int dtype, const void *qkv, const void *cos, const void *s
                       void *out, float *lse, int *status, struct CUstream_st *stream);
 
 /*
+ * pk_attend_mixed -- fp32 inputs, fp32 arithmetic, a 16-bit output: kime's attention variant
+ * with an FP32 qkv and a half output (the qkv stays FP32 because FP16 rounding of q and k
+ * moves the softmax; the pages' plan.rs, fn types). Same operation as pk_attend_f32 (the
+ * CUDA-core path), with out = O / l rounded once to out_dtype.
+ *   - out_dtype: PK_F16 or PK_BF16 (PK_F32 gives pk_attend_f32); out [T, H*64] of that type.
+ *   - qkv, cos, sin: fp32, as pk_attend_f32; the other arguments, alignment and errors as pk_attend.
+ */
+int pk_attend_mixed(int out_dtype, const float *qkv, const float *cos, const float *sin,
+                    const uint32_t *cu, int S, int64_t T, int H, int window, float scale,
+                    void *out, float *lse, struct CUstream_st *stream);
+
+/*
  * pk_rope -- the standalone rotary embedding of a packed qkv: the pages' rope op
  * (hanzo-kernel fast ops, FastOp::Rope and its graph fallback), applied as kime's rope step
  * applies it, to every q and k head vector of qkv.

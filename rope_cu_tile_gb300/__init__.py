@@ -30,7 +30,7 @@ NOALLOC_MAX_T = 1048576
 # names declared in include/pk.h
 EXPORTS = ("pk_attend", "pk_attend_bf16", "pk_attend_f16", "pk_attend_f32", "pk_attend_dt",
            "pk_schedule", "pk_schedule_capacity", "pk_last_status", "pk_status_string",
-           "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop", "pk_attend_noalloc", "pk_rope")
+           "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop", "pk_attend_noalloc", "pk_rope", "pk_attend_mixed")
 
 _lib = None
 
@@ -60,6 +60,8 @@ def load(path: str | None = None):
     L.pk_attend_dt.restype = i32
     L.pk_attend_noalloc.argtypes = [i32] + sig[:11] + [vp, vp]
     L.pk_attend_noalloc.restype = i32
+    L.pk_attend_mixed.argtypes = [i32] + sig
+    L.pk_attend_mixed.restype = i32
     L.pk_rope.argtypes = [i32, vp, vp, vp, vp, i64, vp, i32, i64, i32, i32, i32, i32, vp, vp]
     L.pk_rope.restype = i32
     L.pk_schedule.argtypes = [vp, i32, i64, i32, vp, i64, ctypes.POINTER(i64), vp]
@@ -110,6 +112,11 @@ def pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse
     return load().pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, status, stream)
 
 
+def pk_attend_mixed(out_dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream) -> int:
+    """fp32 inputs and arithmetic, out in out_dtype (see include/pk.h)."""
+    return load().pk_attend_mixed(out_dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream)
+
+
 def pk_rope(dtype, x, y, cos, sin, P, cu, S, T, H, dims, traditional, inverse, status, stream) -> int:
     """The standalone rotation of the q and k head vectors of a packed qkv (see include/pk.h)."""
     return load().pk_rope(dtype, x, y, cos, sin, P, cu, S, T, H, dims, traditional, inverse, status, stream)
@@ -150,9 +157,11 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=None, stream=None):
+def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=None, stream=None,
+           out_dtype=None):
     """out [T, H*64] (qkv's dtype) and lse [H, T] float32 for device tensors qkv [T, 3*H*64],
-    cos/sin [P, 32] (qkv's dtype) and cu [S+1] (int32 or uint32)."""
+    cos/sin [P, 32] (qkv's dtype) and cu [S+1] (int32 or uint32). For float32 inputs,
+    out_dtype=torch.float16 or torch.bfloat16 gives a 16-bit out (pk_attend_mixed)."""
     torch = _torch()
     T = qkv.shape[0]
     S = cu.shape[0] - 1
@@ -165,13 +174,20 @@ def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=N
     for t in (qkv, cos, sin, cu):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("inputs must be contiguous CUDA tensors")
+    odt = qkv.dtype if out_dtype is None else out_dtype
+    if odt != qkv.dtype and qkv.dtype != torch.float32:
+        raise TypeError("a different output type needs float32 inputs")
     if out is None:
-        out = torch.empty((T, H * 64), dtype=qkv.dtype, device=qkv.device)
+        out = torch.empty((T, H * 64), dtype=odt, device=qkv.device)
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=qkv.device)
-    rc = pk_attend_dt(dtype_code(qkv), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(),
-                      S, T, H, window, float(scale), out.data_ptr(), lse.data_ptr(),
-                      _stream_handle(stream))
+    if odt != qkv.dtype:
+        rc = pk_attend_mixed(dtype_code(out), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(),
+                             S, T, H, window, float(scale), out.data_ptr(), lse.data_ptr(), _stream_handle(stream))
+    else:
+        rc = pk_attend_dt(dtype_code(qkv), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(),
+                          S, T, H, window, float(scale), out.data_ptr(), lse.data_ptr(),
+                          _stream_handle(stream))
     _check(rc, "pk_attend")
     return out, lse
 

@@ -10,6 +10,14 @@
 // One 128-thread CTA per work item (tile record, head) at a time, persistent; thread r
 // owns query row r (q' in registers, 64 output accumulators). Keys go through shared
 // memory 32 at a time, rotated once by the CTA.
+//
+// The output may also be written in a 16-bit type (OUT: kime's attention variant with an
+// FP32 qkv and a half output, which keeps q and k in FP32 because rounding them moves the
+// softmax): everything stays fp32 up to one rounding of out = O / l.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "pk.h"
 #include "pk_dev.cuh"
 
 namespace pk {
@@ -19,10 +27,33 @@ constexpr int kThreadsF32 = 128;
 constexpr int kChunk = 32;   // keys per shared-memory chunk
 }  // namespace
 
+namespace {
+// four output values, rounded to the output type and stored together
+template <int OUT>
+__device__ __forceinline__ void store4(void* out, int64_t i, float a, float b, float c, float d) {
+  if constexpr (OUT == PK_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + i) = make_float4(a, b, c, d);
+  } else if constexpr (OUT == PK_BF16) {
+    const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+    const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(c))) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(d))) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + i) = make_uint2(lo, hi);
+  } else {
+    const uint32_t lo = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(a))) |
+                        (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(b))) << 16);
+    const uint32_t hi = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(c))) |
+                        (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(d))) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + i) = make_uint2(lo, hi);
+  }
+}
+}  // namespace
+
+template <int OUT>
 __global__ void __launch_bounds__(kThreadsF32)
 pk_attend_f32_kernel(const float* __restrict__ qkv, const float* __restrict__ cos_t,
                      const float* __restrict__ sin_t, const uint32_t* __restrict__ cu,
-                     const TileRec* __restrict__ tiles, float* __restrict__ out,
+                     const TileRec* __restrict__ tiles, void* __restrict__ out,
                      float* __restrict__ lse, Ctl* ctl, int H, long long T, int window,
                      float scale) {
   __shared__ float sk[kChunk][kD + 1];
@@ -138,20 +169,27 @@ pk_attend_f32_kernel(const float* __restrict__ qkv, const float* __restrict__ co
     }
     if (row_ok) {
       const float inv = 1.0f / l;
-      float* dst = out + static_cast<int64_t>(a) * hd + h * kD;
+      const int64_t at = static_cast<int64_t>(a) * hd + h * kD;
 #pragma unroll
-      for (int d = 0; d < kD; d += 4)
-        *reinterpret_cast<float4*>(dst + d) = make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+      for (int d = 0; d < kD; d += 4) store4<OUT>(out, at + d, o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
       lse[static_cast<int64_t>(h) * T + a] = m + logf(l);
     }
   }
 }
 
+// out_dtype: PK_F32, or PK_BF16 / PK_F16 for a 16-bit output
 cudaError_t attend_f32_launch(const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu,
-                              const TileRec* tiles, float* out, float* lse, Ctl* ctl, int H, long long T,
-                              int window, float scale, int grid, cudaStream_t stream) {
-  pk_attend_f32_kernel<<<grid, kThreadsF32, 0, stream>>>(qkv, cos_t, sin_t, cu, tiles, out, lse, ctl, H, T, window,
-                                                          scale);
+                              const TileRec* tiles, void* out, int out_dtype, float* lse, Ctl* ctl, int H,
+                              long long T, int window, float scale, int grid, cudaStream_t stream) {
+  if (out_dtype == PK_BF16)
+    pk_attend_f32_kernel<PK_BF16><<<grid, kThreadsF32, 0, stream>>>(qkv, cos_t, sin_t, cu, tiles, out, lse, ctl, H,
+                                                                     T, window, scale);
+  else if (out_dtype == PK_F16)
+    pk_attend_f32_kernel<PK_F16><<<grid, kThreadsF32, 0, stream>>>(qkv, cos_t, sin_t, cu, tiles, out, lse, ctl, H,
+                                                                    T, window, scale);
+  else
+    pk_attend_f32_kernel<PK_F32><<<grid, kThreadsF32, 0, stream>>>(qkv, cos_t, sin_t, cu, tiles, out, lse, ctl, H,
+                                                                    T, window, scale);
   return cudaGetLastError();
 }
 

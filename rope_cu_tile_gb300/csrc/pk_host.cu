@@ -24,8 +24,8 @@ cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos
                              long long T, int window, float scale, unsigned long long timeout_ns, int grid,
                              cudaStream_t stream);
 cudaError_t attend_f32_launch(const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu,
-                              const TileRec* tiles, float* out, float* lse, Ctl* ctl, int H, long long T,
-                              int window, float scale, int grid, cudaStream_t stream);
+                              const TileRec* tiles, void* out, int out_dtype, float* lse, Ctl* ctl, int H,
+                              long long T, int window, float scale, int grid, cudaStream_t stream);
 
 namespace {
 
@@ -179,12 +179,13 @@ int launch_schedule(const uint32_t* cu, int S, int64_t T, int window, Workspace*
              : PK_ERR_CUDA;
 }
 
-int launch_attend(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int64_t T,
-                  int H, int window, float scale, void* out, float* lse, Workspace* ws, DeviceInfo* di,
+int launch_attend(int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu,
+                  int64_t T, int H, int window, float scale, void* out, float* lse, Workspace* ws, DeviceInfo* di,
                   cudaStream_t stream);
 
-int attend(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T,
-           int H, int window, float scale, void* out, float* lse, cudaStream_t stream) {
+// out_dtype: the output's type (the input type, except for fp32 inputs with a 16-bit output)
+int attend(int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S,
+           int64_t T, int H, int window, float scale, void* out, float* lse, cudaStream_t stream) {
   int rc = check_args(dtype, qkv, cos, sin, cu, S, T, H, window, out, lse);
   if (rc != PK_OK || T == 0) return rc;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -199,17 +200,17 @@ int attend(int dtype, const void* qkv, const void* cos, const void* sin, const u
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return PK_ERR_CUDA;
   if ((rc = launch_schedule(cu, S, T, window, ws, stream)) != PK_OK) return rc;
   if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return PK_ERR_CUDA;
-  rc = launch_attend(dtype, qkv, cos, sin, cu, T, H, window, scale, out, lse, ws, di, stream);
+  rc = launch_attend(dtype, out_dtype, qkv, cos, sin, cu, T, H, window, scale, out, lse, ws, di, stream);
   if (rc == PK_OK && ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return PK_ERR_CUDA;
   return rc;
 }
 
-int launch_attend(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int64_t T,
-                  int H, int window, float scale, void* out, float* lse, Workspace* ws, DeviceInfo* di,
+int launch_attend(int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu,
+                  int64_t T, int H, int window, float scale, void* out, float* lse, Workspace* ws, DeviceInfo* di,
                   cudaStream_t stream) {
   if (dtype == PK_F32) {
     return attend_f32_launch(static_cast<const float*>(qkv), static_cast<const float*>(cos),
-                             static_cast<const float*>(sin), cu, ws->tiles, static_cast<float*>(out), lse, ws->ctl, H,
+                             static_cast<const float*>(sin), cu, ws->tiles, out, out_dtype, lse, ws->ctl, H,
                              static_cast<long long>(T), window, scale, di->sms * 4, stream) == cudaSuccess
                ? PK_OK
                : PK_ERR_CUDA;
@@ -243,27 +244,33 @@ extern "C" {
 
 int pk_attend_dt(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S,
                  int64_t T, int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
-  return attend(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+  return attend(dtype, dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+}
+
+int pk_attend_mixed(int out_dtype, const float* qkv, const float* cos, const float* sin, const uint32_t* cu, int S,
+                    int64_t T, int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
+  if (out_dtype != PK_F32 && out_dtype != PK_BF16 && out_dtype != PK_F16) return PK_ERR_ARG;
+  return attend(PK_F32, out_dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
 }
 
 int pk_attend(const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T, int H,
               int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
-  return attend(PK_BF16, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+  return attend(PK_BF16, PK_BF16, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
 }
 
 int pk_attend_bf16(const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T,
                    int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
-  return attend(PK_BF16, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+  return attend(PK_BF16, PK_BF16, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
 }
 
 int pk_attend_f16(const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T,
                   int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
-  return attend(PK_F16, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+  return attend(PK_F16, PK_F16, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
 }
 
 int pk_attend_f32(const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T,
                   int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
-  return attend(PK_F32, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+  return attend(PK_F32, PK_F32, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
 }
 
 int64_t pk_schedule_capacity(int64_t T) { return T < 0 ? 0 : schedule_capacity(T); }

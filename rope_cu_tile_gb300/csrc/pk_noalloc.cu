@@ -37,8 +37,8 @@ cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos
                              long long T, int window, float scale, unsigned long long timeout_ns, int grid,
                              cudaStream_t stream);
 cudaError_t attend_f32_launch(const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu,
-                              const TileRec* tiles, float* out, float* lse, Ctl* ctl, int H, long long T,
-                              int window, float scale, int grid, cudaStream_t stream);
+                              const TileRec* tiles, void* out, int out_dtype, float* lse, Ctl* ctl, int H,
+                              long long T, int window, float scale, int grid, cudaStream_t stream);
 
 namespace {
 
@@ -148,7 +148,7 @@ extern "C" int pk_attend_noalloc(int dtype, const void* qkv, const void* cos, co
   cudaError_t e;
   if (dtype == PK_F32) {
     e = attend_f32_launch(static_cast<const float*>(qkv), static_cast<const float*>(cos),
-                          static_cast<const float*>(sin), cu, tiles, static_cast<float*>(out), lse, ctl, H,
+                          static_cast<const float*>(sin), cu, tiles, out, PK_F32, lse, ctl, H,
                           static_cast<long long>(T), window, scale, s->sms * 4, st);
   } else {
     EncodeTiledFn enc = noalloc_encode_fn();
