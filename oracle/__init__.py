@@ -54,6 +54,8 @@ class Oracle:
         L.oracle_rope.restype = None
         L.oracle_rope_qkv.argtypes = [vp, i32, vp, vp, i32, i64, vp, i32, i64, i32, i32, i32, i32, vp]
         L.oracle_rope_qkv.restype = i32
+        L.oracle_attend_backward.argtypes = [vp, i32, vp, vp, i32, vp, i32, i64, i32, i32, dbl, vp, i32, vp]
+        L.oracle_attend_backward.restype = i32
         L.oracle_schedule.argtypes = [vp, i32, i64, i32, vp, i64, ctypes.POINTER(i64)]
         L.oracle_schedule.restype = i32
         L.oracle_schedule_cap.argtypes = [i64]
@@ -144,6 +146,23 @@ class Oracle:
                                       int(bool(inverse)), y.ctypes.data)
         if rc != 0:
             raise ValueError("oracle_rope_qkv: bad arguments")
+        return y
+
+    def attend_backward(self, qkv, cos, sin, cu, H: int, window: int, scale: float, dout, dtype: str = "f64",
+                        table_dtype: str | None = None, dout_dtype: str | None = None):
+        """dqkv [T, 3 H 64] in f64: the gradient of sum(dout * out) with respect to qkv."""
+        cu = np.ascontiguousarray(cu, dtype=np.uint32)
+        S = cu.shape[0] - 1
+        T = int(cu[-1])
+        q, dq_ = self._arr(qkv, dtype)
+        c, dc = self._arr(cos, table_dtype or dtype)
+        s, _ = self._arr(sin, table_dtype or dtype)
+        g, dg = self._arr(dout, dout_dtype or dtype)
+        y = np.zeros((T, 3 * H * 64), dtype=np.float64)
+        rc = self.lib.oracle_attend_backward(q.ctypes.data, dq_, c.ctypes.data, s.ctypes.data, dc, cu.ctypes.data,
+                                             S, T, H, window, float(scale), g.ctypes.data, dg, y.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"oracle_attend_backward -> {rc}")
         return y
 
     def schedule(self, cu, window: int):

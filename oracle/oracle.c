@@ -453,6 +453,117 @@ int oracle_rope_qkv(const void *qkv, int dt, const void *cosb, const void *sinb,
 }
 
 /* ---------------------------------------------------------------------------------------
+ * the backward pass (the pages' attend_back and its f64 reference): the gradient of
+ * L = sum(dout * out) with respect to qkv, through the rotation. Per sequence and head, with
+ * q'_i = rot(q_i, i), k'_j = rot(k_j, j), s_ij = scale q'_i . k'_j on visible pairs,
+ * P = softmax_j(s), O_i = sum_j P_ij v_j:
+ *   D_i = dout_i . O_i,   dP_ij = dout_i . v_j,   dS_ij = P_ij (dP_ij - D_i)
+ *   dv_j = sum_i P_ij dout_i,   dq'_i = scale sum_j dS_ij k'_j,   dk'_j = scale sum_i dS_ij q'_i
+ *   dq_i = rot^T(dq'_i, i),   dk_j = rot^T(dk'_j, j)   (the transposed rotation)
+ * Everything from the inputs in f64 (the forward is recomputed here, not read).
+ */
+int oracle_attend_backward(const void *qkv, int dt, const void *cosb, const void *sinb, int tdt,
+                           const uint32_t *cu, int S, int64_t T, int H, int window, double scale,
+                           const void *dout, int ddt, double *dqkv) {
+    if (H < 1 || window < 0 || check_cu(cu, S, T)) return -1;
+    const int64_t ldq = 3LL * H * HD, hd = (int64_t)H * HD;
+    int64_t maxlen = 1;
+    for (int sq = 0; sq < S; sq++)
+        if ((int64_t)cu[sq + 1] - cu[sq] > maxlen) maxlen = (int64_t)cu[sq + 1] - cu[sq];
+    double *qr = malloc(sizeof(double) * maxlen * HD), *kr = malloc(sizeof(double) * maxlen * HD);
+    double *dk = malloc(sizeof(double) * maxlen * HD), *dv = malloc(sizeof(double) * maxlen * HD);
+    double *pr = malloc(sizeof(double) * maxlen), *dsr = malloc(sizeof(double) * maxlen);
+    if (!qr || !kr || !dk || !dv || !pr || !dsr) {
+        free(qr); free(kr); free(dk); free(dv); free(pr); free(dsr);
+        return -2;
+    }
+    for (int64_t e = 0; e < T * ldq; e++) dqkv[e] = 0.0;
+    for (int sq = 0; sq < S; sq++) {
+        const int64_t start = cu[sq], L = (int64_t)cu[sq + 1] - cu[sq];
+        if (L <= 0) continue;
+        for (int h = 0; h < H; h++) {
+            for (int64_t j = 0; j < L; j++) {
+                rope_row(qkv, dt, (start + j) * ldq + h * HD, j, cosb, sinb, tdt, qr + j * HD);
+                rope_row(qkv, dt, (start + j) * ldq + hd + h * HD, j, cosb, sinb, tdt, kr + j * HD);
+            }
+            for (int64_t e = 0; e < L * HD; e++) dk[e] = dv[e] = 0.0;
+            for (int64_t i = 0; i < L; i++) {
+                /* this row's probabilities */
+                double m = -INFINITY;
+                for (int64_t j = 0; j < L; j++) {
+                    int64_t gap = i > j ? i - j : j - i;
+                    if (window == 0 || gap <= window) {
+                        double dot = 0.0;
+                        for (int d = 0; d < HD; d++) dot += qr[i * HD + d] * kr[j * HD + d];
+                        pr[j] = scale * dot;
+                    } else {
+                        pr[j] = -INFINITY;
+                    }
+                    if (pr[j] > m) m = pr[j];
+                }
+                double z = 0.0;
+                for (int64_t j = 0; j < L; j++) {
+                    pr[j] = exp(pr[j] - m);
+                    z += pr[j];
+                }
+                for (int64_t j = 0; j < L; j++) pr[j] /= z;
+                /* D_i = dout_i . O_i */
+                double di = 0.0;
+                for (int d = 0; d < HD; d++) {
+                    double o = 0.0;
+                    for (int64_t j = 0; j < L; j++)
+                        o += pr[j] * ld(qkv, dt, (start + j) * ldq + 2 * hd + h * HD + d);
+                    di += ld(dout, ddt, (start + i) * hd + h * HD + d) * o;
+                }
+                /* dS_ij, dv, dk' */
+                for (int64_t j = 0; j < L; j++) {
+                    double dp = 0.0;
+                    for (int d = 0; d < HD; d++)
+                        dp += ld(dout, ddt, (start + i) * hd + h * HD + d) *
+                              ld(qkv, dt, (start + j) * ldq + 2 * hd + h * HD + d);
+#if ORACLE_MUTANT == 15
+                    dsr[j] = pr[j] * dp;                                  /* planted: D dropped */
+#else
+                    dsr[j] = pr[j] * (dp - di);
+#endif
+                    for (int d = 0; d < HD; d++) {
+                        dv[j * HD + d] += pr[j] * ld(dout, ddt, (start + i) * hd + h * HD + d);
+                        dk[j * HD + d] += scale * dsr[j] * qr[i * HD + d];
+                    }
+                }
+                /* dq'_i, rotated back */
+                double dq[HD], y[HD];
+                for (int d = 0; d < HD; d++) {
+                    double acc = 0.0;
+                    for (int64_t j = 0; j < L; j++) acc += dsr[j] * kr[j * HD + d];
+#if ORACLE_MUTANT == 17
+                    dq[d] = acc;                                          /* planted: scale missing */
+#else
+                    dq[d] = scale * acc;
+#endif
+                }
+                rope_vector(dq, DT_F64, 0, i, cosb, sinb, tdt, HD, 0, 1, y);
+                for (int d = 0; d < HD; d++) dqkv[(start + i) * ldq + h * HD + d] = y[d];
+            }
+            for (int64_t j = 0; j < L; j++) {
+                double y[HD];
+#if ORACLE_MUTANT == 16
+                rope_vector(dk + j * HD, DT_F64, 0, j, cosb, sinb, tdt, HD, 0, 0, y);  /* planted: forwards */
+#else
+                rope_vector(dk + j * HD, DT_F64, 0, j, cosb, sinb, tdt, HD, 0, 1, y);
+#endif
+                for (int d = 0; d < HD; d++) {
+                    dqkv[(start + j) * ldq + hd + h * HD + d] = y[d];
+                    dqkv[(start + j) * ldq + 2 * hd + h * HD + d] = dv[j * HD + d];
+                }
+            }
+        }
+    }
+    free(qr); free(kr); free(dk); free(dv); free(pr); free(dsr);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------------
  * the tile schedule
  *
  * Records of 8 uint32: {q0, rows, k0, nk, seq, nseq, kind, ktiles}

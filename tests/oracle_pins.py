@@ -395,6 +395,51 @@ def pin_rope_op(orc) -> list[str]:
 
 
 # ----------------------------------------------------------------------------------------
+# backward
+
+
+def pin_backward(orc) -> list[str]:
+    """The gradient of sum(dout * out) against central differences of the forward oracle, and
+    the rows of dS summing to zero (so the rotated key gradients of a sequence sum to zero)."""
+    fails = []
+    rng = np.random.default_rng(21)
+    H = 2
+    for lens, window, scale in (([5, 0, 9], 0, 0.37), ([7, 3], 2, -0.6), ([1, 12], 4, 0.125)):
+        cu = synth.cu_from_lens(lens)
+        T = int(cu[-1])
+        c64, s64 = synth.rope_tables(16, 10000.0)
+        qkv = rng.standard_normal((T, 3 * H * 64))
+        dout = rng.standard_normal((T, H * 64))
+        g = orc.attend_backward(qkv, c64, s64, cu, H, window, scale, dout)
+
+        def loss(x):
+            o, _ = orc.attend(x, c64, s64, cu, H, window, scale, "f64")
+            return float(np.sum(o * dout))
+
+        h = 1e-5
+        idx = rng.choice(T * 3 * H * 64, size=120, replace=False)
+        for e in idx:
+            xp = qkv.copy().reshape(-1)
+            xm = qkv.copy().reshape(-1)
+            xp[e] += h
+            xm[e] -= h
+            fd = (loss(xp.reshape(qkv.shape)) - loss(xm.reshape(qkv.shape))) / (2 * h)
+            if abs(fd - g.reshape(-1)[e]) > 1e-6 * max(1.0, abs(fd)):
+                fails.append(f"backward: d/dqkv[{e}] {g.reshape(-1)[e]:.6g} against central difference {fd:.6g}")
+                break
+        # sum over a sequence's keys of the rotated key gradients: zero
+        seq, pos = token_seq_pos(cu)
+        for sq in range(len(lens)):
+            rows = np.where(seq == sq)[0]
+            for hh in range(H):
+                a = H * 64 + hh * 64
+                tot = sum(orc.rope(g[t, a:a + 64], int(pos[t]), c64, s64) for t in rows) if len(rows) else 0
+                if len(rows) and np.max(np.abs(tot)) > 1e-10 * max(1.0, np.max(np.abs(g))):
+                    fails.append("backward: rotated key gradients of a sequence do not sum to zero")
+    return list(dict.fromkeys(fails))
+
+
+# ----------------------------------------------------------------------------------------
 # schedule
 
 
@@ -514,7 +559,7 @@ def pin_schedule(orc) -> list[str]:
 
 
 ALL_PINS = (pin_sdpa, pin_rope, pin_closed_forms, pin_probabilities, pin_window_and_permutation,
-            pin_widen, pin_schedule, pin_rope_op)
+            pin_widen, pin_schedule, pin_rope_op, pin_backward)
 
 
 def all_failures(orc) -> list[str]:

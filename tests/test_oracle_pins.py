@@ -30,6 +30,9 @@ MUTANTS = {
     12: "rope op: inverse rotates forwards",
     13: "rope op: interleaved layout ignored",
     14: "rope op: features past dims not copied",
+    15: "backward: D term dropped from dS",
+    16: "backward: key gradient rotated forwards",
+    17: "backward: scale missing from the query gradient",
 }
 
 
