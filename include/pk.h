@@ -173,6 +173,26 @@ int pk_attend_noalloc(int dtype, const void *qkv, const void *cos, const void *s
                       void *out, float *lse, int *status, struct CUstream_st *stream);
 
 /*
+ * pk_attend_backward -- the backward pass (the pages' attend_back): the gradient of
+ * sum(dout * out) with respect to qkv, through the rotation, for a forward call with the
+ * same arguments. Per query row i and visible key j: P_ij = exp(scale q'_i . k'_j - lse_i),
+ * D_i = dout_i . out_i, dS_ij = P_ij (dout_i . v_j - D_i); dv_j = sum_i P_ij dout_i,
+ * dq_i = rot^T(scale sum_j dS_ij k'_j), dk_j = rot^T(scale sum_i dS_ij q'_i).
+ *   - dtype, qkv, cos, sin, cu, S, T, H, window, scale: as the forward call (pk_attend_dt).
+ *   - out [T, H*64] (dtype) and lse [H, T] (fp32): the forward's outputs.
+ *   - dout [T, H*64] (dtype): the gradient of the loss with respect to out.
+ *   - dqkv [T, 3*H*64] (dtype): written with the gradients of q | k | v.
+ *   - fp32 arithmetic on the CUDA cores, one rounding of dqkv to dtype. Allocates, on first use
+ *     per (device, stream), an fp32 scratch of H*T*(1 + 3*64) floats (kept with the workspace).
+ *   - Alignment and errors as pk_attend (dout, dqkv 16-byte aligned); device errors (bad cu)
+ *     in pk_last_status(stream).
+ */
+int pk_attend_backward(int dtype, const void *qkv, const void *cos, const void *sin,
+                       const uint32_t *cu, int S, int64_t T, int H, int window, float scale,
+                       const void *out, const float *lse, const void *dout, void *dqkv,
+                       struct CUstream_st *stream);
+
+/*
  * pk_attend_mixed -- fp32 inputs, fp32 arithmetic, a 16-bit output: kime's attention variant
  * with an FP32 qkv and a half output (the qkv stays FP32 because FP16 rounding of q and k
  * moves the softmax; the pages' plan.rs, fn types). Same operation as pk_attend_f32 (the

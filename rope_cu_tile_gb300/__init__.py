@@ -30,7 +30,8 @@ NOALLOC_MAX_T = 1048576
 # names declared in include/pk.h
 EXPORTS = ("pk_attend", "pk_attend_bf16", "pk_attend_f16", "pk_attend_f32", "pk_attend_dt",
            "pk_schedule", "pk_schedule_capacity", "pk_last_status", "pk_status_string",
-           "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop", "pk_attend_noalloc", "pk_rope", "pk_attend_mixed")
+           "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop", "pk_attend_noalloc", "pk_rope", "pk_attend_mixed",
+           "pk_attend_backward")
 
 _lib = None
 
@@ -60,6 +61,8 @@ def load(path: str | None = None):
     L.pk_attend_dt.restype = i32
     L.pk_attend_noalloc.argtypes = [i32] + sig[:11] + [vp, vp]
     L.pk_attend_noalloc.restype = i32
+    L.pk_attend_backward.argtypes = [i32, vp, vp, vp, vp, i32, i64, i32, i32, f32, vp, vp, vp, vp, vp]
+    L.pk_attend_backward.restype = i32
     L.pk_attend_mixed.argtypes = [i32] + sig
     L.pk_attend_mixed.restype = i32
     L.pk_rope.argtypes = [i32, vp, vp, vp, vp, i64, vp, i32, i64, i32, i32, i32, i32, vp, vp]
@@ -110,6 +113,11 @@ def pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse
     """The allocation-free variant (see include/pk.h): for callers that cannot let the library
     cudaMalloc a workspace; `status` is an optional device pointer to one int."""
     return load().pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, status, stream)
+
+
+def pk_attend_backward(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, dout, dqkv, stream) -> int:
+    """The backward pass (see include/pk.h)."""
+    return load().pk_attend_backward(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, dout, dqkv, stream)
 
 
 def pk_attend_mixed(out_dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream) -> int:
@@ -190,6 +198,26 @@ def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=N
                           _stream_handle(stream))
     _check(rc, "pk_attend")
     return out, lse
+
+
+def attend_backward(qkv, cos, sin, cu, H: int, window: int, scale: float, out, lse, dout, dqkv=None, stream=None):
+    """dqkv [T, 3*H*64] (qkv's dtype): the gradient of sum(dout * out) with respect to qkv, for
+    the forward's out and lse."""
+    torch = _torch()
+    T = qkv.shape[0]
+    S = cu.shape[0] - 1
+    for t in (qkv, cos, sin, cu, out, lse, dout):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if out.dtype != qkv.dtype or dout.dtype != qkv.dtype or lse.dtype != torch.float32:
+        raise TypeError("out and dout must have qkv's dtype, lse float32")
+    if dqkv is None:
+        dqkv = torch.empty_like(qkv)
+    rc = pk_attend_backward(dtype_code(qkv), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(), S, T, H,
+                            window, float(scale), out.data_ptr(), lse.data_ptr(), dout.data_ptr(), dqkv.data_ptr(),
+                            _stream_handle(stream))
+    _check(rc, "pk_attend_backward")
+    return dqkv
 
 
 def rope(qkv, cos, sin, cu, H: int, dims: int = 64, traditional: bool = False, inverse: bool = False,

@@ -19,6 +19,12 @@ cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, 
                             TileRec* stage, Ctl* ctl, cudaStream_t stream);
 cudaError_t attend_tc_prepare();
 cudaError_t schedule_prepare();
+cudaError_t backward_prepare();
+long long backward_scratch_floats(long long T, int H);
+cudaError_t backward_launch(int dtype, const void* qkv, const void* cos_t, const void* sin_t, const uint32_t* cu,
+                            int S, long long T, int H, int window, float scale, const void* out, const float* lse,
+                            const void* dout, void* dqkv, const TileRec* tiles, Ctl* ctl, float* scratch, int sms,
+                            cudaStream_t stream);
 cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
                              const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
                              long long T, int window, float scale, unsigned long long timeout_ns, int grid,
@@ -38,6 +44,8 @@ struct Workspace {
   TileRec* stage = nullptr;  // the scheduler's staging slots
   int64_t cap = 0;
   int64_t room = 0;  // tokens the workspace is sized for
+  float* bwd = nullptr;    // the backward pass's fp32 scratch (allocated on its first use)
+  int64_t bwd_floats = 0;
 };
 
 struct DeviceInfo {
@@ -102,7 +110,8 @@ int device_info(int dev, DeviceInfo** out) {
   }
   if (!di.supported) return PK_ERR_UNSUPPORTED;
   if (!di.attrs_set) {
-    if (attend_tc_prepare() != cudaSuccess || schedule_prepare() != cudaSuccess) return PK_ERR_CUDA;
+    if (attend_tc_prepare() != cudaSuccess || schedule_prepare() != cudaSuccess || backward_prepare() != cudaSuccess)
+      return PK_ERR_CUDA;
     di.attrs_set = true;
   }
   *out = &di;
@@ -130,6 +139,7 @@ int workspace(int dev, cudaStream_t stream, int64_t T, Workspace** out) {
     if (cudaMemcpy(&carried, &ws.ctl->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
       return PK_ERR_CUDA;
     cudaFree(ws.base);
+    if (ws.bwd) cudaFree(ws.bwd);
     ws = Workspace();
   }
   int64_t room = T < 65536 ? 65536 : T;
@@ -235,6 +245,54 @@ int launch_attend(int dtype, int out_dtype, const void* qkv, const void* cos, co
              : PK_ERR_CUDA;
 }
 
+// the backward scratch of a workspace, grown to `floats` (caller holds g_mu)
+int backward_scratch(Workspace* ws, cudaStream_t stream, int64_t floats) {
+  if (ws->bwd && ws->bwd_floats >= floats) return PK_OK;
+  cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap_status) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_CUDA;
+  }
+  if (cap_status != cudaStreamCaptureStatusNone) return PK_ERR_CAPTURE;
+  if (ws->bwd) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PK_ERR_CUDA;
+    cudaFree(ws->bwd);
+    ws->bwd = nullptr;
+    ws->bwd_floats = 0;
+  }
+  const int64_t want = floats + floats / 4;
+  void* p = nullptr;
+  if (cudaMalloc(&p, static_cast<size_t>(want) * sizeof(float)) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_NOMEM;
+  }
+  ws->bwd = static_cast<float*>(p);
+  ws->bwd_floats = want;
+  return PK_OK;
+}
+
+int attend_backward(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S,
+                    int64_t T, int H, int window, float scale, const void* out, const float* lse, const void* dout,
+                    void* dqkv, cudaStream_t stream) {
+  int rc = check_args(dtype, qkv, cos, sin, cu, S, T, H, window, out, lse);
+  if (rc != PK_OK || T == 0) return rc;
+  if (!dout || !dqkv) return PK_ERR_ARG;
+  if (!aligned(dout, 16) || !aligned(dqkv, 16)) return PK_ERR_ALIGN;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PK_ERR_CUDA;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(dev, &di)) != PK_OK) return rc;
+  Workspace* ws = nullptr;
+  if ((rc = workspace(dev, stream, T, &ws)) != PK_OK) return rc;
+  if ((rc = backward_scratch(ws, stream, backward_scratch_floats(T, H))) != PK_OK) return rc;
+  if ((rc = launch_schedule(cu, S, T, window, ws, stream)) != PK_OK) return rc;
+  return backward_launch(dtype, qkv, cos, sin, cu, S, static_cast<long long>(T), H, window, scale, out, lse, dout,
+                         dqkv, ws->tiles, ws->ctl, ws->bwd, di->sms, stream) == cudaSuccess
+             ? PK_OK
+             : PK_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace pk
 
@@ -251,6 +309,12 @@ int pk_attend_mixed(int out_dtype, const float* qkv, const float* cos, const flo
                     int64_t T, int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
   if (out_dtype != PK_F32 && out_dtype != PK_BF16 && out_dtype != PK_F16) return PK_ERR_ARG;
   return attend(PK_F32, out_dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+}
+
+int pk_attend_backward(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S,
+                       int64_t T, int H, int window, float scale, const void* out, const float* lse, const void* dout,
+                       void* dqkv, struct CUstream_st* stream) {
+  return attend_backward(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, dout, dqkv, stream);
 }
 
 int pk_attend(const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T, int H,
@@ -404,6 +468,7 @@ int pk_release(void) {
     cudaSetDevice(kv.first.first);
     if (cudaStreamSynchronize(kv.first.second) != cudaSuccess) rc = PK_ERR_CUDA;
     cudaFree(kv.second.base);
+    if (kv.second.bwd) cudaFree(kv.second.bwd);
   }
   g_ws.clear();
   cudaSetDevice(cur);
