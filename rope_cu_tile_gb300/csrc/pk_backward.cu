@@ -9,12 +9,14 @@
 //
 // Three kernels over the forward's tile records (the same device schedule):
 //   prep    D [H, T] = rowsum(dout * out), fp32
-//   main    per work item (tile record, head), persistent CTAs of 128 threads, thread r <->
-//           query row r (q', dout in registers and in shared memory). Keys go through shared
-//           memory 16 at a time (rotated once); each thread forms its row's P and dS for them
-//           and accumulates dq' in registers; the CTA then reduces dv and dk' of the 16 keys
-//           over its rows and adds them to fp32 accumulators in global memory (other records of
-//           the same sequence add to the same keys). dq' of each row is written once.
+//   main    per work item (tile record, head), persistent CTAs of 128 threads (two per SM),
+//           thread r <-> query row r (dout in registers, q' and dout in shared memory). Keys go
+//           through shared memory 16 at a time (rotated once); each thread forms its row's P and
+//           dS for them (key and value rows read as 16-byte broadcasts) and accumulates dq' in
+//           registers; the CTA then reduces dv and dk' of the 16 keys over its rows and adds
+//           them to fp32 accumulators in global memory (other records of the same sequence add
+//           to the same keys). dq' of each row is written once. Shared-memory bandwidth bounds
+//           this version (the column sums read two 64-float rows per row and key).
 //   finish  dq = rot^T(dq'), dk = rot^T(dk'), dv, rounded once to the element type.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -28,8 +30,9 @@ namespace {
 
 constexpr int kBwdThreads = 128;
 constexpr int kBwdChunk = 16;  // keys per shared-memory chunk
+constexpr int kRowF = kD + 4;  // shared-memory row stride in floats (rows start on 16 bytes)
 constexpr int kBwdSmem =
-    static_cast<int>(sizeof(float)) * ((2 * kBwdChunk + 2 * kBwdThreads) * (kD + 1) + 2 * kBwdThreads * (kBwdChunk + 1));
+    static_cast<int>(sizeof(float)) * ((2 * kBwdChunk + 2 * kBwdThreads) * kRowF + 2 * kBwdThreads * (kBwdChunk + 1));
 
 template <int DT>
 __device__ __forceinline__ float ldf(const void* p, int64_t i) {
@@ -75,18 +78,18 @@ __global__ void __launch_bounds__(256) pk_bwd_prep_kernel(const void* __restrict
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(kBwdThreads, 2)
 pk_bwd_main_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, const void* __restrict__ sin_t,
                    const uint32_t* __restrict__ cu, const TileRec* __restrict__ tiles, Ctl* ctl,
                    const float* __restrict__ lse, const void* __restrict__ dout, const float* __restrict__ D,
                    float* __restrict__ dq_acc, float* __restrict__ dk_acc, float* __restrict__ dv_acc, int H,
                    long long T, int window, float scale) {
   // dynamic shared memory (kBwdSmem bytes): keys, values, the rows' q' and dout, P and dS
-  extern __shared__ float bwd_smem[];
-  float(*sk)[kD + 1] = reinterpret_cast<float(*)[kD + 1]>(bwd_smem);
-  float(*sv)[kD + 1] = sk + kBwdChunk;
-  float(*sq)[kD + 1] = sv + kBwdChunk;
-  float(*sdo)[kD + 1] = sq + kBwdThreads;
+  extern __shared__ __align__(16) float bwd_smem[];
+  float(*sk)[kRowF] = reinterpret_cast<float(*)[kRowF]>(bwd_smem);
+  float(*sv)[kRowF] = sk + kBwdChunk;
+  float(*sq)[kRowF] = sv + kBwdChunk;
+  float(*sdo)[kRowF] = sq + kBwdThreads;
   float(*sp)[kBwdChunk + 1] = reinterpret_cast<float(*)[kBwdChunk + 1]>(sdo + kBwdThreads);
   float(*sds)[kBwdChunk + 1] = sp + kBwdThreads;
   __shared__ unsigned int s_item;
@@ -135,9 +138,15 @@ pk_bwd_main_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t,
     } else {
       for (int d = 0; d < kD; ++d) sq[r][d] = sdo[r][d] = 0.f;
     }
-    float dq[kD];
+    // this row's dout in registers as well (the shared copies serve the column sums); its q'
+    // is read from shared memory 16 bytes at a time
+    float dor[kD], dq[kD];
 #pragma unroll
-    for (int d = 0; d < kD; ++d) dq[d] = 0.f;
+    for (int d = 0; d < kD; ++d) {
+      dor[d] = sdo[r][d];
+      dq[d] = 0.f;
+    }
+    const float4* qrow = reinterpret_cast<const float4*>(sq[r]);
 
     const uint32_t kend = rec.k0 + rec.nk;
     for (uint32_t j0 = rec.k0; j0 < kend; j0 += kBwdChunk) {
@@ -170,16 +179,32 @@ pk_bwd_main_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t,
         const int64_t b = static_cast<int64_t>(j0) + c;
         float p = 0.f, ds = 0.f;
         if (row_ok && c < nc && b >= lo && b < hi) {
+          // key and value rows: the same address for every thread (broadcast), 16 bytes a load
+          const float4* kc = reinterpret_cast<const float4*>(sk[c]);
+          const float4* vc = reinterpret_cast<const float4*>(sv[c]);
           float sdot = 0.f, pdot = 0.f;
 #pragma unroll
-          for (int d = 0; d < kD; ++d) {
-            sdot = fmaf(sq[r][d], sk[c][d], sdot);
-            pdot = fmaf(sdo[r][d], sv[c][d], pdot);
+          for (int q4 = 0; q4 < kD / 4; ++q4) {
+            const float4 k4 = kc[q4], v4 = vc[q4], x4 = qrow[q4];
+            sdot = fmaf(x4.x, k4.x, sdot);
+            sdot = fmaf(x4.y, k4.y, sdot);
+            sdot = fmaf(x4.z, k4.z, sdot);
+            sdot = fmaf(x4.w, k4.w, sdot);
+            pdot = fmaf(dor[4 * q4], v4.x, pdot);
+            pdot = fmaf(dor[4 * q4 + 1], v4.y, pdot);
+            pdot = fmaf(dor[4 * q4 + 2], v4.z, pdot);
+            pdot = fmaf(dor[4 * q4 + 3], v4.w, pdot);
           }
           p = __expf(scale * sdot - lse_r);
           ds = p * (pdot - d_r);
 #pragma unroll
-          for (int d = 0; d < kD; ++d) dq[d] = fmaf(ds, sk[c][d], dq[d]);
+          for (int q4 = 0; q4 < kD / 4; ++q4) {
+            const float4 k4 = kc[q4];
+            dq[4 * q4] = fmaf(ds, k4.x, dq[4 * q4]);
+            dq[4 * q4 + 1] = fmaf(ds, k4.y, dq[4 * q4 + 1]);
+            dq[4 * q4 + 2] = fmaf(ds, k4.z, dq[4 * q4 + 2]);
+            dq[4 * q4 + 3] = fmaf(ds, k4.w, dq[4 * q4 + 3]);
+          }
         }
         sp[r][c] = p;
         sds[r][c] = ds;
@@ -195,11 +220,18 @@ pk_bwd_main_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t,
           const int nr = static_cast<int>(rec.rows);
           for (int rr = 0; rr < nr; ++rr) {
             const float p = sp[rr][c], ds = sds[rr][c];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              dv[e] = fmaf(p, sdo[rr][d0 + e], dv[e]);
-              dk[e] = fmaf(ds, sq[rr][d0 + e], dk[e]);
-            }
+            const float4 o0 = *reinterpret_cast<const float4*>(&sdo[rr][d0]);
+            const float4 o1 = *reinterpret_cast<const float4*>(&sdo[rr][d0 + 4]);
+            const float4 q0 = *reinterpret_cast<const float4*>(&sq[rr][d0]);
+            const float4 q1 = *reinterpret_cast<const float4*>(&sq[rr][d0 + 4]);
+            dv[0] = fmaf(p, o0.x, dv[0]); dv[1] = fmaf(p, o0.y, dv[1]);
+            dv[2] = fmaf(p, o0.z, dv[2]); dv[3] = fmaf(p, o0.w, dv[3]);
+            dv[4] = fmaf(p, o1.x, dv[4]); dv[5] = fmaf(p, o1.y, dv[5]);
+            dv[6] = fmaf(p, o1.z, dv[6]); dv[7] = fmaf(p, o1.w, dv[7]);
+            dk[0] = fmaf(ds, q0.x, dk[0]); dk[1] = fmaf(ds, q0.y, dk[1]);
+            dk[2] = fmaf(ds, q0.z, dk[2]); dk[3] = fmaf(ds, q0.w, dk[3]);
+            dk[4] = fmaf(ds, q1.x, dk[4]); dk[5] = fmaf(ds, q1.y, dk[5]);
+            dk[6] = fmaf(ds, q1.z, dk[6]); dk[7] = fmaf(ds, q1.w, dk[7]);
           }
           const int64_t at = (static_cast<int64_t>(j0) + c) * hd + h * kD + d0;
 #pragma unroll
