@@ -20,7 +20,13 @@ What pins what:
   - permute:   permuting the sequences permutes the rows, bit for bit.
   - widen:     bf16 and fp16 inputs widen exactly (same result as float64 inputs).
   - schedule:  the tile records partition the rows, keep every visible key of each row in
-               the key range, keep that range tight, and follow the grouping rule.
+               the key range, keep that range tight, and follow the grouping rule (greedy
+               packing of short sequences within 1024-token windows).
+  - rope_op:   the standalone rotation reduces to the attention path's for full halves, its
+               inverse undoes it, interleaved pairs are the permuted halves, untouched
+               features stay, pair lengths stay, and a unit vector turns the right way.
+  - backward:  the gradient equals central differences of the forward oracle, and the
+               rotated key gradients of a sequence sum to zero.
 """
 
 from __future__ import annotations
