@@ -182,7 +182,9 @@ int pk_attend_noalloc(int dtype, const void *qkv, const void *cos, const void *s
  *   - out [T, H*64] (dtype) and lse [H, T] (fp32): the forward's outputs.
  *   - dout [T, H*64] (dtype): the gradient of the loss with respect to out.
  *   - dqkv [T, 3*H*64] (dtype): written with the gradients of q | k | v.
- *   - fp32 arithmetic on the CUDA cores, one rounding of dqkv to dtype. Allocates, on first use
+ *   - bf16 / fp16: tensor-core products with q', k', P and dS rounded to dtype as operands and
+ *     fp32 accumulation; fp32: fp32 arithmetic on the CUDA cores. One rounding of dqkv to
+ *     dtype. Allocates, on first use
  *     per (device, stream), an fp32 scratch of H*T*(1 + 3*64) floats (kept with the workspace).
  *   - Alignment and errors as pk_attend (dout, dqkv 16-byte aligned); device errors (bad cu)
  *     in pk_last_status(stream).

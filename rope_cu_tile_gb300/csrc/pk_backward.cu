@@ -1,5 +1,6 @@
 // pk_backward.cu -- the backward pass of packed RoPE attention (pk_attend_backward in
-// include/pk.h), on the CUDA cores in fp32.
+// include/pk.h): 16-bit inputs on the tensor cores (mma.sync, fp32 accumulation), fp32 inputs on
+// the CUDA cores.
 //
 // The pages' attend_back (hanzo-kernel packed.rs) computes, per query row i and visible key j of
 // its sequence, with q'_i = rot(q_i, i), k'_j = rot(k_j, j), s_ij = scale q'_i . k'_j and the
@@ -9,7 +10,8 @@
 //
 // Three kernels over the forward's tile records (the same device schedule):
 //   prep    D [H, T] = rowsum(dout * out), fp32
-//   main    per work item (tile record, head), persistent CTAs of 128 threads (two per SM),
+//   main    for 16-bit inputs pk_bwd_mma_kernel (below); for fp32 inputs pk_bwd_main_kernel:
+//           per work item (tile record, head), persistent CTAs of 128 threads (two per SM),
 //           thread r <-> query row r (dout in registers, q' and dout in shared memory). Keys go
 //           through shared memory 16 at a time (rotated once); each thread forms its row's P and
 //           dS for them (key and value rows read as 16-byte broadcasts) and accumulates dq' in
@@ -253,6 +255,311 @@ pk_bwd_main_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t,
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// The 16-bit backward on tensor cores (mma.sync m16n8k16, fp32 accumulation), FA2-style with
+// the key tile owning the work: visibility is symmetric (same sequence, |i - j| <= w), so a
+// tile record's rows serve as a key tile and its key range as the queries that see those keys.
+// Per work item (record, head): 8 warps x 16 keys; the key tile's K' (rotated, rounded to the
+// element type), K'^T and V stay in shared memory; queries come 32 at a time (Q', Q'^T, dout,
+// dout^T, lse, D). Per chunk each warp forms S^T = K' Q'^T and dP^T = V dout^T (16 MMAs each),
+// P^T and dS^T in registers, and accumulates dV += P^T dout and dK' += dS^T Q' in registers;
+// dS goes to shared memory and the CTA forms the chunk's dQ' = dS K' (warp w: dims 8w .. 8w+7),
+// added to the fp32 accumulator with atomics (other records' keys add to the same queries).
+// dK' and dV of each key are written once at the end of the item.
+
+constexpr int kMmaWarps = 8;
+constexpr int kMmaThreads = 32 * kMmaWarps;
+constexpr int kQc = 32;          // queries per chunk
+constexpr int kKP = kD + 8;      // row stride (16-bit elements) of [row][dim] tiles
+constexpr int kKTP = kBR + 8;    // row stride of K'^T [dim][key] and dS [query][key]
+constexpr int kQTP = kQc + 8;    // row stride of Q'^T and dout^T [dim][query]
+constexpr int kMmaSmemHalves = 2 * kBR * kKP + kD * kKTP + 2 * kQc * kKP + 2 * kD * kQTP + kQc * kKTP;
+constexpr int kMmaSmem = kMmaSmemHalves * 2 + 2 * kQc * 4;
+
+template <int DT>
+__device__ __forceinline__ uint16_t to16(float x) {
+  if constexpr (DT == PK_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  else return __half_as_ushort(__float2half_rn(x));
+}
+template <int DT>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  return static_cast<uint32_t>(to16<DT>(lo)) | (static_cast<uint32_t>(to16<DT>(hi)) << 16);
+}
+__device__ __forceinline__ uint32_t lds32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// D += A B, m16n8k16, A row-major 16x16, B column-major 16x8, fp32 accumulators
+template <int DT>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (DT == PK_BF16) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kMmaThreads, 2)
+pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, const void* __restrict__ sin_t,
+                  const uint32_t* __restrict__ cu, const TileRec* __restrict__ tiles, Ctl* ctl,
+                  const float* __restrict__ lse, const void* __restrict__ dout, const float* __restrict__ D,
+                  float* __restrict__ dq_acc, float* __restrict__ dk_acc, float* __restrict__ dv_acc, int H,
+                  long long T, int window, float scale) {
+  extern __shared__ __align__(16) uint16_t mma_smem[];
+  uint16_t* sK = mma_smem;                // [128][kKP]   K' (rotated)
+  uint16_t* sV = sK + kBR * kKP;          // [128][kKP]   V
+  uint16_t* sKT = sV + kBR * kKP;         // [64][kKTP]   K'^T
+  uint16_t* sQ = sKT + kD * kKTP;         // [32][kKP]    Q' of the chunk
+  uint16_t* sDO = sQ + kQc * kKP;         // [32][kKP]    dout of the chunk
+  uint16_t* sQT = sDO + kQc * kKP;        // [64][kQTP]   Q'^T
+  uint16_t* sDOT = sQT + kD * kQTP;       // [64][kQTP]   dout^T
+  uint16_t* sDS = sDOT + kD * kQTP;       // [32][kKTP]   dS [query][key]
+  float* sLse = reinterpret_cast<float*>(sDS + kQc * kKTP);  // [32]
+  float* sD = sLse + kQc;                                       // [32]
+  __shared__ unsigned int s_item;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t4 = lane & 3;
+  const unsigned int n_items = __ldcg(&ctl->ntiles) * static_cast<unsigned int>(H);
+  const int64_t ldq = 3ll * H * kD;
+  const int64_t hd = static_cast<int64_t>(H) * kD;
+
+  for (;;) {
+    if (tid == 0) s_item = atomicAdd(&ctl->next, 1u);
+    __syncthreads();
+    const unsigned int item = s_item;
+    __syncthreads();
+    if (item >= n_items) break;
+    const unsigned int ti = item / static_cast<unsigned int>(H);
+    const int h = static_cast<int>(item % static_cast<unsigned int>(H));
+    const TileRec rec = tiles[ti];
+    const int nkeys = static_cast<int>(rec.rows);  // the record's rows are the key tile
+
+    // stage the key tile: thread t rotates half the pairs of key row t / 2 and copies half its v
+    {
+      const int kr = tid >> 1, half = tid & 1;
+      if (kr < nkeys) {
+        const uint32_t b = rec.q0 + kr;
+        const uint32_t sb = rec.kind == 0 ? rec.seq : seq_of_token(cu, rec.seq, rec.nseq, b);
+        const int64_t pos = static_cast<int64_t>(b) - __ldg(cu + sb);
+        const int64_t x = static_cast<int64_t>(b) * ldq + hd + h * kD;
+        const int64_t v = static_cast<int64_t>(b) * ldq + 2 * hd + h * kD;
+        for (int e = 0; e < 16; ++e) {
+          const int u = half * 16 + e;
+          const float c = ldf<DT>(cos_t, pos * kHalf + u), sn = ldf<DT>(sin_t, pos * kHalf + u);
+          const float x1 = ldf<DT>(qkv, x + u), x2 = ldf<DT>(qkv, x + u + kHalf);
+          const uint16_t y1 = to16<DT>(x1 * c - x2 * sn), y2 = to16<DT>(x1 * sn + x2 * c);
+          sK[kr * kKP + u] = y1;
+          sK[kr * kKP + u + kHalf] = y2;
+          sKT[u * kKTP + kr] = y1;
+          sKT[(u + kHalf) * kKTP + kr] = y2;
+        }
+        for (int e = 0; e < 32; ++e)
+          sV[kr * kKP + half * 32 + e] = static_cast<const uint16_t*>(qkv)[v + half * 32 + e];
+      } else {
+        for (int e = 0; e < 16; ++e) {
+          const int u = half * 16 + e;
+          sK[kr * kKP + u] = sK[kr * kKP + u + kHalf] = 0;
+          sKT[u * kKTP + kr] = sKT[(u + kHalf) * kKTP + kr] = 0;
+        }
+        for (int e = 0; e < 32; ++e) sV[kr * kKP + half * 32 + e] = 0;
+      }
+    }
+    // this thread's two keys (rows g and g + 8 of the warp's 16): validity and visible queries
+    int64_t klo[2], khi[2];
+    bool kok[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int kr = warp * 16 + g + 8 * e;
+      kok[e] = kr < nkeys;
+      klo[e] = khi[e] = 0;
+      if (kok[e]) {
+        const uint32_t b = rec.q0 + kr;
+        const uint32_t sb = rec.kind == 0 ? rec.seq : seq_of_token(cu, rec.seq, rec.nseq, b);
+        const int64_t ss = __ldg(cu + sb), se = __ldg(cu + sb + 1);
+        klo[e] = ss;
+        khi[e] = se;
+        if (window > 0) {
+          klo[e] = max(ss, static_cast<int64_t>(b) - window);
+          khi[e] = min(se, static_cast<int64_t>(b) + window + 1);
+        }
+      }
+    }
+    float dv[8][4], dk[8][4];
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dv[n][e] = dk[n][e] = 0.f;
+
+    const uint32_t qend = rec.k0 + rec.nk;
+    for (uint32_t qb = rec.k0; qb < qend; qb += kQc) {
+      __syncthreads();  // the previous chunk is done with sQ, sDO, sQT, sDOT, sDS (and the key tile is staged)
+      // stage 32 queries: thread (row t / 8, 4 rotary pairs and 8 dout values)
+      {
+        const int qr = tid >> 3, part = tid & 7;
+        const uint32_t a = qb + qr;
+        if (a < qend) {
+          const uint32_t sa = rec.kind == 0 ? rec.seq : seq_of_token(cu, rec.seq, rec.nseq, a);
+          const int64_t pos = static_cast<int64_t>(a) - __ldg(cu + sa);
+          const int64_t x = static_cast<int64_t>(a) * ldq + h * kD;
+          for (int e = 0; e < 4; ++e) {
+            const int u = part * 4 + e;
+            const float c = ldf<DT>(cos_t, pos * kHalf + u), sn = ldf<DT>(sin_t, pos * kHalf + u);
+            const float x1 = ldf<DT>(qkv, x + u), x2 = ldf<DT>(qkv, x + u + kHalf);
+            const uint16_t y1 = to16<DT>(x1 * c - x2 * sn), y2 = to16<DT>(x1 * sn + x2 * c);
+            sQ[qr * kKP + u] = y1;
+            sQ[qr * kKP + u + kHalf] = y2;
+            sQT[u * kQTP + qr] = y1;
+            sQT[(u + kHalf) * kQTP + qr] = y2;
+          }
+          const int64_t go = static_cast<int64_t>(a) * hd + h * kD;
+          for (int e = 0; e < 8; ++e) {
+            const int d = part * 8 + e;
+            const uint16_t o = static_cast<const uint16_t*>(dout)[go + d];
+            sDO[qr * kKP + d] = o;
+            sDOT[d * kQTP + qr] = o;
+          }
+          if (part == 0) {
+            sLse[qr] = __ldg(lse + static_cast<int64_t>(h) * T + a);
+            sD[qr] = __ldg(D + static_cast<int64_t>(h) * T + a);
+          }
+        } else {
+          for (int e = 0; e < 4; ++e) {
+            const int u = part * 4 + e;
+            sQ[qr * kKP + u] = sQ[qr * kKP + u + kHalf] = 0;
+            sQT[u * kQTP + qr] = sQT[(u + kHalf) * kQTP + qr] = 0;
+          }
+          for (int e = 0; e < 8; ++e) {
+            const int d = part * 8 + e;
+            sDO[qr * kKP + d] = 0;
+            sDOT[d * kQTP + qr] = 0;
+          }
+          if (part == 0) sLse[qr] = sD[qr] = 0.f;
+        }
+      }
+      __syncthreads();
+
+      // S^T = K'_w Q'^T and dP^T = V_w dout^T: 16 keys x 32 queries (four n-blocks of 8)
+      float st[4][4], dpt[4][4];
+#pragma unroll
+      for (int nb = 0; nb < 4; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st[nb][e] = dpt[nb][e] = 0.f;
+      const int k0r = warp * 16;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t ak[4], av[4];
+        ak[0] = lds32(sK + (k0r + g) * kKP + 16 * kk + 2 * t4);
+        ak[1] = lds32(sK + (k0r + g + 8) * kKP + 16 * kk + 2 * t4);
+        ak[2] = lds32(sK + (k0r + g) * kKP + 16 * kk + 2 * t4 + 8);
+        ak[3] = lds32(sK + (k0r + g + 8) * kKP + 16 * kk + 2 * t4 + 8);
+        av[0] = lds32(sV + (k0r + g) * kKP + 16 * kk + 2 * t4);
+        av[1] = lds32(sV + (k0r + g + 8) * kKP + 16 * kk + 2 * t4);
+        av[2] = lds32(sV + (k0r + g) * kKP + 16 * kk + 2 * t4 + 8);
+        av[3] = lds32(sV + (k0r + g + 8) * kKP + 16 * kk + 2 * t4 + 8);
+#pragma unroll
+        for (int nb = 0; nb < 4; ++nb) {
+          const uint32_t bq0 = lds32(sQ + (8 * nb + g) * kKP + 16 * kk + 2 * t4);
+          const uint32_t bq1 = lds32(sQ + (8 * nb + g) * kKP + 16 * kk + 2 * t4 + 8);
+          mma16816<DT>(st[nb], ak, bq0, bq1);
+          const uint32_t bo0 = lds32(sDO + (8 * nb + g) * kKP + 16 * kk + 2 * t4);
+          const uint32_t bo1 = lds32(sDO + (8 * nb + g) * kKP + 16 * kk + 2 * t4 + 8);
+          mma16816<DT>(dpt[nb], av, bo0, bo1);
+        }
+      }
+      // P^T and dS^T (element e of tile nb: key row g + 8 (e >> 1), query 8 nb + 2 t4 + (e & 1));
+      // dS goes to shared memory as [query][key] for the dQ' product
+#pragma unroll
+      for (int nb = 0; nb < 4; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kr = e >> 1;
+          const int ql = 8 * nb + 2 * t4 + (e & 1);
+          const int64_t a = static_cast<int64_t>(qb) + ql;
+          float p = 0.f, ds = 0.f;
+          if (kok[kr] && a < qend && a >= klo[kr] && a < khi[kr]) {
+            p = __expf(scale * st[nb][e] - sLse[ql]);
+            ds = p * (dpt[nb][e] - sD[ql]);
+          }
+          st[nb][e] = p;
+          dpt[nb][e] = ds;
+          sDS[ql * kKTP + k0r + g + 8 * kr] = to16<DT>(ds);
+        }
+      // dV += P^T dout and dK' += dS^T Q': A from the accumulators (two n-blocks = one k-step)
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        uint32_t ap[4], ad[4];
+        ap[0] = pack16<DT>(st[2 * ks][0], st[2 * ks][1]);
+        ap[1] = pack16<DT>(st[2 * ks][2], st[2 * ks][3]);
+        ap[2] = pack16<DT>(st[2 * ks + 1][0], st[2 * ks + 1][1]);
+        ap[3] = pack16<DT>(st[2 * ks + 1][2], st[2 * ks + 1][3]);
+        ad[0] = pack16<DT>(dpt[2 * ks][0], dpt[2 * ks][1]);
+        ad[1] = pack16<DT>(dpt[2 * ks][2], dpt[2 * ks][3]);
+        ad[2] = pack16<DT>(dpt[2 * ks + 1][0], dpt[2 * ks + 1][1]);
+        ad[3] = pack16<DT>(dpt[2 * ks + 1][2], dpt[2 * ks + 1][3]);
+#pragma unroll
+        for (int nd = 0; nd < 8; ++nd) {
+          const uint32_t bo0 = lds32(sDOT + (8 * nd + g) * kQTP + 16 * ks + 2 * t4);
+          const uint32_t bo1 = lds32(sDOT + (8 * nd + g) * kQTP + 16 * ks + 2 * t4 + 8);
+          mma16816<DT>(dv[nd], ap, bo0, bo1);
+          const uint32_t bq0 = lds32(sQT + (8 * nd + g) * kQTP + 16 * ks + 2 * t4);
+          const uint32_t bq1 = lds32(sQT + (8 * nd + g) * kQTP + 16 * ks + 2 * t4 + 8);
+          mma16816<DT>(dk[nd], ad, bq0, bq1);
+        }
+      }
+      __syncthreads();  // every warp's dS is in shared memory
+      // dQ' of the chunk, dims 8 warp .. 8 warp + 7: dS [32 x 128] K' [128 x 8]
+      {
+        float acc[2][4];
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[mb][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < kBR / 16; ++kk) {
+          const uint32_t b0 = lds32(sKT + (8 * warp + g) * kKTP + 16 * kk + 2 * t4);
+          const uint32_t b1 = lds32(sKT + (8 * warp + g) * kKTP + 16 * kk + 2 * t4 + 8);
+#pragma unroll
+          for (int mb = 0; mb < 2; ++mb) {
+            uint32_t a4[4];
+            a4[0] = lds32(sDS + (16 * mb + g) * kKTP + 16 * kk + 2 * t4);
+            a4[1] = lds32(sDS + (16 * mb + g + 8) * kKTP + 16 * kk + 2 * t4);
+            a4[2] = lds32(sDS + (16 * mb + g) * kKTP + 16 * kk + 2 * t4 + 8);
+            a4[3] = lds32(sDS + (16 * mb + g + 8) * kKTP + 16 * kk + 2 * t4 + 8);
+            mma16816<DT>(acc[mb], a4, b0, b1);
+          }
+        }
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int ql = 16 * mb + g + 8 * (e >> 1);
+            const int64_t a = static_cast<int64_t>(qb) + ql;
+            if (a < qend)
+              atomicAdd(dq_acc + a * hd + h * kD + 8 * warp + 2 * t4 + (e & 1), scale * acc[mb][e]);
+          }
+      }
+    }
+    // dK' and dV of this warp's keys, written once (fp32)
+#pragma unroll
+    for (int kr = 0; kr < 2; ++kr) {
+      if (!kok[kr]) continue;
+      const int64_t b = static_cast<int64_t>(rec.q0) + warp * 16 + g + 8 * kr;
+#pragma unroll
+      for (int nd = 0; nd < 8; ++nd) {
+        const int64_t at = b * hd + h * kD + 8 * nd + 2 * t4;
+        *reinterpret_cast<float2*>(dk_acc + at) = make_float2(scale * dk[nd][2 * kr], scale * dk[nd][2 * kr + 1]);
+        *reinterpret_cast<float2*>(dv_acc + at) = make_float2(dv[nd][2 * kr], dv[nd][2 * kr + 1]);
+      }
+    }
+  }
+}
+
 // dqkv: dq = rot^T(dq'), dk = rot^T(dk'), dv; one warp per token, lane l holding the rotary pair
 // (l, l + 32) of a head vector (the halves' pairing), positions from cu
 template <int DT>
@@ -306,12 +613,20 @@ cudaError_t launch_backward_t(const void* qkv, const void* cos_t, const void* si
   float* dq = D + (static_cast<int64_t>(H) * T + 63) / 64 * 64;
   float* dk = dq + T * H * kD;
   float* dv = dk + T * H * kD;
-  cudaError_t e = cudaMemsetAsync(dk, 0, static_cast<size_t>(2) * T * H * kD * sizeof(float), stream);
+  // the 16-bit types take the tensor-core kernel (dq' by atomics, dk' and dv written once); fp32
+  // the CUDA-core one (dk' and dv by atomics, dq' written once)
+  constexpr bool kMma = DT != PK_F32;
+  cudaError_t e = kMma ? cudaMemsetAsync(dq, 0, static_cast<size_t>(T) * H * kD * sizeof(float), stream)
+                       : cudaMemsetAsync(dk, 0, static_cast<size_t>(2) * T * H * kD * sizeof(float), stream);
   if (e != cudaSuccess) return e;
   const long long prep_blocks = min(static_cast<long long>(sms) * 8, (T * H + 255) / 256);
   pk_bwd_prep_kernel<DT><<<static_cast<unsigned int>(max(prep_blocks, 1ll)), 256, 0, stream>>>(out, dout, D, H, T);
-  pk_bwd_main_kernel<DT><<<sms * 2, kBwdThreads, kBwdSmem, stream>>>(qkv, cos_t, sin_t, cu, tiles, ctl, lse, dout, D,
-                                                                      dq, dk, dv, H, T, window, scale);
+  if constexpr (kMma)
+    pk_bwd_mma_kernel<DT><<<sms * 2, kMmaThreads, kMmaSmem, stream>>>(qkv, cos_t, sin_t, cu, tiles, ctl, lse, dout, D,
+                                                                       dq, dk, dv, H, T, window, scale);
+  else
+    pk_bwd_main_kernel<DT><<<sms * 2, kBwdThreads, kBwdSmem, stream>>>(qkv, cos_t, sin_t, cu, tiles, ctl, lse, dout, D,
+                                                                        dq, dk, dv, H, T, window, scale);
   const long long fin_blocks = min(static_cast<long long>(sms) * 8, (T + 7) / 8);
   pk_bwd_finish_kernel<DT><<<static_cast<unsigned int>(max(fin_blocks, 1ll)), 256, 0, stream>>>(
       cos_t, sin_t, cu, S, T, H, dq, dk, dv, dqkv);
@@ -327,6 +642,10 @@ cudaError_t backward_prepare() {
     e = cudaFuncSetAttribute(pk_bwd_main_kernel<PK_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(pk_bwd_main_kernel<PK_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pk_bwd_mma_kernel<PK_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pk_bwd_mma_kernel<PK_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
   return e;
 }
 
