@@ -265,7 +265,11 @@ pk_bwd_main_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t,
 // P^T and dS^T in registers, and accumulates dV += P^T dout and dK' += dS^T Q' in registers;
 // dS goes to shared memory and the CTA forms the chunk's dQ' = dS K' (warp w: dims 8w .. 8w+7),
 // added to the fp32 accumulator with atomics (other records' keys add to the same queries).
-// dK' and dV of each key are written once at the end of the item.
+// dK' and dV of each key are written once at the end of the item. Fragments come by ldmatrix
+// from [row][element] tiles whose rows start on 16 bytes (strides of 72, 40 and 136 elements keep
+// the eight rows of each 8x8 load in distinct banks). Measured shares (global workload, parts
+// knocked out): the query chunks' staging about 10 %, the dQ' atomics about 5 %; the rest is the
+// products and the element-wise P and dS.
 
 constexpr int kMmaWarps = 8;
 constexpr int kMmaThreads = 32 * kMmaWarps;
@@ -285,7 +289,22 @@ template <int DT>
 __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   return static_cast<uint32_t>(to16<DT>(lo)) | (static_cast<uint32_t>(to16<DT>(hi)) << 16);
 }
-__device__ __forceinline__ uint32_t lds32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+// four (two) 8x8 16-bit matrices from shared memory; lane l gives the address of one matrix row
+__device__ __forceinline__ void ldsm4(const uint16_t* p, uint32_t (&r)[4]) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+// the A fragment (16 x 16, row-major tile with `stride` elements per row) at (row0, col0)
+__device__ __forceinline__ void lda(const uint16_t* tile, int stride, int row0, int col0, int lane, uint32_t (&r)[4]) {
+  ldsm4(tile + (row0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * stride + col0 + 8 * (lane >> 4), r);
+}
+// the B fragments (16 x 8, column-major: element (k, n) at tile[n][k]) of n-blocks n0 and n0 + 8
+// at k-step k0: r[0], r[1] for n0 and r[2], r[3] for n0 + 8
+__device__ __forceinline__ void ldb2(const uint16_t* tile, int stride, int n0, int k0, int lane, uint32_t (&r)[4]) {
+  ldsm4(tile + (n0 + (lane & 7) + 8 * (lane >> 4)) * stride + k0 + 8 * ((lane >> 3) & 1), r);
+}
 
 // D += A B, m16n8k16, A row-major 16x16, B column-major 16x8, fp32 accumulators
 template <int DT>
@@ -454,22 +473,17 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         uint32_t ak[4], av[4];
-        ak[0] = lds32(sK + (k0r + g) * kKP + 16 * kk + 2 * t4);
-        ak[1] = lds32(sK + (k0r + g + 8) * kKP + 16 * kk + 2 * t4);
-        ak[2] = lds32(sK + (k0r + g) * kKP + 16 * kk + 2 * t4 + 8);
-        ak[3] = lds32(sK + (k0r + g + 8) * kKP + 16 * kk + 2 * t4 + 8);
-        av[0] = lds32(sV + (k0r + g) * kKP + 16 * kk + 2 * t4);
-        av[1] = lds32(sV + (k0r + g + 8) * kKP + 16 * kk + 2 * t4);
-        av[2] = lds32(sV + (k0r + g) * kKP + 16 * kk + 2 * t4 + 8);
-        av[3] = lds32(sV + (k0r + g + 8) * kKP + 16 * kk + 2 * t4 + 8);
+        lda(sK, kKP, k0r, 16 * kk, lane, ak);
+        lda(sV, kKP, k0r, 16 * kk, lane, av);
 #pragma unroll
-        for (int nb = 0; nb < 4; ++nb) {
-          const uint32_t bq0 = lds32(sQ + (8 * nb + g) * kKP + 16 * kk + 2 * t4);
-          const uint32_t bq1 = lds32(sQ + (8 * nb + g) * kKP + 16 * kk + 2 * t4 + 8);
-          mma16816<DT>(st[nb], ak, bq0, bq1);
-          const uint32_t bo0 = lds32(sDO + (8 * nb + g) * kKP + 16 * kk + 2 * t4);
-          const uint32_t bo1 = lds32(sDO + (8 * nb + g) * kKP + 16 * kk + 2 * t4 + 8);
-          mma16816<DT>(dpt[nb], av, bo0, bo1);
+        for (int nb = 0; nb < 4; nb += 2) {
+          uint32_t bq[4], bo[4];
+          ldb2(sQ, kKP, 8 * nb, 16 * kk, lane, bq);
+          ldb2(sDO, kKP, 8 * nb, 16 * kk, lane, bo);
+          mma16816<DT>(st[nb], ak, bq[0], bq[1]);
+          mma16816<DT>(st[nb + 1], ak, bq[2], bq[3]);
+          mma16816<DT>(dpt[nb], av, bo[0], bo[1]);
+          mma16816<DT>(dpt[nb + 1], av, bo[2], bo[3]);
         }
       }
       // P^T and dS^T (element e of tile nb: key row g + 8 (e >> 1), query 8 nb + 2 t4 + (e & 1));
@@ -503,13 +517,14 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
         ad[2] = pack16<DT>(dpt[2 * ks + 1][0], dpt[2 * ks + 1][1]);
         ad[3] = pack16<DT>(dpt[2 * ks + 1][2], dpt[2 * ks + 1][3]);
 #pragma unroll
-        for (int nd = 0; nd < 8; ++nd) {
-          const uint32_t bo0 = lds32(sDOT + (8 * nd + g) * kQTP + 16 * ks + 2 * t4);
-          const uint32_t bo1 = lds32(sDOT + (8 * nd + g) * kQTP + 16 * ks + 2 * t4 + 8);
-          mma16816<DT>(dv[nd], ap, bo0, bo1);
-          const uint32_t bq0 = lds32(sQT + (8 * nd + g) * kQTP + 16 * ks + 2 * t4);
-          const uint32_t bq1 = lds32(sQT + (8 * nd + g) * kQTP + 16 * ks + 2 * t4 + 8);
-          mma16816<DT>(dk[nd], ad, bq0, bq1);
+        for (int nd = 0; nd < 8; nd += 2) {
+          uint32_t bo[4], bq[4];
+          ldb2(sDOT, kQTP, 8 * nd, 16 * ks, lane, bo);
+          ldb2(sQT, kQTP, 8 * nd, 16 * ks, lane, bq);
+          mma16816<DT>(dv[nd], ap, bo[0], bo[1]);
+          mma16816<DT>(dv[nd + 1], ap, bo[2], bo[3]);
+          mma16816<DT>(dk[nd], ad, bq[0], bq[1]);
+          mma16816<DT>(dk[nd + 1], ad, bq[2], bq[3]);
         }
       }
       __syncthreads();  // every warp's dS is in shared memory
@@ -521,17 +536,18 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[mb][e] = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < kBR / 16; ++kk) {
-          const uint32_t b0 = lds32(sKT + (8 * warp + g) * kKTP + 16 * kk + 2 * t4);
-          const uint32_t b1 = lds32(sKT + (8 * warp + g) * kKTP + 16 * kk + 2 * t4 + 8);
+        for (int kk = 0; kk < kBR / 16; kk += 2) {
+          // B of this warp's 8 dims for k-steps kk and kk + 1 (the x4 load's two "n-blocks" are
+          // read here as two k-steps of one n-block: rows 8 warp .. + 7, columns 16 kk .. + 31)
+          uint32_t b[4];
+          ldsm4(sKT + (8 * warp + (lane & 7)) * kKTP + 16 * kk + 8 * (lane >> 3), b);
 #pragma unroll
           for (int mb = 0; mb < 2; ++mb) {
-            uint32_t a4[4];
-            a4[0] = lds32(sDS + (16 * mb + g) * kKTP + 16 * kk + 2 * t4);
-            a4[1] = lds32(sDS + (16 * mb + g + 8) * kKTP + 16 * kk + 2 * t4);
-            a4[2] = lds32(sDS + (16 * mb + g) * kKTP + 16 * kk + 2 * t4 + 8);
-            a4[3] = lds32(sDS + (16 * mb + g + 8) * kKTP + 16 * kk + 2 * t4 + 8);
-            mma16816<DT>(acc[mb], a4, b0, b1);
+            uint32_t a4[4], a5[4];
+            lda(sDS, kKTP, 16 * mb, 16 * kk, lane, a4);
+            lda(sDS, kKTP, 16 * mb, 16 * kk + 16, lane, a5);
+            mma16816<DT>(acc[mb], a4, b[0], b[1]);
+            mma16816<DT>(acc[mb], a5, b[2], b[3]);
           }
         }
 #pragma unroll
