@@ -381,6 +381,45 @@ def run_rope(wl, steps, warmup, dev_index, dims=64):
     return {"ms": ms, "bytes": abytes, "nsets": nsets, "clocks": clk.summary(), "dims": dims}
 
 
+def run_backward(wl, steps, warmup, dev_index):
+    """pk_attend_backward on the workload (the forward's out and lse computed once, outside the
+    timed region; a fixed random dout). Useful FLOP: 640 per visible pair (S, dP, dV, dQ, dK)."""
+    import torch
+
+    import rope_cu_tile_gb300 as pk
+
+    pk.load()
+    dev = torch.device("cuda", dev_index)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    qkv, cos, sin, cu = device_tensors(wl, torch, dev)
+    with torch.cuda.stream(stream):
+        out, lse = pk.attend(qkv, cos, sin, cu, wl.H, wl.window, wl.scale, stream=stream)
+        g = torch.Generator(device=dev).manual_seed(5)
+        dout = torch.randn(out.shape, generator=g, device=dev).to(out.dtype)
+        dqkv = torch.empty_like(qkv)
+    torch.cuda.synchronize()
+
+    def step():
+        pk.attend_backward(qkv, cos, sin, cu, wl.H, wl.window, wl.scale, out, lse, dout, dqkv=dqkv, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev_index) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(steps):
+                step()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+    if pk.last_status(stream) != 0:
+        raise RuntimeError("device error in pk_attend_backward")
+    return {"ms": ev0.elapsed_time(ev1) / steps, "clocks": clk.summary()}
+
+
 def roofline(wl, attend_ms, peaks, peak_src):
     flops, abytes = work(wl)
     t_bw = abytes / (peaks["hbm_gbs"] * 1e9)
@@ -410,8 +449,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="global", choices=list(synth.CONFIG_NAMES))
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
-    ap.add_argument("--op", default="attend", choices=["attend", "rope"],
-                    help="attend: the attention path (default); rope: the standalone rotation")
+    ap.add_argument("--op", default="attend", choices=["attend", "rope", "backward"],
+                    help="attend: the attention path (default); rope: the standalone rotation; "
+                         "backward: pk_attend_backward")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -469,6 +509,25 @@ def main():
                              "frac": gbs / peaks["hbm_gbs"], "peak_source": psrc, "traffic": None,
                              "kernel": "pk_rope_kernel"},
                 "gpu_launches": args.steps, "clocks": r["clocks"]}
+        print(json.dumps(line))
+        return
+    if args.op == "backward":
+        if rank != 0:
+            return
+        r = run_backward(wl, args.steps, args.warmup, local)
+        peaks, psrc = load_peaks()
+        bflops = 2.5 * flops  # 640 against the forward's 256 per visible pair
+        tfs = bflops / (r["ms"] * 1e-3) / 1e12
+        cfg.update({"op": "pk_attend_backward (dqkv from dout; forward's out and lse precomputed)",
+                    "useful_gflop": bflops / 1e9})
+        line = {"metric": "pk_attend_backward: useful TFLOP/s on 1 GB300; % of roofline", "value": tfs,
+                "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+                "data": "synthetic", "config": cfg,
+                "roofline": {"bound": "tensor", "achieved": tfs, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": tfs / peaks["bf16_tflops"], "peak_source": psrc, "traffic": None,
+                             "kernel": "pk_bwd_mma_kernel" if wl.dtype != "f32" else "pk_bwd_main_kernel"},
+                "gpu_launches": 4 * args.steps, "clocks": r["clocks"]}
         print(json.dumps(line))
         return
     if world > 1:

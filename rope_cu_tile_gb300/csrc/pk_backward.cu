@@ -62,20 +62,46 @@ __device__ __forceinline__ void stf2(void* p, int64_t i, float a, float b) {
   }
 }
 
-// D [h * T + t] = sum_d dout[t, h, d] out[t, h, d]
+// D [h * T + t] = sum_d dout[t, h, d] out[t, h, d]. A row (t, h) is 64 contiguous elements of
+// both arrays (rows of one token are contiguous too): L lanes read one row 16 bytes each
+// (L = 8 for 16-bit types, 16 for fp32), so a warp reads 32 / L whole rows per load, and the
+// row's lanes sum by shuffles.
 template <int DT>
 __global__ void __launch_bounds__(256) pk_bwd_prep_kernel(const void* __restrict__ out, const void* __restrict__ dout,
                                                           float* __restrict__ D, int H, long long T) {
+  constexpr int kEl = DT == PK_F32 ? 4 : 8;  // elements per 16-byte piece
+  constexpr int kLanes = kD / kEl;           // lanes per row
+  constexpr int kRows = 32 / kLanes;         // rows per warp load
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / kLanes, part = lane % kLanes;
   const long long n = T * H;
-  for (long long u = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; u < n;
-       u += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long t = u / H;
-    const int h = static_cast<int>(u % H);
-    const int64_t at = t * H * kD + h * kD;
+  const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long u0 = gw * kRows; u0 < n; u0 += nw * kRows) {
+    const long long u = u0 + sub;  // row (t, h) = (u / H, u % H): element offset u * 64
     float acc = 0.f;
-#pragma unroll 8
-    for (int d = 0; d < kD; ++d) acc = fmaf(ldf<DT>(dout, at + d), ldf<DT>(out, at + d), acc);
-    D[static_cast<int64_t>(h) * T + t] = acc;
+    if (u < n) {
+      const uint4 o4 = *reinterpret_cast<const uint4*>(static_cast<const char*>(out) + (u * kD + part * kEl) * (DT == PK_F32 ? 4 : 2));
+      const uint4 g4 = *reinterpret_cast<const uint4*>(static_cast<const char*>(dout) + (u * kD + part * kEl) * (DT == PK_F32 ? 4 : 2));
+      const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, gw4[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        if constexpr (DT == PK_F32) {
+          acc = fmaf(__uint_as_float(ow[w]), __uint_as_float(gw4[w]), acc);
+        } else if constexpr (DT == PK_BF16) {
+          acc = fmaf(__uint_as_float(ow[w] << 16), __uint_as_float(gw4[w] << 16), acc);
+          acc = fmaf(__uint_as_float(ow[w] & 0xffff0000u), __uint_as_float(gw4[w] & 0xffff0000u), acc);
+        } else {
+          acc = fmaf(__half2float(__ushort_as_half(static_cast<unsigned short>(ow[w] & 0xffffu))),
+                     __half2float(__ushort_as_half(static_cast<unsigned short>(gw4[w] & 0xffffu))), acc);
+          acc = fmaf(__half2float(__ushort_as_half(static_cast<unsigned short>(ow[w] >> 16))),
+                     __half2float(__ushort_as_half(static_cast<unsigned short>(gw4[w] >> 16))), acc);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = kLanes / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (u < n && part == 0) D[static_cast<int64_t>(u % H) * T + u / H] = acc;
   }
 }
 
@@ -635,7 +661,7 @@ cudaError_t launch_backward_t(const void* qkv, const void* cos_t, const void* si
   cudaError_t e = kMma ? cudaMemsetAsync(dq, 0, static_cast<size_t>(T) * H * kD * sizeof(float), stream)
                        : cudaMemsetAsync(dk, 0, static_cast<size_t>(2) * T * H * kD * sizeof(float), stream);
   if (e != cudaSuccess) return e;
-  const long long prep_blocks = min(static_cast<long long>(sms) * 8, (T * H + 255) / 256);
+  const long long prep_blocks = min(static_cast<long long>(sms) * 8, (T * H + 31) / 32);
   pk_bwd_prep_kernel<DT><<<static_cast<unsigned int>(max(prep_blocks, 1ll)), 256, 0, stream>>>(out, dout, D, H, T);
   if constexpr (kMma)
     pk_bwd_mma_kernel<DT><<<sms * 2, kMmaThreads, kMmaSmem, stream>>>(qkv, cos_t, sin_t, cu, tiles, ctl, lse, dout, D,
