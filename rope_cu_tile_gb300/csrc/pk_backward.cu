@@ -353,8 +353,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
 pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, const void* __restrict__ sin_t,
                   const uint32_t* __restrict__ cu, const TileRec* __restrict__ tiles, Ctl* ctl,
                   const float* __restrict__ lse, const void* __restrict__ dout, const float* __restrict__ D,
-                  float* __restrict__ dq_acc, float* __restrict__ dk_acc, float* __restrict__ dv_acc, int H,
-                  long long T, int window, float scale) {
+                  float* __restrict__ dq_acc, void* __restrict__ dqkv, int H, long long T, int window,
+                  float scale) {
   extern __shared__ __align__(16) uint16_t mma_smem[];
   uint16_t* sK = mma_smem;                // [128][kKP]   K' (rotated)
   uint16_t* sV = sK + kBR * kKP;          // [128][kKP]   V
@@ -416,18 +416,19 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
       }
     }
     // this thread's two keys (rows g and g + 8 of the warp's 16): validity and visible queries
-    int64_t klo[2], khi[2];
+    int64_t klo[2], khi[2], kstart[2];
     bool kok[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int kr = warp * 16 + g + 8 * e;
       kok[e] = kr < nkeys;
-      klo[e] = khi[e] = 0;
+      klo[e] = khi[e] = kstart[e] = 0;
       if (kok[e]) {
         const uint32_t b = rec.q0 + kr;
         const uint32_t sb = rec.kind == 0 ? rec.seq : seq_of_token(cu, rec.seq, rec.nseq, b);
         const int64_t ss = __ldg(cu + sb), se = __ldg(cu + sb + 1);
         klo[e] = ss;
+        kstart[e] = ss;
         khi[e] = se;
         if (window > 0) {
           klo[e] = max(ss, static_cast<int64_t>(b) - window);
@@ -587,17 +588,31 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
           }
       }
     }
-    // dK' and dV of this warp's keys, written once (fp32)
+    // dk = rot^T(dk') and dv of this warp's keys, rounded once and written to dqkv: this thread
+    // holds dims 8 nd + 2 t4 + {0, 1} of its keys, so both members u and u + 32 of each rotary pair
+    // (n-blocks nd and nd + 4)
 #pragma unroll
     for (int kr = 0; kr < 2; ++kr) {
       if (!kok[kr]) continue;
       const int64_t b = static_cast<int64_t>(rec.q0) + warp * 16 + g + 8 * kr;
+      const int64_t pos = b - kstart[kr];
+      const int64_t row = b * ldq + h * kD;
 #pragma unroll
-      for (int nd = 0; nd < 8; ++nd) {
-        const int64_t at = b * hd + h * kD + 8 * nd + 2 * t4;
-        *reinterpret_cast<float2*>(dk_acc + at) = make_float2(scale * dk[nd][2 * kr], scale * dk[nd][2 * kr + 1]);
-        *reinterpret_cast<float2*>(dv_acc + at) = make_float2(dv[nd][2 * kr], dv[nd][2 * kr + 1]);
+      for (int nd = 0; nd < 4; ++nd) {
+        float ya[2], yb[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int u = 8 * nd + 2 * t4 + i;
+          const float c = ldf<DT>(cos_t, pos * kHalf + u), sn = ldf<DT>(sin_t, pos * kHalf + u);
+          const float xa = scale * dk[nd][2 * kr + i], xb = scale * dk[nd + 4][2 * kr + i];
+          ya[i] = fmaf(xa, c, xb * sn);
+          yb[i] = fmaf(xb, c, -xa * sn);
+        }
+        stf2<DT>(dqkv, row + hd + 8 * nd + 2 * t4, ya[0], ya[1]);
+        stf2<DT>(dqkv, row + hd + kHalf + 8 * nd + 2 * t4, yb[0], yb[1]);
       }
+#pragma unroll
+      for (int nd = 0; nd < 8; ++nd) stf2<DT>(dqkv, row + 2 * hd + 8 * nd + 2 * t4, dv[nd][2 * kr], dv[nd][2 * kr + 1]);
     }
   }
 }
@@ -608,7 +623,7 @@ template <int DT>
 __global__ void __launch_bounds__(256)
 pk_bwd_finish_kernel(const void* __restrict__ cos_t, const void* __restrict__ sin_t, const uint32_t* __restrict__ cu,
                      int S, long long T, int H, const float* __restrict__ dq_acc, const float* __restrict__ dk_acc,
-                     const float* __restrict__ dv_acc, void* __restrict__ dqkv) {
+                     const float* __restrict__ dv_acc, void* __restrict__ dqkv, int dq_only) {
   const int lane = threadIdx.x & 31;
   const long long gw = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nw = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -627,17 +642,21 @@ pk_bwd_finish_kernel(const void* __restrict__ cos_t, const void* __restrict__ si
       const int64_t g = t * hd + h * kD;
       // rot^T: y_a = x_a c + x_b s, y_b = x_b c - x_a s
       const float qa = dq_acc[g + lane], qb = dq_acc[g + lane + kHalf];
-      const float ka = dk_acc[g + lane], kb = dk_acc[g + lane + kHalf];
       const int64_t o = t * ldq + h * kD;
-      float y[4] = {fmaf(qa, c, qb * sn), fmaf(qb, c, -qa * sn), fmaf(ka, c, kb * sn), fmaf(kb, c, -ka * sn)};
+      const float y0 = fmaf(qa, c, qb * sn), y1 = fmaf(qb, c, -qa * sn);
       // lanes write pairs of neighbouring features: gather them by shuffle
-      const float qa1 = __shfl_down_sync(0xffffffffu, y[0], 1), qb1 = __shfl_down_sync(0xffffffffu, y[1], 1);
-      const float ka1 = __shfl_down_sync(0xffffffffu, y[2], 1), kb1 = __shfl_down_sync(0xffffffffu, y[3], 1);
+      const float y01 = __shfl_down_sync(0xffffffffu, y0, 1), y11 = __shfl_down_sync(0xffffffffu, y1, 1);
       if ((lane & 1) == 0) {
-        stf2<DT>(dqkv, o + lane, y[0], qa1);
-        stf2<DT>(dqkv, o + lane + kHalf, y[1], qb1);
-        stf2<DT>(dqkv, o + hd + lane, y[2], ka1);
-        stf2<DT>(dqkv, o + hd + lane + kHalf, y[3], kb1);
+        stf2<DT>(dqkv, o + lane, y0, y01);
+        stf2<DT>(dqkv, o + lane + kHalf, y1, y11);
+      }
+      if (dq_only) continue;  // dk and dv were written by the main kernel
+      const float ka = dk_acc[g + lane], kb = dk_acc[g + lane + kHalf];
+      const float z0 = fmaf(ka, c, kb * sn), z1 = fmaf(kb, c, -ka * sn);
+      const float z01 = __shfl_down_sync(0xffffffffu, z0, 1), z11 = __shfl_down_sync(0xffffffffu, z1, 1);
+      if ((lane & 1) == 0) {
+        stf2<DT>(dqkv, o + hd + lane, z0, z01);
+        stf2<DT>(dqkv, o + hd + lane + kHalf, z1, z11);
       }
       const float2 v = *reinterpret_cast<const float2*>(dv_acc + g + 2 * lane);
       stf2<DT>(dqkv, o + 2 * hd + 2 * lane, v.x, v.y);
@@ -665,13 +684,13 @@ cudaError_t launch_backward_t(const void* qkv, const void* cos_t, const void* si
   pk_bwd_prep_kernel<DT><<<static_cast<unsigned int>(max(prep_blocks, 1ll)), 256, 0, stream>>>(out, dout, D, H, T);
   if constexpr (kMma)
     pk_bwd_mma_kernel<DT><<<sms * 2, kMmaThreads, kMmaSmem, stream>>>(qkv, cos_t, sin_t, cu, tiles, ctl, lse, dout, D,
-                                                                       dq, dk, dv, H, T, window, scale);
+                                                                       dq, dqkv, H, T, window, scale);
   else
     pk_bwd_main_kernel<DT><<<sms * 2, kBwdThreads, kBwdSmem, stream>>>(qkv, cos_t, sin_t, cu, tiles, ctl, lse, dout, D,
                                                                         dq, dk, dv, H, T, window, scale);
   const long long fin_blocks = min(static_cast<long long>(sms) * 8, (T + 7) / 8);
   pk_bwd_finish_kernel<DT><<<static_cast<unsigned int>(max(fin_blocks, 1ll)), 256, 0, stream>>>(
-      cos_t, sin_t, cu, S, T, H, dq, dk, dv, dqkv);
+      cos_t, sin_t, cu, S, T, H, dq, dk, dv, dqkv, kMma ? 1 : 0);
   return cudaGetLastError();
 }
 
