@@ -286,24 +286,23 @@ pk_bwd_main_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t,
 // the key tile owning the work: visibility is symmetric (same sequence, |i - j| <= w), so a
 // tile record's rows serve as a key tile and its key range as the queries that see those keys.
 // Per work item (record, head): 8 warps x 16 keys; the key tile's K' (rotated, rounded to the
-// element type), K'^T and V stay in shared memory; queries come 32 at a time (Q', Q'^T, dout,
-// dout^T, lse, D). Per chunk each warp forms S^T = K' Q'^T and dP^T = V dout^T (16 MMAs each),
-// P^T and dS^T in registers, and accumulates dV += P^T dout and dK' += dS^T Q' in registers;
-// dS goes to shared memory and the CTA forms the chunk's dQ' = dS K' (warp w: dims 8w .. 8w+7),
-// added to the fp32 accumulator with atomics (other records' keys add to the same queries).
-// dK' and dV of each key are written once at the end of the item. Fragments come by ldmatrix
-// from [row][element] tiles whose rows start on 16 bytes (strides of 72, 40 and 136 elements keep
-// the eight rows of each 8x8 load in distinct banks). Measured shares (global workload, parts
-// knocked out): the query chunks' staging about 10 %, the dQ' atomics about 5 %; the rest is the
-// products and the element-wise P and dS.
+// element type) and V stay in shared memory; queries come 32 at a time (Q', dout, lse, D).
+// Per chunk each warp forms S^T = K' Q'^T and dP^T = V dout^T (16 MMAs each), P^T and dS^T in
+// registers, and accumulates dV += P^T dout and dK' += dS^T Q' in registers; dS goes to shared
+// memory and the CTA forms the chunk's dQ' = dS K' (warp w: dims 8w .. 8w+7), added to the fp32
+// accumulator with atomics (other records' keys add to the same queries). dK' and dV of each key
+// are complete at the end of the item: rotated back and written once. Fragments come by
+// ldmatrix from [row][element] tiles whose rows start on 16 bytes (strides of 72 and 136
+// elements keep the eight rows of each 8x8 load in distinct banks); the operands used
+// transposed (dout and Q' for dV and dK', K' for dQ') come by transposing loads rather than
+// transposed copies.
 
 constexpr int kMmaWarps = 8;
 constexpr int kMmaThreads = 32 * kMmaWarps;
 constexpr int kQc = 32;          // queries per chunk
 constexpr int kKP = kD + 8;      // row stride (16-bit elements) of [row][dim] tiles
-constexpr int kKTP = kBR + 8;    // row stride of K'^T [dim][key] and dS [query][key]
-constexpr int kQTP = kQc + 8;    // row stride of Q'^T and dout^T [dim][query]
-constexpr int kMmaSmemHalves = 2 * kBR * kKP + kD * kKTP + 2 * kQc * kKP + 2 * kD * kQTP + kQc * kKTP;
+constexpr int kKTP = kBR + 8;    // row stride of dS [query][key]
+constexpr int kMmaSmemHalves = 2 * kBR * kKP + 2 * kQc * kKP + kQc * kKTP;
 constexpr int kMmaSmem = kMmaSmemHalves * 2 + 2 * kQc * 4;
 
 template <int DT>
@@ -321,6 +320,17 @@ __device__ __forceinline__ void ldsm4(const uint16_t* p, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(a));
+}
+__device__ __forceinline__ void ldsm4t(const uint16_t* p, uint32_t (&r)[4]) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+// the B fragments (16 x 8) of n-blocks n0 and n0 + 8 at k-step k0 from a row-major [k][n] tile
+// (transposing load): r[0], r[1] for n0 and r[2], r[3] for n0 + 8
+__device__ __forceinline__ void ldb2t(const uint16_t* tile, int stride, int n0, int k0, int lane, uint32_t (&r)[4]) {
+  ldsm4t(tile + (k0 + (lane & 7) + 8 * ((lane >> 3) & 1)) * stride + n0 + 8 * (lane >> 4), r);
 }
 // the A fragment (16 x 16, row-major tile with `stride` elements per row) at (row0, col0)
 __device__ __forceinline__ void lda(const uint16_t* tile, int stride, int row0, int col0, int lane, uint32_t (&r)[4]) {
@@ -358,12 +368,9 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
   extern __shared__ __align__(16) uint16_t mma_smem[];
   uint16_t* sK = mma_smem;                // [128][kKP]   K' (rotated)
   uint16_t* sV = sK + kBR * kKP;          // [128][kKP]   V
-  uint16_t* sKT = sV + kBR * kKP;         // [64][kKTP]   K'^T
-  uint16_t* sQ = sKT + kD * kKTP;         // [32][kKP]    Q' of the chunk
+  uint16_t* sQ = sV + kBR * kKP;          // [32][kKP]    Q' of the chunk
   uint16_t* sDO = sQ + kQc * kKP;         // [32][kKP]    dout of the chunk
-  uint16_t* sQT = sDO + kQc * kKP;        // [64][kQTP]   Q'^T
-  uint16_t* sDOT = sQT + kD * kQTP;       // [64][kQTP]   dout^T
-  uint16_t* sDS = sDOT + kD * kQTP;       // [32][kKTP]   dS [query][key]
+  uint16_t* sDS = sDO + kQc * kKP;        // [32][kKTP]   dS [query][key]
   float* sLse = reinterpret_cast<float*>(sDS + kQc * kKTP);  // [32]
   float* sD = sLse + kQc;                                       // [32]
   __shared__ unsigned int s_item;
@@ -401,8 +408,6 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
           const uint16_t y1 = to16<DT>(x1 * c - x2 * sn), y2 = to16<DT>(x1 * sn + x2 * c);
           sK[kr * kKP + u] = y1;
           sK[kr * kKP + u + kHalf] = y2;
-          sKT[u * kKTP + kr] = y1;
-          sKT[(u + kHalf) * kKTP + kr] = y2;
         }
         for (int e = 0; e < 32; ++e)
           sV[kr * kKP + half * 32 + e] = static_cast<const uint16_t*>(qkv)[v + half * 32 + e];
@@ -410,7 +415,6 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
         for (int e = 0; e < 16; ++e) {
           const int u = half * 16 + e;
           sK[kr * kKP + u] = sK[kr * kKP + u + kHalf] = 0;
-          sKT[u * kKTP + kr] = sKT[(u + kHalf) * kKTP + kr] = 0;
         }
         for (int e = 0; e < 32; ++e) sV[kr * kKP + half * 32 + e] = 0;
       }
@@ -444,7 +448,7 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
 
     const uint32_t qend = rec.k0 + rec.nk;
     for (uint32_t qb = rec.k0; qb < qend; qb += kQc) {
-      __syncthreads();  // the previous chunk is done with sQ, sDO, sQT, sDOT, sDS (and the key tile is staged)
+      __syncthreads();  // the previous chunk is done with sQ, sDO, sDS (and the key tile is staged)
       // stage 32 queries: thread (row t / 8, 4 rotary pairs and 8 dout values)
       {
         const int qr = tid >> 3, part = tid & 7;
@@ -460,15 +464,11 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
             const uint16_t y1 = to16<DT>(x1 * c - x2 * sn), y2 = to16<DT>(x1 * sn + x2 * c);
             sQ[qr * kKP + u] = y1;
             sQ[qr * kKP + u + kHalf] = y2;
-            sQT[u * kQTP + qr] = y1;
-            sQT[(u + kHalf) * kQTP + qr] = y2;
           }
           const int64_t go = static_cast<int64_t>(a) * hd + h * kD;
           for (int e = 0; e < 8; ++e) {
             const int d = part * 8 + e;
-            const uint16_t o = static_cast<const uint16_t*>(dout)[go + d];
-            sDO[qr * kKP + d] = o;
-            sDOT[d * kQTP + qr] = o;
+            sDO[qr * kKP + d] = static_cast<const uint16_t*>(dout)[go + d];
           }
           if (part == 0) {
             sLse[qr] = __ldg(lse + static_cast<int64_t>(h) * T + a);
@@ -478,12 +478,10 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
           for (int e = 0; e < 4; ++e) {
             const int u = part * 4 + e;
             sQ[qr * kKP + u] = sQ[qr * kKP + u + kHalf] = 0;
-            sQT[u * kQTP + qr] = sQT[(u + kHalf) * kQTP + qr] = 0;
           }
           for (int e = 0; e < 8; ++e) {
             const int d = part * 8 + e;
             sDO[qr * kKP + d] = 0;
-            sDOT[d * kQTP + qr] = 0;
           }
           if (part == 0) sLse[qr] = sD[qr] = 0.f;
         }
@@ -546,8 +544,8 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
 #pragma unroll
         for (int nd = 0; nd < 8; nd += 2) {
           uint32_t bo[4], bq[4];
-          ldb2(sDOT, kQTP, 8 * nd, 16 * ks, lane, bo);
-          ldb2(sQT, kQTP, 8 * nd, 16 * ks, lane, bq);
+          ldb2t(sDO, kKP, 8 * nd, 16 * ks, lane, bo);
+          ldb2t(sQ, kKP, 8 * nd, 16 * ks, lane, bq);
           mma16816<DT>(dv[nd], ap, bo[0], bo[1]);
           mma16816<DT>(dv[nd + 1], ap, bo[2], bo[3]);
           mma16816<DT>(dk[nd], ad, bq[0], bq[1]);
@@ -566,8 +564,10 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
         for (int kk = 0; kk < kBR / 16; kk += 2) {
           // B of this warp's 8 dims for k-steps kk and kk + 1 (the x4 load's two "n-blocks" are
           // read here as two k-steps of one n-block: rows 8 warp .. + 7, columns 16 kk .. + 31)
+          // B of this warp's 8 dims for k-steps kk and kk + 1 from K' [key][dim] (transposing
+          // load): matrices at key rows 16 kk, 16 kk + 8, 16 kk + 16, 16 kk + 24
           uint32_t b[4];
-          ldsm4(sKT + (8 * warp + (lane & 7)) * kKTP + 16 * kk + 8 * (lane >> 3), b);
+          ldsm4t(sK + (16 * kk + (lane & 7) + 8 * (lane >> 3)) * kKP + 8 * warp, b);
 #pragma unroll
           for (int mb = 0; mb < 2; ++mb) {
             uint32_t a4[4], a5[4];
