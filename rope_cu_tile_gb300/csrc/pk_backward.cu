@@ -47,6 +47,16 @@ __device__ __forceinline__ float ldf(const void* p, int64_t i) {
   }
 }
 
+// the value of 16-bit storage bits (a shared-memory copy of an element)
+template <int DT>
+__device__ __forceinline__ float bits_f(uint16_t u) {
+  if constexpr (DT == PK_BF16) {
+    return __uint_as_float(static_cast<uint32_t>(u) << 16);
+  } else {
+    return __half2float(__ushort_as_half(u));
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ void stf2(void* p, int64_t i, float a, float b) {
   if constexpr (DT == PK_F32) {
@@ -302,8 +312,9 @@ constexpr int kMmaThreads = 32 * kMmaWarps;
 constexpr int kQc = 32;          // queries per chunk
 constexpr int kKP = kD + 8;      // row stride (16-bit elements) of [row][dim] tiles
 constexpr int kKTP = kBR + 8;    // row stride of dS [query][key]
-constexpr int kMmaSmemHalves = 2 * kBR * kKP + 2 * kQc * kKP + kQc * kKTP;
-constexpr int kMmaSmem = kMmaSmemHalves * 2 + 2 * kQc * 4;
+// K', V; two buffers of Q' and dout; dS; two raw staging buffers of q rows and of cos | sin rows
+constexpr int kMmaSmemHalves = 2 * kBR * kKP + 4 * kQc * kKP + kQc * kKTP + 4 * kQc * kD;
+constexpr int kMmaSmem = kMmaSmemHalves * 2 + 4 * kQc * 4;
 
 template <int DT>
 __device__ __forceinline__ uint16_t to16(float x) {
@@ -321,6 +332,18 @@ __device__ __forceinline__ void ldsm4(const uint16_t* p, uint32_t (&r)[4]) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(a));
 }
+// asynchronous global -> shared copy of kBytes (4 or 16) bytes; when `valid` is false nothing is
+// read and the destination is filled with zeros
+template <int kBytes>
+__device__ __forceinline__ void cp_async(void* dst, const void* src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(d), "l"(__cvta_generic_to_global(src)),
+               "n"(kBytes), "r"(valid ? kBytes : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_b() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all_b() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void ldsm4t(const uint16_t* p, uint32_t (&r)[4]) {
   const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -368,11 +391,13 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
   extern __shared__ __align__(16) uint16_t mma_smem[];
   uint16_t* sK = mma_smem;                // [128][kKP]   K' (rotated)
   uint16_t* sV = sK + kBR * kKP;          // [128][kKP]   V
-  uint16_t* sQ = sV + kBR * kKP;          // [32][kKP]    Q' of the chunk
-  uint16_t* sDO = sQ + kQc * kKP;         // [32][kKP]    dout of the chunk
-  uint16_t* sDS = sDO + kQc * kKP;        // [32][kKTP]   dS [query][key]
-  float* sLse = reinterpret_cast<float*>(sDS + kQc * kKTP);  // [32]
-  float* sD = sLse + kQc;                                       // [32]
+  uint16_t* sQ2 = sV + kBR * kKP;         // [2][32][kKP] Q' of the chunk (two buffers)
+  uint16_t* sDO2 = sQ2 + 2 * kQc * kKP;   // [2][32][kKP] dout of the chunk
+  uint16_t* sDS = sDO2 + 2 * kQc * kKP;   // [32][kKTP]   dS [query][key]
+  uint16_t* rawX2 = sDS + kQc * kKTP;     // [2][32][64]  q rows as loaded
+  uint16_t* rawCS2 = rawX2 + 2 * kQc * kD;  // [2][32][64]  cos (32) | sin (32) rows of the queries' positions
+  float* sLse2 = reinterpret_cast<float*>(rawCS2 + 2 * kQc * kD);  // [2][32]
+  float* sD2 = sLse2 + 2 * kQc;                                     // [2][32]
   __shared__ unsigned int s_item;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -447,46 +472,57 @@ pk_bwd_mma_kernel(const void* __restrict__ qkv, const void* __restrict__ cos_t, 
       for (int e = 0; e < 4; ++e) dv[n][e] = dk[n][e] = 0.f;
 
     const uint32_t qend = rec.k0 + rec.nk;
-    for (uint32_t qb = rec.k0; qb < qend; qb += kQc) {
-      __syncthreads();  // the previous chunk is done with sQ, sDO, sDS (and the key tile is staged)
-      // stage 32 queries: thread (row t / 8, 4 rotary pairs and 8 dout values)
+    // chunk copies: thread (query row t / 8, 16-byte piece t % 8) copies its piece of the raw q
+    // row, of the cos | sin rows at the query's position and of the dout row; lanes of piece 0
+    // also copy lse and D. Chunk i + 1 is in flight while chunk i is computed.
+    auto issue = [&](uint32_t qb, int buf) {
+      const int qr = tid >> 3, part = tid & 7;
+      const uint32_t a = qb + qr;
+      const bool ok = a < qend;
+      int64_t pos = 0;
+      if (ok) {
+        const uint32_t sa = rec.kind == 0 ? rec.seq : seq_of_token(cu, rec.seq, rec.nseq, a);
+        pos = static_cast<int64_t>(a) - __ldg(cu + sa);
+      }
+      const int64_t ar = ok ? static_cast<int64_t>(a) : 0;
+      const uint16_t* q16 = static_cast<const uint16_t*>(qkv);
+      const uint16_t* c16 = static_cast<const uint16_t*>(part < 4 ? cos_t : sin_t);
+      cp_async<16>(rawX2 + (buf * kQc + qr) * kD + part * 8, q16 + ar * ldq + h * kD + part * 8, ok);
+      cp_async<16>(rawCS2 + (buf * kQc + qr) * kD + part * 8, c16 + pos * kHalf + (part & 3) * 8, ok);
+      cp_async<16>(sDO2 + (buf * kQc + qr) * kKP + part * 8,
+                   static_cast<const uint16_t*>(dout) + ar * hd + h * kD + part * 8, ok);
+      if (part == 0) {
+        cp_async<4>(sLse2 + buf * kQc + qr, lse + static_cast<int64_t>(h) * T + ar, ok);
+        cp_async<4>(sD2 + buf * kQc + qr, D + static_cast<int64_t>(h) * T + ar, ok);
+      }
+      cp_async_commit_b();
+    };
+    if (rec.nk > 0) issue(rec.k0, 0);
+    int ci = 0;
+    for (uint32_t qb = rec.k0; qb < qend; qb += kQc, ++ci) {
+      const int buf = ci & 1;
+      uint16_t* sQ = sQ2 + buf * kQc * kKP;
+      const uint16_t* sDO = sDO2 + buf * kQc * kKP;
+      const float* sLse = sLse2 + buf * kQc;
+      const float* sD = sD2 + buf * kQc;
+      cp_async_wait_all_b();  // this chunk's copies (the only ones in flight)
+      __syncthreads();        // ... visible to all; the previous chunk is done with sDS (and the key tile is staged)
+      // rotate this chunk's q rows: thread (row t / 8, 4 rotary pairs)
       {
         const int qr = tid >> 3, part = tid & 7;
-        const uint32_t a = qb + qr;
-        if (a < qend) {
-          const uint32_t sa = rec.kind == 0 ? rec.seq : seq_of_token(cu, rec.seq, rec.nseq, a);
-          const int64_t pos = static_cast<int64_t>(a) - __ldg(cu + sa);
-          const int64_t x = static_cast<int64_t>(a) * ldq + h * kD;
-          for (int e = 0; e < 4; ++e) {
-            const int u = part * 4 + e;
-            const float c = ldf<DT>(cos_t, pos * kHalf + u), sn = ldf<DT>(sin_t, pos * kHalf + u);
-            const float x1 = ldf<DT>(qkv, x + u), x2 = ldf<DT>(qkv, x + u + kHalf);
-            const uint16_t y1 = to16<DT>(x1 * c - x2 * sn), y2 = to16<DT>(x1 * sn + x2 * c);
-            sQ[qr * kKP + u] = y1;
-            sQ[qr * kKP + u + kHalf] = y2;
-          }
-          const int64_t go = static_cast<int64_t>(a) * hd + h * kD;
-          for (int e = 0; e < 8; ++e) {
-            const int d = part * 8 + e;
-            sDO[qr * kKP + d] = static_cast<const uint16_t*>(dout)[go + d];
-          }
-          if (part == 0) {
-            sLse[qr] = __ldg(lse + static_cast<int64_t>(h) * T + a);
-            sD[qr] = __ldg(D + static_cast<int64_t>(h) * T + a);
-          }
-        } else {
-          for (int e = 0; e < 4; ++e) {
-            const int u = part * 4 + e;
-            sQ[qr * kKP + u] = sQ[qr * kKP + u + kHalf] = 0;
-          }
-          for (int e = 0; e < 8; ++e) {
-            const int d = part * 8 + e;
-            sDO[qr * kKP + d] = 0;
-          }
-          if (part == 0) sLse[qr] = sD[qr] = 0.f;
+        const uint16_t* xr = rawX2 + (buf * kQc + qr) * kD;
+        const uint16_t* cr = rawCS2 + (buf * kQc + qr) * kD;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int u = part * 4 + e;
+          const float c = bits_f<DT>(cr[u]), sn = bits_f<DT>(cr[kHalf + u]);
+          const float x1 = bits_f<DT>(xr[u]), x2 = bits_f<DT>(xr[u + kHalf]);
+          sQ[qr * kKP + u] = to16<DT>(x1 * c - x2 * sn);
+          sQ[qr * kKP + u + kHalf] = to16<DT>(x1 * sn + x2 * c);
         }
       }
-      __syncthreads();
+      if (qb + kQc < qend) issue(qb + kQc, buf ^ 1);
+      __syncthreads();  // this chunk's Q' is in place
 
       // S^T = K'_w Q'^T and dP^T = V_w dout^T: 16 keys x 32 queries (four n-blocks of 8)
       float st[4][4], dpt[4][4];
