@@ -14,7 +14,7 @@
 // a head vector (one 4-byte word in 16 bits, 8 bytes in fp32), so a head vector is one
 // coalesced 128- or 256-byte access; the partner of a feature sits in another lane (halves) or
 // the same lane (interleaved pairs) and comes by shuffle. Head vectors are processed twelve at a
-// time so that several loads are in flight per warp. Arithmetic in fp32, one rounding to the
+// time so that several loads are in flight per warp; the grid is one wave of resident blocks. Arithmetic in fp32, one rounding to the
 // element type.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -116,8 +116,10 @@ __device__ __forceinline__ void flag(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// At most 64 registers a thread, so that four blocks are resident per SM: the kernel is bound by
+// the bytes in flight per SM.
 template <int DT>
-__global__ void __launch_bounds__(kRopeThreads) pk_rope_kernel(const RopeArgs a) {
+__global__ void __launch_bounds__(kRopeThreads, 4) pk_rope_kernel(const RopeArgs a) {
   using P2 = Pair2<DT>;
   using Word = typename P2::Word;
   const int lane = threadIdx.x & 31;
@@ -221,9 +223,13 @@ __global__ void __launch_bounds__(kRopeThreads) pk_rope_kernel(const RopeArgs a)
 
 template <int DT>
 cudaError_t launch_rope(const RopeArgs& a, int sms, cudaStream_t stream) {
-  // enough warps to cover every token, at most eight 256-thread blocks per SM
+  // one wave: as many blocks as are resident at once (each warp then takes a longer run of
+  // tokens), never more warps than tokens
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pk_rope_kernel<DT>, kRopeThreads, 0);
+  if (e != cudaSuccess) return e;
   const long long warps_needed = a.T;
-  const long long blocks = min(static_cast<long long>(sms) * 8, (warps_needed + 7) / 8);
+  const long long blocks = min(static_cast<long long>(sms) * max(per_sm, 1), (warps_needed + 7) / 8);
   pk_rope_kernel<DT><<<static_cast<unsigned int>(blocks > 0 ? blocks : 1), kRopeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
