@@ -1,5 +1,7 @@
 /*
- * pk.h -- packed-sequence RoPE attention, forward pass, on one GB300 (sm_103a).
+ * pk.h -- packed-sequence RoPE attention on one GB300 (sm_103a): the forward pass (pk_attend
+ * and its typed forms, pk_attend_noalloc, pk_attend_mixed), its backward pass
+ * (pk_attend_backward), the tile schedule (pk_schedule) and the standalone rotation (pk_rope).
  *
  * The operation (hanzo-kernel 0.2.42 packed.rs, module doc and fn attend / fn attend_ref):
  * attention over packed variable-length sequences straight from a packed QKV projection,
@@ -184,8 +186,11 @@ int pk_attend_noalloc(int dtype, const void *qkv, const void *cos, const void *s
  *   - dqkv [T, 3*H*64] (dtype): written with the gradients of q | k | v.
  *   - bf16 / fp16: tensor-core products with q', k', P and dS rounded to dtype as operands and
  *     fp32 accumulation; fp32: fp32 arithmetic on the CUDA cores. One rounding of dqkv to
- *     dtype. Allocates, on first use
- *     per (device, stream), an fp32 scratch of H*T*(1 + 3*64) floats (kept with the workspace).
+ *     dtype.
+ *   - Allocates, on first use per (device, stream) and when a larger H*T arrives, an fp32
+ *     scratch of about H*T*(1 + 3*64) floats (kept with the workspace, freed by pk_release).
+ *     The capture rule of the workspace applies to it: a captured call that would have to
+ *     allocate it returns PK_ERR_CAPTURE, nothing launched.
  *   - Alignment and errors as pk_attend (dout, dqkv 16-byte aligned); device errors (bad cu)
  *     in pk_last_status(stream).
  */
