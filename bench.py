@@ -21,6 +21,10 @@ copies of the input and output buffers whose total is well above the L2 size.
 
 --impl reference times the oracle (the slow CPU statement of the method) as the reference
 arm, on the same workload and metric.
+
+--op rope and --op backward time the standalone rotation (pk_rope: GB/s against the measured
+HBM copy rate) and the backward pass (pk_attend_backward: useful TFLOP/s at 640 flop per
+visible pair) on the same workloads; the default --op attend is the forward above.
 """
 
 from __future__ import annotations
