@@ -506,7 +506,9 @@ int oracle_attend_backward(const void *qkv, int dt, const void *cosb, const void
                     pr[j] = exp(pr[j] - m);
                     z += pr[j];
                 }
+#if ORACLE_MUTANT != 20
                 for (int64_t j = 0; j < L; j++) pr[j] /= z;
+#endif                                                    /* planted (20): not normalised */
                 /* D_i = dout_i . O_i */
                 double di = 0.0;
                 for (int d = 0; d < HD; d++) {
@@ -527,7 +529,11 @@ int oracle_attend_backward(const void *qkv, int dt, const void *cosb, const void
                     dsr[j] = pr[j] * (dp - di);
 #endif
                     for (int d = 0; d < HD; d++) {
+#if ORACLE_MUTANT == 19
+                        dv[j * HD + d] += dsr[j] * ld(dout, ddt, (start + i) * hd + h * HD + d);  /* planted */
+#else
                         dv[j * HD + d] += pr[j] * ld(dout, ddt, (start + i) * hd + h * HD + d);
+#endif
                         dk[j * HD + d] += scale * dsr[j] * qr[i * HD + d];
                     }
                 }
@@ -542,7 +548,11 @@ int oracle_attend_backward(const void *qkv, int dt, const void *cosb, const void
                     dq[d] = scale * acc;
 #endif
                 }
+#if ORACLE_MUTANT == 18
+                rope_vector(dq, DT_F64, 0, i, cosb, sinb, tdt, HD, 0, 0, y);  /* planted: forwards */
+#else
                 rope_vector(dq, DT_F64, 0, i, cosb, sinb, tdt, HD, 0, 1, y);
+#endif
                 for (int d = 0; d < HD; d++) dqkv[(start + i) * ldq + h * HD + d] = y[d];
             }
             for (int64_t j = 0; j < L; j++) {

@@ -33,6 +33,9 @@ MUTANTS = {
     15: "backward: D term dropped from dS",
     16: "backward: key gradient rotated forwards",
     17: "backward: scale missing from the query gradient",
+    18: "backward: query gradient rotated forwards",
+    19: "backward: value gradient weighted by dS instead of P",
+    20: "backward: probabilities not normalised",
 }
 
 
