@@ -402,11 +402,18 @@ static void rope_vector(const void *x, int dt, int64_t at, int64_t pos, const vo
     for (int j = 0; j < h; j++) {
 #if ORACLE_MUTANT == 13
         int a = j, b = j + h;                                      /* planted: layout ignored */
+#elif ORACLE_MUTANT == 21
+        int a = traditional ? 2 * j : j;
+        int b = traditional ? 2 * j + 1 : j + HD / 2;              /* planted: pairs across the head */
 #else
         int a = traditional ? 2 * j : j;
         int b = traditional ? 2 * j + 1 : j + h;
 #endif
+#if ORACLE_MUTANT == 22
+        double c = ld(sinb, tdt, pos * h + j), sn = ld(cosb, tdt, pos * h + j);  /* planted: swapped */
+#else
         double c = ld(cosb, tdt, pos * h + j), sn = ld(sinb, tdt, pos * h + j);
+#endif
         double xa = ld(x, dt, at + a), xb = ld(x, dt, at + b);
 #if ORACLE_MUTANT == 12
         int fwd = 1;                                               /* planted: direction ignored */

@@ -36,6 +36,8 @@ MUTANTS = {
     18: "backward: query gradient rotated forwards",
     19: "backward: value gradient weighted by dS instead of P",
     20: "backward: probabilities not normalised",
+    21: "rope op: partial dims paired across the whole head",
+    22: "rope op: cos and sin tables swapped",
 }
 
 
