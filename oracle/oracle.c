@@ -170,8 +170,25 @@ static void one_row(const problem *p, int64_t start, int64_t L, int h, int64_t i
     }
 #if ORACLE_MUTANT == 6
     *lse_out = m + log2(z);                               /* planted: wrong log base */
+#elif ORACLE_MUTANT == 24
+    *lse_out = log(z);                                    /* planted: the max left out */
 #else
     *lse_out = m + log(z);
+#endif
+#if ORACLE_MUTANT == 23
+    /* planted: the values rotated like the keys */
+    double *vr = malloc(sizeof(double) * L * HD);
+    if (vr) {
+        for (int64_t j = 0; j < L; j++)
+            rope_row(p->qkv, p->dt, (start + j) * ldq + 2 * hd + h * HD, j, p->cosb, p->sinb, p->tdt, vr + j * HD);
+        for (int d = 0; d < HD; d++) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < L; j++) acc += sc[j] / z * vr[j * HD + d];
+            out_row[d] = acc;
+        }
+        free(vr);
+        return;
+    }
 #endif
     for (int d = 0; d < HD; d++) {
         double acc = 0.0;

@@ -38,6 +38,8 @@ MUTANTS = {
     20: "backward: probabilities not normalised",
     21: "rope op: partial dims paired across the whole head",
     22: "rope op: cos and sin tables swapped",
+    23: "values rotated like the keys",
+    24: "lse without the row maximum",
 }
 
 
