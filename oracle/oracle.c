@@ -680,7 +680,11 @@ int oracle_schedule(const uint32_t *cu, int S, int64_t T, int window, uint32_t *
         /* a long sequence: packed.rs fn layout's tiles at rows 0, BR, 2BR, ... with the key
          * range of each clipped to the window */
         for (int64_t i0 = 0; i0 < L; i0 += SCH_BR) {
+#if ORACLE_MUTANT == 26
+            int64_t rows = SCH_BR;                                  /* planted: last piece overruns */
+#else
             int64_t rows = L - i0 < SCH_BR ? L - i0 : SCH_BR;
+#endif
             int64_t q0 = start + i0;
             int64_t k0 = start, k1 = start + L;
             if (window > 0) {
@@ -690,6 +694,9 @@ int oracle_schedule(const uint32_t *cu, int S, int64_t T, int window, uint32_t *
 #elif ORACLE_MUTANT == 9
                 if (q0 - window - 1 > k0) k0 = q0 - window - 1;              /* planted: loose */
                 if (q0 + rows + window < k1) k1 = q0 + rows + window;
+#elif ORACLE_MUTANT == 25
+                if (q0 - window > k0) k0 = q0 - window;
+                k1 = q0 + rows + window;                     /* planted: not clipped at the end */
 #else
                 if (q0 - window > k0) k0 = q0 - window;
                 if (q0 + rows + window < k1) k1 = q0 + rows + window;

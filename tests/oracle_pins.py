@@ -510,6 +510,9 @@ def schedule_failures(tiles: np.ndarray, cu: np.ndarray, window: int) -> list[st
                 fails.append("piece rows")
         else:
             fails.append("kind")
+        if q0[n] < 0 or rows[n] < 1 or q0[n] + rows[n] > T:
+            fails.append("rows outside [0, T)")
+            continue
         # key range: holds every visible key, and its ends are visible to some row
         a = np.arange(q0[n], q0[n] + rows[n])
         sid = np.searchsorted(cu, a, side="right") - 1

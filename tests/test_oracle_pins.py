@@ -40,6 +40,8 @@ MUTANTS = {
     22: "rope op: cos and sin tables swapped",
     23: "values rotated like the keys",
     24: "lse without the row maximum",
+    25: "schedule: key range not clipped at the sequence end",
+    26: "schedule: last piece of a long sequence given a full tile of rows",
 }
 
 
