@@ -1,5 +1,6 @@
-"""bench.py and __graft_entry__.py import cleanly and their host-side tables are well formed
-(no GPU needed)."""
+"""bench.py and __graft_entry__.py import cleanly, their host-side tables are well formed, and
+the bench's reporting logic (roofline bound and fraction, clock summary) computes what its JSON
+line claims (no GPU needed)."""
 
 import importlib.util
 import os
@@ -26,3 +27,41 @@ def test_bench_imports_and_traffic_table():
 def test_graft_entry_imports():
     entry = _load("__graft_entry__")
     assert callable(entry.build) and callable(entry.smoke)
+
+
+def test_roofline_bound_and_fraction():
+    import synth
+
+    bench = _load("bench")
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0}
+    # many short sequences: bytes dominate -> HBM bound
+    short = synth.make_lens_workload("probe_short", [8] * 64, "bf16", H=2, window=0)
+    r = bench.roofline(short, 0.01, peaks, "measured")
+    flops, nbytes = bench.work(short)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - nbytes / 1e-5 / 1e9) < 1e-9 * r["achieved"]
+    assert abs(r["frac"] - r["achieved"] / 6000.0) < 1e-12
+    assert r["traffic"] is None  # no ncu counters recorded for this workload
+    # one long sequence: flops dominate -> tensor bound
+    long = synth.make_lens_workload("probe_long", [4096], "bf16", H=2, window=0)
+    r = bench.roofline(long, 1.0, peaks, "fallback")
+    flops, nbytes = bench.work(long)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak_source"] == "fallback"
+    assert abs(r["achieved"] - flops / 1e-3 / 1e12) < 1e-9 * r["achieved"]
+    assert abs(r["t_roof_us"] - flops / 2000e12 * 1e6) < 1e-9
+
+
+def test_clock_summary():
+    bench = _load("bench")
+    c = bench.ClockSampler(0)
+    c.lines = [
+        "0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 2070, 2070, 950.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 345, 2070, 100.0, 0x0, Not Active, Not Active, Not Active, Not Active",  # idle sample
+        "garbage",
+    ]
+    s = c.summary()
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 3
+    c.lines = []
+    assert c.summary() is None
