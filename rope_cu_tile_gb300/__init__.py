@@ -158,6 +158,32 @@ def dtype_code(t) -> int:
     return m[t.dtype]
 
 
+def _need(t, shape, dtype, what):
+    """A caller's buffer must have exactly this shape and dtype and be a contiguous CUDA tensor:
+    the C ABI receives only its address and writes the sizes the call implies."""
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError(f"{what} must be {tuple(shape)} {dtype}, not {tuple(t.shape)} {t.dtype}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous CUDA tensor")
+
+
+def _check_inputs(qkv, cos, sin, cu, H, half):
+    """qkv [T, 3*H*64], cos/sin [P, half] of qkv's dtype, cu [S+1] int32/uint32; all contiguous
+    CUDA tensors."""
+    torch = _torch()
+    if qkv.dim() != 2 or qkv.shape[1] != 3 * H * 64:
+        raise ValueError("qkv must be [T, 3*H*64]")
+    if cos.dtype != qkv.dtype or sin.dtype != qkv.dtype or cos.shape != sin.shape:
+        raise TypeError("cos/sin must have qkv's dtype and one shape")
+    if cos.dim() != 2 or cos.shape[1] != half:
+        raise ValueError(f"cos/sin must be [P, {half}]")
+    if cu.dim() != 1 or cu.dtype not in (torch.int32, torch.uint32):
+        raise TypeError("cu must be a 1-D int32 or uint32 tensor")
+    for t in (qkv, cos, sin, cu):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+
+
 def _stream_handle(stream):
     torch = _torch()
     if stream is None:
@@ -173,22 +199,19 @@ def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=N
     torch = _torch()
     T = qkv.shape[0]
     S = cu.shape[0] - 1
-    if qkv.dim() != 2 or qkv.shape[1] != 3 * H * 64:
-        raise ValueError("qkv must be [T, 3*H*64]")
-    if cos.dtype != qkv.dtype or sin.dtype != qkv.dtype:
-        raise TypeError("cos/sin must have qkv's dtype")
-    if cu.dtype not in (torch.int32, torch.uint32):
-        raise TypeError("cu must be int32 or uint32")
-    for t in (qkv, cos, sin, cu):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("inputs must be contiguous CUDA tensors")
-    odt = qkv.dtype if out_dtype is None else out_dtype
+    _check_inputs(qkv, cos, sin, cu, H, 32)
+    # the output type: out_dtype, else a given out's, else qkv's
+    odt = out_dtype if out_dtype is not None else (out.dtype if out is not None else qkv.dtype)
     if odt != qkv.dtype and qkv.dtype != torch.float32:
         raise TypeError("a different output type needs float32 inputs")
     if out is None:
         out = torch.empty((T, H * 64), dtype=odt, device=qkv.device)
+    else:
+        _need(out, (T, H * 64), odt, "out")
     if lse is None:
         lse = torch.empty((H, T), dtype=torch.float32, device=qkv.device)
+    else:
+        _need(lse, (H, T), torch.float32, "lse")
     if odt != qkv.dtype:
         rc = pk_attend_mixed(dtype_code(out), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(),
                              S, T, H, window, float(scale), out.data_ptr(), lse.data_ptr(), _stream_handle(stream))
@@ -206,13 +229,14 @@ def attend_backward(qkv, cos, sin, cu, H: int, window: int, scale: float, out, l
     torch = _torch()
     T = qkv.shape[0]
     S = cu.shape[0] - 1
-    for t in (qkv, cos, sin, cu, out, lse, dout):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("inputs must be contiguous CUDA tensors")
-    if out.dtype != qkv.dtype or dout.dtype != qkv.dtype or lse.dtype != torch.float32:
-        raise TypeError("out and dout must have qkv's dtype, lse float32")
+    _check_inputs(qkv, cos, sin, cu, H, 32)
+    _need(out, (T, H * 64), qkv.dtype, "out")
+    _need(dout, (T, H * 64), qkv.dtype, "dout")
+    _need(lse, (H, T), torch.float32, "lse")
     if dqkv is None:
         dqkv = torch.empty_like(qkv)
+    else:
+        _need(dqkv, tuple(qkv.shape), qkv.dtype, "dqkv")
     rc = pk_attend_backward(dtype_code(qkv), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(), S, T, H,
                             window, float(scale), out.data_ptr(), lse.data_ptr(), dout.data_ptr(), dqkv.data_ptr(),
                             _stream_handle(stream))
@@ -228,19 +252,13 @@ def rope(qkv, cos, sin, cu, H: int, dims: int = 64, traditional: bool = False, i
     torch = _torch()
     T = qkv.shape[0]
     S = cu.shape[0] - 1
-    if qkv.dim() != 2 or qkv.shape[1] != 3 * H * 64:
-        raise ValueError("qkv must be [T, 3*H*64]")
-    if cos.dtype != qkv.dtype or sin.dtype != qkv.dtype or cos.shape != sin.shape:
-        raise TypeError("cos/sin must have qkv's dtype and one shape")
-    if cos.dim() != 2 or cos.shape[1] != dims // 2:
-        raise ValueError("cos/sin must be [P, dims/2]")
-    if cu.dtype not in (torch.int32, torch.uint32):
-        raise TypeError("cu must be int32 or uint32")
-    for t in (qkv, cos, sin, cu):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("inputs must be contiguous CUDA tensors")
+    _check_inputs(qkv, cos, sin, cu, H, dims // 2)
     if out is None:
         out = torch.empty_like(qkv)
+    else:
+        _need(out, tuple(qkv.shape), qkv.dtype, "out")
+    if status is not None:
+        _need(status, (1,), torch.int32, "status")
     rc = pk_rope(dtype_code(qkv), qkv.data_ptr(), out.data_ptr(), cos.data_ptr(), sin.data_ptr(),
                  cos.shape[0], cu.data_ptr(), S, T, H, int(dims), int(bool(traditional)), int(bool(inverse)),
                  status.data_ptr() if status is not None else None, _stream_handle(stream))
@@ -251,6 +269,8 @@ def rope(qkv, cos, sin, cu, H: int, dims: int = 64, traditional: bool = False, i
 def schedule(cu, T: int, window: int, stream=None):
     """Tile records [NT, 8] (int32 tensor holding the uint32 fields) of the device scheduler."""
     torch = _torch()
+    if cu.dim() != 1 or cu.dtype not in (torch.int32, torch.uint32) or not cu.is_cuda or not cu.is_contiguous():
+        raise ValueError("cu must be a contiguous 1-D int32 or uint32 CUDA tensor")
     cap = int(load().pk_schedule_capacity(T))
     tiles = torch.zeros((max(cap, 1), 8), dtype=torch.int32, device=cu.device)
     rc, nt = pk_schedule(cu.data_ptr(), cu.shape[0] - 1, T, window, tiles.data_ptr(), cap,
