@@ -50,3 +50,19 @@ def test_pins_catch_planted_mistake(tmp_path, mutant):
     path = oracle.compile_oracle(str(tmp_path / f"liboracle_m{mutant}.so"), mutant=mutant)
     bad = oracle.Oracle(path)
     assert P.all_failures(bad), f"no pin fails for mutant {mutant}: {MUTANTS[mutant]}"
+
+
+def test_oracle_rejects_malformed_offsets(orc):
+    # the offsets must run from 0 and never decrease (the GPU path reports the same cases as
+    # PK_ERR_BAD_CU); the oracle refuses them rather than computing something
+    import numpy as np
+
+    for cu in ([1, 4, 9], [0, 6, 4, 9]):
+        cu = np.asarray(cu, dtype=np.uint32)
+        with pytest.raises(ValueError):
+            orc.schedule(cu, 0)
+        T = int(cu[-1])
+        qkv = np.zeros((T, 3 * 64), dtype=np.float64)
+        tbl = np.zeros((T, 32), dtype=np.float64)
+        with pytest.raises(ValueError):
+            orc.attend(qkv, tbl, tbl, cu, 1, 0, 0.125, "f64")
