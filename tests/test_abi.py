@@ -110,3 +110,43 @@ def test_rope_argument_checks_need_no_gpu(lib):
 def test_schedule_capacity_matches_oracle(lib, orc):
     for T in (0, 1, 63, 64, 65, 131072, 10**9):
         assert lib.pk_schedule_capacity(T) == orc.schedule_cap(T)
+
+
+def test_backward_mixed_noalloc_argument_checks_need_no_gpu(lib):
+    # rejected before any CUDA call, like pk_attend's
+    p = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1002)
+    null = ctypes.c_void_p(0)
+
+    def bwd(**kw):
+        a = dict(dtype=1, qkv=p, cos=p, sin=p, cu=p, S=1, T=5, H=2, window=0, scale=0.125, out=p, lse=p,
+                 dout=p, dqkv=p, stream=null)
+        a.update(kw)
+        return pk.pk_attend_backward(a["dtype"], a["qkv"], a["cos"], a["sin"], a["cu"], a["S"], a["T"], a["H"],
+                                     a["window"], a["scale"], a["out"], a["lse"], a["dout"], a["dqkv"],
+                                     a["stream"])
+
+    assert bwd(dtype=7) == 1
+    assert bwd(H=0) == 1
+    assert bwd(dout=null) == 1
+    assert bwd(dqkv=null) == 1
+    assert bwd(dout=odd) == 2
+    assert bwd(dqkv=odd) == 2
+    assert bwd(qkv=odd) == 2
+    assert bwd(T=0, S=0, qkv=null, cos=null, sin=null, cu=null, out=null, lse=null, dout=null, dqkv=null) == 0
+
+    assert pk.pk_attend_mixed(7, p, p, p, p, 1, 5, 2, 0, 0.125, p, p, null) == 1       # out type
+    assert pk.pk_attend_mixed(2, odd, p, p, p, 1, 5, 2, 0, 0.125, p, p, null) == 2     # qkv alignment
+
+    def noalloc(**kw):
+        a = dict(dtype=1, qkv=p, cos=p, sin=p, cu=p, S=1, T=5, H=2, window=0, scale=0.125, out=p, lse=p,
+                 status=null, stream=null)
+        a.update(kw)
+        return pk.pk_attend_noalloc(a["dtype"], a["qkv"], a["cos"], a["sin"], a["cu"], a["S"], a["T"], a["H"],
+                                    a["window"], a["scale"], a["out"], a["lse"], a["status"], a["stream"])
+
+    assert noalloc(dtype=7) == 1
+    assert noalloc(T=(1 << 20) + 1) == 9   # PK_ERR_TOO_LARGE past PK_NOALLOC_MAX_T
+    assert noalloc(cu=null) == 1
+    assert noalloc(status=odd) == 2
+    assert noalloc(T=0, S=0, qkv=null, cos=null, sin=null, cu=null, out=null, lse=null) == 0
