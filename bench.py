@@ -3,9 +3,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--config NAME]
 
 One step = one pk_attend call (tile scheduler + attention kernel) over the whole workload.
-The default workload is the encoder-base global layer (H=12, bf16, 64 sequences of U{32..512}
-tokens, RoPE base 160000, every key), the configuration the metric is quoted on; --config
-picks another of tiny / global / local / long / short for diagnosis.
+The default workload is the largest of the five configurations that fits one GPU, the long
+packed batch (H=16, bf16, log-normal lengths of median 256 clipped to [1, 8192], packed to
+T = 131072 tokens, RoPE base 160000, every key); --config picks another of tiny / global /
+local / long / short.
 
 Reported (one JSON line on rank 0):
   value       useful TFLOP/s: 256 x (query, key) pairs the window lets through x heads,
@@ -88,6 +89,23 @@ def load_peaks():
         d = json.load(open(p))
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def input_sets(wl) -> int:
+    """How many copies of the input and output buffers the timed steps rotate through, so
+    that no step finds its inputs in the 129 MB L2 (1 when one set is already larger than
+    twice the L2)."""
+    e = synth.elem_size(wl.dtype)
+    set_bytes = wl.T * 3 * wl.H * 64 * e + wl.T * wl.H * 64 * e + 4 * wl.H * wl.T
+    return max(1, min(8, int(np.ceil(3 * L2_BYTES / set_bytes)))) if set_bytes < 2 * L2_BYTES else 1
+
+
+def l2_note(wl) -> str:
+    n = input_sets(wl)
+    if n == 1:
+        return "inputs larger than L2"
+    return (f"rotating {n} input/output sets ({n} x {(wl.T * 3 * wl.H * 64 * synth.elem_size(wl.dtype)) / 1e6:.0f} "
+            f"MB qkv) so no step finds its inputs in the 129 MB L2")
 
 
 def work(wl):
@@ -221,8 +239,8 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
     stream = torch.cuda.Stream(device=dev)
     flops, abytes = work(wl)
     e = synth.elem_size(wl.dtype)
-    set_bytes = wl.T * 3 * wl.H * 64 * e + wl.T * wl.H * 64 * e + 4 * wl.H * wl.T
-    nsets = max(1, min(8, int(np.ceil(3 * L2_BYTES / set_bytes)))) if set_bytes < 2 * L2_BYTES else 1
+    nsets = input_sets(wl)
+    max_len = int(wl.lens.max())
     qkv0, cos, sin, cu = device_tensors(wl, torch, dev)
     td = qkv0.dtype
     sets = []
@@ -234,7 +252,7 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
 
     def step(i):
         q, o, l = sets[i % nsets]
-        pk.attend(q, cos, sin, cu, wl.H, wl.window, wl.scale, out=o, lse=l, stream=stream)
+        pk.attend(q, cos, sin, cu, wl.H, wl.window, wl.scale, out=o, lse=l, stream=stream, max_len=max_len)
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -405,7 +423,8 @@ def run_backward(wl, steps, warmup, dev_index):
     torch.cuda.synchronize()
 
     def step():
-        pk.attend_backward(qkv, cos, sin, cu, wl.H, wl.window, wl.scale, out, lse, dout, dqkv=dqkv, stream=stream)
+        pk.attend_backward(qkv, cos, sin, cu, wl.H, wl.window, wl.scale, out, lse, dout, dqkv=dqkv, stream=stream,
+                           max_len=int(wl.lens.max()))
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -451,7 +470,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="global", choices=list(synth.CONFIG_NAMES))
+    ap.add_argument("--config", default="long", choices=list(synth.CONFIG_NAMES))
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
     ap.add_argument("--op", default="attend", choices=["attend", "rope", "backward"],
                     help="attend: the attention path (default); rope: the standalone rotation; "
@@ -469,7 +488,8 @@ def main():
     flops, abytes = work(wl)
     cfg = {"workload": f"{args.config}: {synth.CONFIG_TEXT[args.config]}", "T": wl.T, "S": wl.S, "H": wl.H,
            "D": 64, "window": wl.window, "scale": wl.scale, "seed": synth.CONFIG_NAMES.index(args.config),
-           "useful_gflop": flops / 1e9, "algorithmic_mb": abytes / 1e6}
+           "useful_gflop": flops / 1e9, "algorithmic_mb": abytes / 1e6,
+           "l2": l2_note(wl), "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
     if args.impl == "reference":
         if rank != 0:
@@ -540,10 +560,6 @@ def main():
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     r = run_gpu(wl, args.steps, args.warmup, rank, world, local)
     peaks, psrc = load_peaks()
-    cfg["l2"] = (f"rotating {r['nsets']} input/output sets ({r['nsets']} x "
-                 f"{(wl.T * 3 * wl.H * 64 * synth.elem_size(wl.dtype)) / 1e6:.0f} MB qkv) so no step finds its "
-                 f"inputs in the 129 MB L2" if r["nsets"] > 1 else "inputs larger than L2")
-    cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
     value = world * flops / (r["ms_per_step"] * 1e-3) / 1e12
     tokens_s = world * wl.T / (r["ms_per_step"] * 1e-3)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

@@ -245,7 +245,8 @@ const char *pk_status_string(int status);
 /* Library version: major * 10000 + minor * 100 + patch. */
 int pk_version(void);
 
-/* Frees every workspace (synchronizing the streams that own them). */
+/* Frees every workspace, after synchronizing each device that holds one (so it may be called
+ * after the streams the workspaces were made for have been destroyed). */
 int pk_release(void);
 
 #ifdef __cplusplus

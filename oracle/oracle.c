@@ -336,9 +336,15 @@ static int64_t seq_of(const uint32_t *cu, int S, int64_t a) {
     int64_t lo = 0, hi = S; /* answer in [lo, hi) */
     while (hi - lo > 1) {
         int64_t mid = (lo + hi) / 2;
+#if ORACLE_MUTANT == 27
+        if ((int64_t)cu[mid] < a) lo = mid; else hi = mid;  /* planted: a sequence's first token given to the one before */
+#else
         if ((int64_t)cu[mid] <= a) lo = mid; else hi = mid;
+#endif
     }
+#if ORACLE_MUTANT != 27
     while (lo < S && (int64_t)cu[lo + 1] <= a) lo++;   /* step over empty sequences */
+#endif
     return lo;
 }
 
@@ -349,7 +355,11 @@ static void *rows_worker(void *arg) {
         int64_t n = atomic_fetch_add(&job->next, 1);
         if (n >= job->n) break;
         int64_t a = job->tok[n];
+#if ORACLE_MUTANT == 28
+        int h = 0;                                       /* planted: the row's head ignored */
+#else
         int h = job->head[n];
+#endif
         int64_t s = seq_of(p->cu, p->S, a);
         int64_t start = p->cu[s];
         int64_t L = (int64_t)p->cu[s + 1] - start;

@@ -169,7 +169,7 @@ def _need(t, shape, dtype, what):
 
 def _check_inputs(qkv, cos, sin, cu, H, half):
     """qkv [T, 3*H*64], cos/sin [P, half] of qkv's dtype, cu [S+1] int32/uint32; all contiguous
-    CUDA tensors."""
+    CUDA tensors on one device."""
     torch = _torch()
     if qkv.dim() != 2 or qkv.shape[1] != 3 * H * 64:
         raise ValueError("qkv must be [T, 3*H*64]")
@@ -182,6 +182,36 @@ def _check_inputs(qkv, cos, sin, cu, H, half):
     for t in (qkv, cos, sin, cu):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("inputs must be contiguous CUDA tensors")
+    _same_device(qkv, cos, sin, cu)
+
+
+def _same_device(first, *rest):
+    """Every tensor on the device of the first: the library launches on one device and
+    dereferences every address there."""
+    for t in rest:
+        if t.device != first.device:
+            raise ValueError(f"tensors on different devices ({first.device} and {t.device})")
+
+
+def _check_stream(stream, device):
+    """A torch stream given for the call must belong to the tensors' device."""
+    dev = getattr(stream, "device", None)
+    if dev is not None and dev != device:
+        raise ValueError(f"stream of {dev} for tensors on {device}")
+
+
+def _check_table_rows(cu, rows: int, max_len):
+    """The tables must hold a row for every in-sequence position: rows >= the longest sequence.
+    Without max_len this reads the longest length back from the device (one reduction and a
+    synchronisation; skipped while a CUDA graph is being captured, where the caller vouches
+    for the tables)."""
+    torch = _torch()
+    if max_len is None:
+        if cu.shape[0] < 2 or (cu.is_cuda and torch.cuda.is_current_stream_capturing()):
+            return
+        max_len = int((cu[1:].to(torch.int64) - cu[:-1].to(torch.int64)).max().item())
+    if int(max_len) > rows:
+        raise ValueError(f"cos/sin hold {rows} positions but a sequence has {int(max_len)} tokens")
 
 
 def _stream_handle(stream):
@@ -192,14 +222,24 @@ def _stream_handle(stream):
 
 
 def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=None, stream=None,
-           out_dtype=None):
+           out_dtype=None, max_len=None):
     """out [T, H*64] (qkv's dtype) and lse [H, T] float32 for device tensors qkv [T, 3*H*64],
-    cos/sin [P, 32] (qkv's dtype) and cu [S+1] (int32 or uint32). For float32 inputs,
-    out_dtype=torch.float16 or torch.bfloat16 gives a 16-bit out (pk_attend_mixed)."""
+    cos/sin [P, 32] (qkv's dtype) and cu [S+1] (int32 or uint32), all on one device. For
+    float32 inputs, out_dtype=torch.float16 or torch.bfloat16 gives a 16-bit out
+    (pk_attend_mixed). max_len: the longest sequence's length, if the caller knows it
+    (otherwise it is read back from cu to check that the tables are long enough)."""
+    torch = _torch()
+    _check_inputs(qkv, cos, sin, cu, H, 32)
+    _check_stream(stream, qkv.device)
+    with torch.cuda.device(qkv.device):
+        _check_table_rows(cu, cos.shape[0], max_len)
+        return _attend(qkv, cos, sin, cu, H, window, scale, out, lse, stream, out_dtype)
+
+
+def _attend(qkv, cos, sin, cu, H, window, scale, out, lse, stream, out_dtype):
     torch = _torch()
     T = qkv.shape[0]
     S = cu.shape[0] - 1
-    _check_inputs(qkv, cos, sin, cu, H, 32)
     # the output type: out_dtype, else a given out's, else qkv's
     odt = out_dtype if out_dtype is not None else (out.dtype if out is not None else qkv.dtype)
     if odt != qkv.dtype and qkv.dtype != torch.float32:
@@ -212,6 +252,7 @@ def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=N
         lse = torch.empty((H, T), dtype=torch.float32, device=qkv.device)
     else:
         _need(lse, (H, T), torch.float32, "lse")
+    _same_device(qkv, out, lse)
     if odt != qkv.dtype:
         rc = pk_attend_mixed(dtype_code(out), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(),
                              S, T, H, window, float(scale), out.data_ptr(), lse.data_ptr(), _stream_handle(stream))
@@ -223,9 +264,10 @@ def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=N
     return out, lse
 
 
-def attend_backward(qkv, cos, sin, cu, H: int, window: int, scale: float, out, lse, dout, dqkv=None, stream=None):
+def attend_backward(qkv, cos, sin, cu, H: int, window: int, scale: float, out, lse, dout, dqkv=None, stream=None,
+                    max_len=None):
     """dqkv [T, 3*H*64] (qkv's dtype): the gradient of sum(dout * out) with respect to qkv, for
-    the forward's out and lse."""
+    the forward's out and lse (max_len as for attend)."""
     torch = _torch()
     T = qkv.shape[0]
     S = cu.shape[0] - 1
@@ -233,10 +275,19 @@ def attend_backward(qkv, cos, sin, cu, H: int, window: int, scale: float, out, l
     _need(out, (T, H * 64), qkv.dtype, "out")
     _need(dout, (T, H * 64), qkv.dtype, "dout")
     _need(lse, (H, T), torch.float32, "lse")
-    if dqkv is None:
-        dqkv = torch.empty_like(qkv)
-    else:
+    if dqkv is not None:
         _need(dqkv, tuple(qkv.shape), qkv.dtype, "dqkv")
+        _same_device(qkv, dqkv)
+    _same_device(qkv, out, lse, dout)
+    _check_stream(stream, qkv.device)
+    with torch.cuda.device(qkv.device):
+        _check_table_rows(cu, cos.shape[0], max_len)
+        if dqkv is None:
+            dqkv = torch.empty_like(qkv)
+        return _attend_backward(qkv, cos, sin, cu, S, T, H, window, scale, out, lse, dout, dqkv, stream)
+
+
+def _attend_backward(qkv, cos, sin, cu, S, T, H, window, scale, out, lse, dout, dqkv, stream):
     rc = pk_attend_backward(dtype_code(qkv), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(), S, T, H,
                             window, float(scale), out.data_ptr(), lse.data_ptr(), dout.data_ptr(), dqkv.data_ptr(),
                             _stream_handle(stream))
@@ -253,12 +304,20 @@ def rope(qkv, cos, sin, cu, H: int, dims: int = 64, traditional: bool = False, i
     T = qkv.shape[0]
     S = cu.shape[0] - 1
     _check_inputs(qkv, cos, sin, cu, H, dims // 2)
+    _check_stream(stream, qkv.device)
     if out is None:
         out = torch.empty_like(qkv)
     else:
         _need(out, tuple(qkv.shape), qkv.dtype, "out")
+        _same_device(qkv, out)
     if status is not None:
         _need(status, (1,), torch.int32, "status")
+        _same_device(qkv, status)
+    with torch.cuda.device(qkv.device):
+        return _rope(qkv, cos, sin, cu, S, T, H, dims, traditional, inverse, out, status, stream)
+
+
+def _rope(qkv, cos, sin, cu, S, T, H, dims, traditional, inverse, out, status, stream):
     rc = pk_rope(dtype_code(qkv), qkv.data_ptr(), out.data_ptr(), cos.data_ptr(), sin.data_ptr(),
                  cos.shape[0], cu.data_ptr(), S, T, H, int(dims), int(bool(traditional)), int(bool(inverse)),
                  status.data_ptr() if status is not None else None, _stream_handle(stream))

@@ -463,10 +463,16 @@ int pk_release(void) {
   int rc = PK_OK;
   int cur = 0;
   cudaGetDevice(&cur);
+  // each device with a workspace is synchronized as a whole (the streams the workspaces were
+  // made for may have been destroyed by now: their handles are not used again)
+  int synced = -1;
   for (auto& kv : g_ws) {
     if (!kv.second.base) continue;
     cudaSetDevice(kv.first.first);
-    if (cudaStreamSynchronize(kv.first.second) != cudaSuccess) rc = PK_ERR_CUDA;
+    if (kv.first.first != synced) {
+      if (cudaDeviceSynchronize() != cudaSuccess) rc = PK_ERR_CUDA;
+      synced = kv.first.first;
+    }
     cudaFree(kv.second.base);
     if (kv.second.bwd) cudaFree(kv.second.bwd);
   }

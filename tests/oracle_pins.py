@@ -19,6 +19,8 @@ What pins what:
   - window:    window 0 equals a window >= max length - 1, bit for bit.
   - permute:   permuting the sequences permutes the rows, bit for bit.
   - widen:     bf16 and fp16 inputs widen exactly (same result as float64 inputs).
+  - rows:      the row-at-a-time oracle equals the whole-batch one bit for bit and SDPA to
+               1e-12 on every (token, head), empty sequences anywhere in the batch.
   - schedule:  the tile records partition the rows, keep every visible key of each row in
                the key range, keep that range tight, and follow the grouping rule (greedy
                packing of short sequences within 1024-token windows).
@@ -558,6 +560,47 @@ def schedule_cases():
     return cases
 
 
+def pin_attend_rows(orc) -> list[str]:
+    """oracle_attend_rows (the row-at-a-time form, for spot checks of large outputs) finds each
+    token's sequence by a search over cu; every (token, head) it returns must equal the
+    whole-batch oracle bit for bit, and torch's SDPA over the packed batch to 1e-12, with
+    empty sequences at the start, between others and at the end, and windows 0, 1 and 64.
+    The tables have a few rows more than the longest sequence."""
+    fails = []
+    rng = np.random.default_rng(2024)
+    layouts = [
+        ("lead_empty", [0, 0, 7, 1, 30]),
+        ("between_empty", [5, 0, 0, 9, 0, 1, 0, 12]),
+        ("trail_empty", [17, 3, 0, 0]),
+        ("all_single", [1, 1, 0, 1, 1]),
+        ("mixed", [0, 70, 0, 2, 0, 0, 33, 1, 0]),
+    ]
+    for name, lens in layouts:
+        for w in (0, 1, 64):
+            wl = synth.make_lens_workload(f"{name}_w{w}", lens, "bf16", H=3, window=w, base=700.0,
+                                          seed=len(lens) + w, P=max(lens) + 8)
+            T = wl.T
+            tok = np.repeat(np.arange(T, dtype=np.int64), wl.H)
+            hd = np.tile(np.arange(wl.H, dtype=np.int32), T)
+            perm = rng.permutation(tok.shape[0])
+            tok, hd = tok[perm], hd[perm]
+            got_o, got_l = orc.attend_rows(wl.qkv, wl.cos, wl.sin, wl.cu, wl.H, wl.window, wl.scale,
+                                           wl.dtype, tok, hd)
+            full_o, full_l = orc.attend(wl.qkv, wl.cos, wl.sin, wl.cu, wl.H, wl.window, wl.scale, wl.dtype)
+            want_o = np.stack([full_o[t, h * D:(h + 1) * D] for t, h in zip(tok, hd)])
+            want_l = np.array([full_l[h, t] for t, h in zip(tok, hd)])
+            if not (np.array_equal(got_o, want_o) and np.array_equal(got_l, want_l)):
+                fails.append(f"rows vs whole batch {name} w{w}: "
+                             f"{np.max(np.abs(got_o - want_o)):.3e} / {np.max(np.abs(got_l - want_l)):.3e}")
+            qkv64, c64, s64 = _f64(wl)
+            ref_o, ref_l = sdpa_reference(qkv64, c64, s64, wl.cu, wl.H, wl.window, wl.scale)
+            ro = np.stack([ref_o[t, h * D:(h + 1) * D] for t, h in zip(tok, hd)])
+            rl = np.array([ref_l[h, t] for t, h in zip(tok, hd)])
+            if not (_rel_close(got_o, ro, 1e-12) and _rel_close(got_l, rl, 1e-12)):
+                fails.append(f"rows vs sdpa {name} w{w}")
+    return fails
+
+
 def pin_schedule(orc) -> list[str]:
     fails = []
     for name, cu, w in schedule_cases():
@@ -568,7 +611,7 @@ def pin_schedule(orc) -> list[str]:
 
 
 ALL_PINS = (pin_sdpa, pin_rope, pin_closed_forms, pin_probabilities, pin_window_and_permutation,
-            pin_widen, pin_schedule, pin_rope_op, pin_backward)
+            pin_widen, pin_schedule, pin_rope_op, pin_backward, pin_attend_rows)
 
 
 def all_failures(orc) -> list[str]:

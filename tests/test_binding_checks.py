@@ -53,3 +53,51 @@ def test_buffer_check():
         pk._need(t, (4, 64), torch.bfloat16, "out")
     with pytest.raises(ValueError, match="contiguous CUDA"):
         pk._need(t, (4, 64), torch.float16, "out")  # right shape and type, but on the host
+
+
+class _FakeCuda:
+    """Stands in for a contiguous CUDA tensor on a given device (no GPU needed): the checks
+    read only shape, dtype, dim, device and contiguity before anything reaches the library."""
+
+    def __init__(self, t, device):
+        self._t = t
+        self.device = torch.device(device)
+        self.is_cuda = True
+        self.shape = t.shape
+        self.dtype = t.dtype
+
+    def dim(self):
+        return self._t.dim()
+
+    def is_contiguous(self):
+        return True
+
+
+def test_tensors_on_different_devices_are_refused():
+    qkv, cos, sin, cu = inputs()
+    a = [_FakeCuda(x, "cuda:0") for x in (qkv, cos, sin, cu)]
+    pk._check_inputs(*a, 2, 32)  # one device: accepted
+    for k in range(1, 4):
+        b = list(a)
+        b[k] = _FakeCuda((qkv, cos, sin, cu)[k], "cuda:1")
+        with pytest.raises(ValueError, match="different devices"):
+            pk._check_inputs(*b, 2, 32)
+
+
+def test_stream_of_another_device_is_refused():
+    class S:
+        device = torch.device("cuda:1")
+
+    pk._check_stream(None, torch.device("cuda:0"))
+    pk._check_stream(12345, torch.device("cuda:0"))  # a raw handle carries no device
+    with pytest.raises(ValueError, match="stream"):
+        pk._check_stream(S(), torch.device("cuda:0"))
+
+
+def test_tables_shorter_than_a_sequence_are_refused():
+    cu = torch.tensor([0, 5, 40, 41], dtype=torch.int32)
+    pk._check_table_rows(cu, 35, 35)
+    with pytest.raises(ValueError, match="positions"):
+        pk._check_table_rows(cu, 34, 35)
+    with pytest.raises(ValueError, match="positions"):
+        pk._check_table_rows(cu, 34, None)  # the longest length read from cu: 35

@@ -1,12 +1,17 @@
 """The five measured configurations at full size, in the launch configuration the benchmark
-times (GPU): sampled rows against the oracle one by one, plus properties of every row.
+times (GPU): every element of out and lse against the whole-batch oracle, at the method's
+tolerances (fp32 1e-4 / 1e-4, bf16 2e-2 / 1e-2, fp16 5e-3 / 5e-3).
 
-Properties checked on the whole output (they hold at any size):
+Besides, properties that hold at any size are checked on the whole output:
   - every value is finite;
   - lse of a row is at least the row's own (diagonal) score, scale * q'_i . k'_i;
   - every output element lies between the smallest and largest value of that dimension over
     the row's visible keys (out is a convex combination of them), up to the tolerance.
+
+With PK_PARITY_REPORT set to a file name, each test appends one line "name max|dout| max|dlse|".
 """
+
+import os
 
 import numpy as np
 import pytest
@@ -15,26 +20,6 @@ import synth
 from gpu_util import TOL, device_inputs, max_err, run
 
 pytestmark = pytest.mark.gpu
-
-
-def sample_rows(wl, n_random=160, seed=0):
-    """(token, head) pairs: first/last rows of sequences, rows around 128-row tile edges,
-    and random rows."""
-    rng = np.random.default_rng(seed)
-    cu = wl.cu.astype(np.int64)
-    S, T, H = wl.S, wl.T, wl.H
-    toks = []
-    for s in rng.choice(S, size=min(S, 24), replace=False):
-        a, b = cu[s], cu[s + 1]
-        if b > a:
-            toks += [a, b - 1]
-            for e in (127, 128, 129):
-                if a + e < b:
-                    toks.append(a + e)
-    toks += list(rng.integers(0, T, n_random))
-    toks = np.asarray(toks, dtype=np.int64)
-    heads = rng.integers(0, H, toks.shape[0]).astype(np.int32)
-    return toks, heads
 
 
 def rotate(x, cos_rows, sin_rows):
@@ -78,18 +63,22 @@ def check_properties(wl, out, lse):
     assert worst_hull <= to, f"out outside the visible values' range by {worst_hull:.3e}"
 
 
+def _report(name, eo, el):
+    path = os.environ.get("PK_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(f"{name} {eo:.3e} {el:.3e}\n")
+
+
 @pytest.mark.parametrize("name", ["global", "local", "long", "short"])
 def test_config_full_size(pk, orc, name):
     wl = synth.make_config(name)
     got_o, got_l = run(pk, wl, inputs=device_inputs(wl))
-    tok, hd = sample_rows(wl)
-    want_o, want_l = orc.attend_rows(wl.qkv, wl.cos, wl.sin, wl.cu, wl.H, wl.window, wl.scale, wl.dtype,
-                                     tok, hd)
-    go = np.stack([got_o[t, h * 64:(h + 1) * 64] for t, h in zip(tok, hd)])
-    gl = np.array([got_l[h, t] for t, h in zip(tok, hd)])
+    want_o, want_l = orc.attend(wl.qkv, wl.cos, wl.sin, wl.cu, wl.H, wl.window, wl.scale, wl.dtype)
     to, tl = TOL[wl.dtype]
-    eo, el = max_err(go, want_o), max_err(gl, want_l)
-    assert eo <= to and el <= tl, f"{name}: max|dout| {eo:.3e}, max|dlse| {el:.3e} over {len(tok)} rows"
+    eo, el = max_err(got_o, want_o), max_err(got_l, want_l)
+    _report(name, eo, el)
+    assert eo <= to and el <= tl, f"{name}: max|dout| {eo:.3e}, max|dlse| {el:.3e} over every element"
     check_properties(wl, got_o, got_l)
 
 
@@ -97,4 +86,6 @@ def test_tiny_full(pk, orc):
     wl = synth.make_config("tiny")
     got_o, got_l = run(pk, wl)
     want_o, want_l = orc.attend(wl.qkv, wl.cos, wl.sin, wl.cu, wl.H, wl.window, wl.scale, wl.dtype)
-    assert max_err(got_o, want_o) <= 1e-4 and max_err(got_l, want_l) <= 1e-4
+    eo, el = max_err(got_o, want_o), max_err(got_l, want_l)
+    _report("tiny", eo, el)
+    assert eo <= 1e-4 and el <= 1e-4

@@ -42,6 +42,8 @@ MUTANTS = {
     24: "lse without the row maximum",
     25: "schedule: key range not clipped at the sequence end",
     26: "schedule: last piece of a long sequence given a full tile of rows",
+    27: "rows: a sequence's first token given to the sequence before",
+    28: "rows: the row's head ignored",
 }
 
 
