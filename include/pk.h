@@ -26,11 +26,15 @@
  *   lse = m + ln(sum_j exp(score_j - m)), out = sum_j exp(score_j - lse) v_{cu[s]+j}.
  * `window` = 0 lets every key of the sequence through (the pages' "0: every key").
  *
- * Precision: bf16 and fp16 inputs are multiplied on the tensor cores (tcgen05, fp32
- * accumulation) after rotation in fp32 (the rotated q and k are rounded to the input type);
- * a positive scale multiplies the fp32 scores, any other scale the rotated q; the
- * probabilities are rounded to the input type before the product with v. fp32 inputs are
- * computed in fp32 on the CUDA cores.
+ * Kernels and precision (enum pk_kernel; pk_forward_kernel says which one a call runs):
+ *   - 1 <= window <= 16, any element type: PK_KERNEL_BAND, CUDA cores, every product and sum
+ *     in fp32 from the stored values (a row sees at most 33 keys: the work is moving qkv).
+ *   - otherwise fp32 inputs: PK_KERNEL_F32, CUDA cores, fp32.
+ *   - otherwise bf16 and fp16 inputs: a tensor-core kernel (tcgen05, fp32 accumulation) after
+ *     rotation in fp32, the rotated q and k rounded to the input type; a positive scale
+ *     multiplies the fp32 scores, any other scale the rotated q; the probabilities are
+ *     rounded to the input type before the product with v. pk_attend and its typed forms
+ *     run PK_KERNEL_TC (or the one PK_ATTN names); pk_attend_tuned picks by timing.
  *
  * Conventions for every entry point below:
  *   - All array pointers are DEVICE pointers of the current CUDA device; the caller owns
@@ -50,10 +54,13 @@
  * Environment (read by the library, for tests and debugging):
  *   PK_TIMEOUT_MS          bound of every pipeline wait inside the kernels (default 2000);
  *                          read at the first call of the process.
- *   PK_DEBUG_SKIP_ARRIVE=1 test hook of the bf16 / fp16 path, read at every call: the
+ *   PK_DEBUG_SKIP_ARRIVE=1 test hook of the tensor-core kernels, read at every call: the
  *                          producer of each CTA withholds its first work-item hand-off, so
  *                          the call ends with PK_ERR_TIMEOUT after one wait bound and writes
  *                          no valid output; later calls without it are unaffected.
+ *   PK_ATTN=q4|tc_single   pk_attend and its typed forms run PK_KERNEL_Q4 or
+ *                          PK_KERNEL_TC_SINGLE instead of PK_KERNEL_TC for bf16 / fp16 inputs
+ *                          outside the narrow windows (read at every call).
  */
 #ifndef PK_H
 #define PK_H
@@ -84,6 +91,17 @@ enum pk_status {
 
 enum pk_dtype { PK_F32 = 0, PK_BF16 = 1, PK_F16 = 2 };
 
+/* The forward kernels (pk_kernel_name gives each one's name). */
+enum pk_kernel {
+    PK_KERNEL_BAND = 0,       /* narrow windows: CUDA cores, fp32, no tile schedule */
+    PK_KERNEL_F32 = 1,        /* fp32 inputs: CUDA cores, fp32, one tile record per CTA item */
+    PK_KERNEL_TC = 2,         /* 16-bit: tcgen05, two query tiles of a record pair per SM,
+                                 128-key stream tiles */
+    PK_KERNEL_Q4 = 3,         /* 16-bit: tcgen05, two pipes of two query tiles per SM,
+                                 64-key stream tiles */
+    PK_KERNEL_TC_SINGLE = 4   /* 16-bit: PK_KERNEL_TC with one tile record per work item */
+};
+
 /* Limits: T <= PK_MAX_T, H <= PK_MAX_H. */
 #define PK_MAX_T 2147483647LL
 #define PK_MAX_H 1024
@@ -113,6 +131,47 @@ int pk_attend_dt(int dtype, const void *qkv, const void *cos, const void *sin,
                  float *lse, struct CUstream_st *stream);
 
 /*
+ * pk_attend_tuned -- the forward pass at the fastest usable kernel for the call's shape
+ * (the pages' attend_tuned: each usable variant is timed once per key, the fastest is kept).
+ *   - The arguments of pk_attend_dt, plus `longest`: the length of the longest sequence
+ *     (host value; only the tuning key uses it).
+ *   - Key: (current device, dtype, H, window + 1 (0 when window = 0), T rounded up to a power
+ *     of two, longest rounded up to a power of two); pk_tune_key writes it as text.
+ *   - Usable kernels: PK_KERNEL_BAND for 1 <= window <= 16 (its fp32 arithmetic keeps fp16
+ *     inputs of large magnitude in tolerance), PK_KERNEL_F32 for other fp32 calls, and
+ *     PK_KERNEL_TC, PK_KERNEL_TC_SINGLE and PK_KERNEL_Q4 for other bf16 / fp16 calls.
+ *   - A key met for the first time with more than one usable kernel is tuned on the call's
+ *     own arguments: each kernel runs once untimed and three times between two events on
+ *     `stream`, the host waiting for the second event; the output is then that of one more
+ *     run of the winner. Such a first call synchronizes the stream and cannot be captured in
+ *     a CUDA graph (it returns PK_ERR_CAPTURE, nothing launched); later calls with the key
+ *     are asynchronous. The cache lives until pk_tune_clear() or the end of the process.
+ *   - Errors as pk_attend; longest < 0 gives PK_ERR_ARG.
+ */
+int pk_attend_tuned(int dtype, const void *qkv, const void *cos, const void *sin,
+                    const uint32_t *cu, int S, int64_t T, int H, int window, float scale,
+                    int64_t longest, void *out, float *lse, struct CUstream_st *stream);
+
+/* The kernel pk_attend_tuned keeps for a key on the current device (enum pk_kernel), or -1
+ * when the key has not been tuned. */
+int pk_tune_pick(int dtype, int H, int window, int64_t T, int64_t longest);
+
+/* The text of a tuning key, "dtype=bf16,heads=12,window=0,tokens=32768,longest=512", into
+ * buf (n bytes, NUL-terminated). PK_ERR_ARG when it does not fit or an argument is invalid.
+ * Needs no device. */
+int pk_tune_key(int dtype, int H, int window, int64_t T, int64_t longest, char *buf, int n);
+
+/* Forgets every tuned key. */
+int pk_tune_clear(void);
+
+/* The kernel pk_attend_dt runs for an element type and window (enum pk_kernel). Needs no
+ * device. */
+int pk_forward_kernel(int dtype, int window);
+
+/* Name of a forward kernel (static storage; "" for an unknown id). */
+const char *pk_kernel_name(int kernel);
+
+/*
  * The tile schedule alone (for inspection and tests). Runs the device scheduler on `cu`
  * (device pointer) and copies its records to `tiles` (device pointer, room for `cap`
  * records of 8 uint32 each: q0, rows, k0, nk, seq, nseq, kind, ktiles -- query tokens
@@ -137,9 +196,9 @@ int64_t pk_schedule_capacity(int64_t T);
 int pk_last_status(struct CUstream_st *stream);
 
 /*
- * Kernel timing. pk_profile_start(n) makes the next n attention calls on the current device
+ * Kernel timing. pk_profile_start(n) makes the next n forward calls on the current device
  * record a CUDA event pair on their stream around each of their two kernels (the tile
- * scheduler and the attention kernel). pk_profile_stop() synchronizes those events, writes
+ * scheduler, or for narrow windows the check of cu, and the attention kernel). pk_profile_stop() synchronizes those events, writes
  * the summed durations in milliseconds and the number of calls recorded, and stops the
  * recording. Returns PK_ERR_ARG for n < 1 or null outputs, PK_ERR_CUDA on event failures.
  */
@@ -154,7 +213,8 @@ int pk_profile_stop(double *schedule_ms, double *attend_ms, int *calls);
  * that plan every byte of device memory themselves (a serving process with a fixed budget,
  * a plugin whose enqueue step may not allocate, an application whose pool allocator owns
  * the device) or that cannot afford the synchronization a cudaMalloc brings use this call
- * instead: it allocates nothing, and runs the same kernels on a scratch area compiled into
+ * instead: it allocates nothing, and runs the kernels pk_attend_dt runs for the same
+ * arguments (pk_forward_kernel) on a scratch area compiled into
  * the library (a static __device__ array of about 4 MB, present on every GPU that loads
  * the library until the process exits).
  *   - dtype: enum pk_dtype; the other arguments as pk_attend.

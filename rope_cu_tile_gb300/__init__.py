@@ -5,7 +5,7 @@ Argument marshalling only: every step of the computation runs in the CUDA librar
 library is missing or cannot load, every call raises.
 
 The entry points mirror include/pk.h:
-    attend(qkv, cos, sin, cu, H, window, scale, out=None, lse=None, stream=None)
+    attend(qkv, cos, sin, cu, H, window, scale, out=None, lse=None, stream=None, tuned=False)
     pk_attend(qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream)   (raw pointers)
     schedule(cu, T, window)      -> tile records [NT, 8]
     last_status(stream=None)     -> int
@@ -31,7 +31,9 @@ NOALLOC_MAX_T = 1048576
 EXPORTS = ("pk_attend", "pk_attend_bf16", "pk_attend_f16", "pk_attend_f32", "pk_attend_dt",
            "pk_schedule", "pk_schedule_capacity", "pk_last_status", "pk_status_string",
            "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop", "pk_attend_noalloc", "pk_rope", "pk_attend_mixed",
-           "pk_attend_backward")
+           "pk_attend_backward", "pk_attend_tuned", "pk_tune_pick", "pk_tune_key", "pk_tune_clear",
+           "pk_forward_kernel", "pk_kernel_name")
+KERNELS = {0: "band", 1: "f32", 2: "tc", 3: "q4", 4: "tc_single"}
 
 _lib = None
 
@@ -65,6 +67,18 @@ def load(path: str | None = None):
     L.pk_attend_backward.restype = i32
     L.pk_attend_mixed.argtypes = [i32] + sig
     L.pk_attend_mixed.restype = i32
+    L.pk_attend_tuned.argtypes = [i32, vp, vp, vp, vp, i32, i64, i32, i32, f32, i64, vp, vp, vp]
+    L.pk_attend_tuned.restype = i32
+    L.pk_tune_pick.argtypes = [i32, i32, i32, i64, i64]
+    L.pk_tune_pick.restype = i32
+    L.pk_tune_key.argtypes = [i32, i32, i32, i64, i64, ctypes.c_char_p, i32]
+    L.pk_tune_key.restype = i32
+    L.pk_tune_clear.argtypes = []
+    L.pk_tune_clear.restype = i32
+    L.pk_forward_kernel.argtypes = [i32, i32]
+    L.pk_forward_kernel.restype = i32
+    L.pk_kernel_name.argtypes = [i32]
+    L.pk_kernel_name.restype = ctypes.c_char_p
     L.pk_rope.argtypes = [i32, vp, vp, vp, vp, i64, vp, i32, i64, i32, i32, i32, i32, vp, vp]
     L.pk_rope.restype = i32
     L.pk_schedule.argtypes = [vp, i32, i64, i32, vp, i64, ctypes.POINTER(i64), vp]
@@ -113,6 +127,34 @@ def pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse
     """The allocation-free variant (see include/pk.h): for callers that cannot let the library
     cudaMalloc a workspace; `status` is an optional device pointer to one int."""
     return load().pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, status, stream)
+
+
+def pk_attend_tuned(dtype, qkv, cos, sin, cu, S, T, H, window, scale, longest, out, lse, stream) -> int:
+    """The forward pass at the fastest usable kernel for the shape, tuned once per key (see
+    include/pk.h)."""
+    return load().pk_attend_tuned(dtype, qkv, cos, sin, cu, S, T, H, window, scale, longest, out, lse, stream)
+
+
+def pk_tune_pick(dtype, H, window, T, longest) -> int:
+    return load().pk_tune_pick(dtype, H, window, T, longest)
+
+
+def pk_tune_key(dtype, H, window, T, longest) -> str:
+    buf = ctypes.create_string_buffer(128)
+    _check(load().pk_tune_key(dtype, H, window, T, longest, buf, 128), "pk_tune_key")
+    return buf.value.decode()
+
+
+def pk_tune_clear() -> int:
+    return load().pk_tune_clear()
+
+
+def pk_forward_kernel(dtype, window) -> int:
+    return load().pk_forward_kernel(dtype, window)
+
+
+def pk_kernel_name(kernel) -> str:
+    return load().pk_kernel_name(kernel).decode()
 
 
 def pk_attend_backward(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, dout, dqkv, stream) -> int:
@@ -222,21 +264,33 @@ def _stream_handle(stream):
 
 
 def attend(qkv, cos, sin, cu, H: int, window: int, scale: float, out=None, lse=None, stream=None,
-           out_dtype=None, max_len=None):
+           out_dtype=None, max_len=None, tuned=False):
     """out [T, H*64] (qkv's dtype) and lse [H, T] float32 for device tensors qkv [T, 3*H*64],
     cos/sin [P, 32] (qkv's dtype) and cu [S+1] (int32 or uint32), all on one device. For
     float32 inputs, out_dtype=torch.float16 or torch.bfloat16 gives a 16-bit out
     (pk_attend_mixed). max_len: the longest sequence's length, if the caller knows it
-    (otherwise it is read back from cu to check that the tables are long enough)."""
+    (otherwise it is read back from cu to check that the tables are long enough).
+    tuned=True: pk_attend_tuned (the fastest usable kernel for the shape, tuned on the
+    first call of each key; that call synchronizes the stream)."""
     torch = _torch()
     _check_inputs(qkv, cos, sin, cu, H, 32)
     _check_stream(stream, qkv.device)
     with torch.cuda.device(qkv.device):
+        if tuned and max_len is None:
+            max_len = _longest(cu)
         _check_table_rows(cu, cos.shape[0], max_len)
-        return _attend(qkv, cos, sin, cu, H, window, scale, out, lse, stream, out_dtype)
+        return _attend(qkv, cos, sin, cu, H, window, scale, out, lse, stream, out_dtype,
+                       max_len if tuned else None)
 
 
-def _attend(qkv, cos, sin, cu, H, window, scale, out, lse, stream, out_dtype):
+def _longest(cu) -> int:
+    torch = _torch()
+    if cu.shape[0] < 2:
+        return 0
+    return int((cu[1:].to(torch.int64) - cu[:-1].to(torch.int64)).max().item())
+
+
+def _attend(qkv, cos, sin, cu, H, window, scale, out, lse, stream, out_dtype, tuned_longest=None):
     torch = _torch()
     T = qkv.shape[0]
     S = cu.shape[0] - 1
@@ -253,7 +307,13 @@ def _attend(qkv, cos, sin, cu, H, window, scale, out, lse, stream, out_dtype):
     else:
         _need(lse, (H, T), torch.float32, "lse")
     _same_device(qkv, out, lse)
-    if odt != qkv.dtype:
+    if tuned_longest is not None and odt != qkv.dtype:
+        raise TypeError("the tuned entry point writes out in qkv's type")
+    if tuned_longest is not None:
+        rc = pk_attend_tuned(dtype_code(qkv), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(),
+                             S, T, H, window, float(scale), int(tuned_longest), out.data_ptr(), lse.data_ptr(),
+                             _stream_handle(stream))
+    elif odt != qkv.dtype:
         rc = pk_attend_mixed(dtype_code(out), qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(),
                              S, T, H, window, float(scale), out.data_ptr(), lse.data_ptr(), _stream_handle(stream))
     else:

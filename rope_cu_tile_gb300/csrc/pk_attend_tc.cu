@@ -7,7 +7,7 @@
 // masked keys weighing exactly zero, then out = O / l and lse = m + ln l.
 //
 // How (GB300): one persistent 512-thread CTA per SM. A work item is a PAIR of consecutive
-// tile records (A, B) of one head. When both are pieces of the same sequence they share
+// tile records (A, B) of one head (or, in the single-record mode, one record alone). When both are pieces of the same sequence they share
 // one key stream -- key tiles of 128 tokens from A's first key to the last key either can
 // see -- so every K / V tile is loaded and rotated once for two query tiles; otherwise B's
 // key tiles follow A's in the stream. A uses stream tiles [0, a1), B uses [b0, b1).
@@ -234,6 +234,7 @@ struct Params {
   float s_mul;  // multiplies the scores in the softmax (the scale when it is positive, else 1)
   unsigned long long timeout_ns;
   int skip_first_item_arrive;  // test hook: the producer withholds its first item hand-off
+  int singles;                 // 1: a work item is one tile record (no B), 0: a pair of records
 };
 
 // The member sequence offsets cu[rec.seq .. rec.seq + rec.nseq] of a record, copied by the
@@ -386,8 +387,9 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, uint8_t* smem
     }
     const unsigned int pair = item / static_cast<unsigned int>(p.H);
     const int h = static_cast<int>(item % static_cast<unsigned int>(p.H));
-    const TileRec ra = p.tiles[2 * pair];
-    const bool has_b = 2 * pair + 1 < ntiles;
+    const unsigned int first_rec = p.singles ? pair : 2 * pair;
+    const TileRec ra = p.tiles[first_rec];
+    const bool has_b = !p.singles && 2 * pair + 1 < ntiles;
     TileRec rb = ra;
     if (has_b) rb = p.tiles[2 * pair + 1];
     const bool shared = has_b && ra.kind == 0 && rb.kind == 0 && ra.seq == rb.seq;
@@ -1002,7 +1004,8 @@ pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_c
       if (lane == 0) {
         // the records and the work counter come from the scheduler launched just before
         griddep_wait();
-        producer(&tmap_qkv, p, smem, meta, (__ldcg(&p.ctl->ntiles) + 1u) / 2u * static_cast<unsigned int>(p.H));
+        const unsigned int nt = __ldcg(&p.ctl->ntiles);
+        producer(&tmap_qkv, p, smem, meta, (p.singles ? nt : (nt + 1u) / 2u) * static_cast<unsigned int>(p.H));
       }
     } else if (warp == kWarpMma || warp == kWarpMma + 1) {
       if (lane == 0) mma_issuer(p, smem, meta, meta->tmem, BF16, warp - kWarpMma);
@@ -1045,7 +1048,7 @@ cudaError_t attend_tc_prepare() {
 cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
                              const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
                              long long T, int window, float scale, unsigned long long timeout_ns, int grid,
-                             cudaStream_t stream) {
+                             bool singles, cudaStream_t stream) {
   Params p;
   p.cos_t = static_cast<const uint16_t*>(cos_t);
   p.sin_t = static_cast<const uint16_t*>(sin_t);
@@ -1062,6 +1065,7 @@ cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos
   p.q_mul = scale > 0.0f ? 1.0f : scale;
   p.s_mul = scale > 0.0f ? scale : 1.0f;
   p.timeout_ns = timeout_ns;
+  p.singles = singles ? 1 : 0;
   // test hook for the bounded waits (PK_DEBUG_SKIP_ARRIVE=1): every CTA's producer withholds
   // its first work-item hand-off, so the consumers' waits run out and the call ends with
   // PK_ERR_TIMEOUT in the stream's status word; nothing faults and the context stays usable

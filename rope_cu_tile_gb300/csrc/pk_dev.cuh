@@ -58,6 +58,22 @@ struct Ctl {
 };
 static_assert(sizeof(Ctl) == 32, "control block is 32 bytes");
 
+// The forward kernels (host-side dispatch: select_forward_kernel, forward_launch in pk_host.cu).
+constexpr int kKernelBand = 0;  // narrow windows, CUDA cores, fp32
+constexpr int kKernelF32 = 1;   // fp32 inputs, CUDA cores
+constexpr int kKernelTc = 2;    // 16-bit inputs, paired-stream tensor-core kernel
+constexpr int kKernelQ4 = 3;    // 16-bit inputs, four-chain tensor-core kernel
+constexpr int kKernelTcSingle = 4;  // 16-bit inputs, paired-stream kernel with one record per item
+int select_forward_kernel(int dtype, int window);
+// The launches of one forward call on caller-provided scratch (control block, `cap` tile
+// records, the scheduler's staging slots); `ev`, when not null, gets three events recorded
+// (before the first launch, between the preparation and the attention kernel, after it).
+// Returns a pk_status code.
+int forward_launch(int kernel, int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin,
+                   const uint32_t* cu, int S, long long T, int H, int window, float scale, void* out, float* lse,
+                   Ctl* ctl, TileRec* tiles, long long cap, TileRec* stage, int sms, unsigned long long timeout_ns,
+                   cudaStream_t stream, cudaEvent_t* ev);
+
 // status codes (mirror enum pk_status)
 constexpr int kErrBadCu = 5;
 constexpr int kErrTimeout = 6;
@@ -252,6 +268,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
       "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+// 16 consecutive 32-bit columns of this thread's TMEM lane <- r
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
+      " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -28,7 +29,18 @@ cudaError_t backward_launch(int dtype, const void* qkv, const void* cos_t, const
 cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
                              const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
                              long long T, int window, float scale, unsigned long long timeout_ns, int grid,
+                             bool singles, cudaStream_t stream);
+cudaError_t attend_q4_prepare();
+cudaError_t attend_q4_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
+                             const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
+                             long long T, int window, float scale, unsigned long long timeout_ns, int grid,
                              cudaStream_t stream);
+cudaError_t band_prepare();
+long long band_first_words(long long T);
+cudaError_t band_prep_launch(const uint32_t* cu, int S, long long T, uint32_t* first, Ctl* ctl, cudaStream_t stream);
+cudaError_t band_launch(int dtype, int out_dtype, const void* qkv, const void* cos_t, const void* sin_t,
+                        const uint32_t* cu, int S, uint32_t* first, void* out, float* lse, Ctl* ctl, int H, long long T,
+                        int window, float scale, cudaStream_t stream);
 cudaError_t attend_f32_launch(const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu,
                               const TileRec* tiles, void* out, int out_dtype, float* lse, Ctl* ctl, int H,
                               long long T, int window, float scale, int grid, cudaStream_t stream);
@@ -66,6 +78,24 @@ struct Profile {
 
 std::mutex g_mu;
 Profile g_prof;
+
+// Tile autotuning (hanzo-kernel packed.rs fn attend_tuned): the fastest usable kernel for a
+// (device, element type, heads, window, tokens, longest sequence) key, timed once and kept.
+// Like the pages' key, the window enters as w + 1 (0: every key) and the token count and the
+// longest length as their next powers of two.
+struct TuneKey {
+  int dev, dtype, heads, window1;
+  long long tokens, longest;
+  bool operator<(const TuneKey& o) const {
+    if (dev != o.dev) return dev < o.dev;
+    if (dtype != o.dtype) return dtype < o.dtype;
+    if (heads != o.heads) return heads < o.heads;
+    if (window1 != o.window1) return window1 < o.window1;
+    if (tokens != o.tokens) return tokens < o.tokens;
+    return longest < o.longest;
+  }
+};
+std::map<TuneKey, int> g_tune;
 std::map<std::pair<int, cudaStream_t>, Workspace> g_ws;
 std::map<int, DeviceInfo> g_dev;
 
@@ -98,6 +128,33 @@ unsigned long long timeout_ns() {
   return t;
 }
 
+// The forward kernels a call can run:
+//   kBand  narrow windows (1 <= w <= kBandMaxW), any element type: CUDA cores, fp32 (no tile
+//          records: a check of cu replaces the scheduler);
+//   kF32   fp32 inputs otherwise: CUDA cores, fp32;
+//   kTc    16-bit inputs: the paired-stream tensor-core kernel (two query tiles in flight per
+//          SM, 128-key stream tiles);
+//   kQ4    16-bit inputs: the four-chain tensor-core kernel (two pipes of two query tiles,
+//          64-key stream tiles).
+// PK_ATTN=tc, q4 or tc_single picks the tensor-core kernel for 16-bit inputs.
+constexpr int kBandMaxW = 16;
+int tensor_kernel_choice() {
+  const char* e = std::getenv("PK_ATTN");
+  if (e && std::strcmp(e, "q4") == 0) return kKernelQ4;
+  if (e && std::strcmp(e, "tc_single") == 0) return kKernelTcSingle;
+  return kKernelTc;
+}
+
+}  // namespace
+
+int select_forward_kernel(int dtype, int window) {
+  if (window >= 1 && window <= kBandMaxW) return kKernelBand;
+  if (dtype == PK_F32) return kKernelF32;
+  return tensor_kernel_choice();
+}
+
+namespace {
+
 // device checks (caller holds g_mu)
 int device_info(int dev, DeviceInfo** out) {
   DeviceInfo& di = g_dev[dev];
@@ -110,7 +167,8 @@ int device_info(int dev, DeviceInfo** out) {
   }
   if (!di.supported) return PK_ERR_UNSUPPORTED;
   if (!di.attrs_set) {
-    if (attend_tc_prepare() != cudaSuccess || schedule_prepare() != cudaSuccess || backward_prepare() != cudaSuccess)
+    if (attend_tc_prepare() != cudaSuccess || attend_q4_prepare() != cudaSuccess || band_prepare() != cudaSuccess ||
+        schedule_prepare() != cudaSuccess || backward_prepare() != cudaSuccess)
       return PK_ERR_CUDA;
     di.attrs_set = true;
   }
@@ -189,10 +247,6 @@ int launch_schedule(const uint32_t* cu, int S, int64_t T, int window, Workspace*
              : PK_ERR_CUDA;
 }
 
-int launch_attend(int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu,
-                  int64_t T, int H, int window, float scale, void* out, float* lse, Workspace* ws, DeviceInfo* di,
-                  cudaStream_t stream);
-
 // out_dtype: the output's type (the input type, except for fp32 inputs with a 16-bit output)
 int attend(int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S,
            int64_t T, int H, int window, float scale, void* out, float* lse, cudaStream_t stream) {
@@ -207,42 +261,103 @@ int attend(int dtype, int out_dtype, const void* qkv, const void* cos, const voi
   if ((rc = workspace(dev, stream, T, &ws)) != PK_OK) return rc;
   cudaEvent_t* ev = nullptr;
   if (g_prof.on && g_prof.dev == dev && g_prof.used < g_prof.cap) ev = g_prof.ev + 3 * g_prof.used++;
-  if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return PK_ERR_CUDA;
-  if ((rc = launch_schedule(cu, S, T, window, ws, stream)) != PK_OK) return rc;
-  if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return PK_ERR_CUDA;
-  rc = launch_attend(dtype, out_dtype, qkv, cos, sin, cu, T, H, window, scale, out, lse, ws, di, stream);
-  if (rc == PK_OK && ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return PK_ERR_CUDA;
-  return rc;
+  return forward_launch(select_forward_kernel(dtype, window), dtype, out_dtype, qkv, cos, sin, cu, S,
+                        static_cast<long long>(T), H, window, scale, out, lse, ws->ctl, ws->tiles, ws->cap, ws->stage,
+                        di->sms, timeout_ns(), stream, ev);
 }
 
-int launch_attend(int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu,
-                  int64_t T, int H, int window, float scale, void* out, float* lse, Workspace* ws, DeviceInfo* di,
-                  cudaStream_t stream) {
-  if (dtype == PK_F32) {
-    return attend_f32_launch(static_cast<const float*>(qkv), static_cast<const float*>(cos),
-                             static_cast<const float*>(sin), cu, ws->tiles, out, out_dtype, lse, ws->ctl, H,
-                             static_cast<long long>(T), window, scale, di->sms * 4, stream) == cudaSuccess
-               ? PK_OK
-               : PK_ERR_CUDA;
-  }
+long long next_pow2(long long x) {
+  long long p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
 
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return PK_ERR_CUDA;
-  CUtensorMap tmap;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(3) * H * kD, static_cast<cuuint64_t>(T)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(3) * H * kD * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBR)};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt =
-      dtype == PK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if (enc(&tmap, dt, 2, const_cast<void*>(qkv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return PK_ERR_CUDA;
-  return attend_tc_launch(dtype == PK_BF16, tmap, cos, sin, cu, ws->tiles, out, lse, ws->ctl, H,
-                          static_cast<long long>(T), window, scale, timeout_ns(), di->sms, stream) == cudaSuccess
-             ? PK_OK
-             : PK_ERR_CUDA;
+TuneKey tune_key(int dev, int dtype, int H, int window, long long T, long long longest) {
+  return TuneKey{dev, dtype, H, window > 0 ? window + 1 : 0, next_pow2(T), next_pow2(longest)};
+}
+
+// The kernels a call may run, fastest first unknown: narrow windows keep to the band kernel
+// (fp32 arithmetic: the tensor-core kernels round q' and k' to the element type, which costs
+// fp16 inputs of large magnitude their tolerance), fp32 inputs to the CUDA-core kernels.
+int tune_candidates(int dtype, int window, int* c) {
+  if (window >= 1 && window <= kBandMaxW) {
+    c[0] = kKernelBand;
+    return 1;
+  }
+  if (dtype == PK_F32) {
+    c[0] = kKernelF32;
+    return 1;
+  }
+  c[0] = kKernelTc;
+  c[1] = kKernelTcSingle;
+  c[2] = kKernelQ4;
+  return 3;
+}
+
+constexpr int kTuneReps = 3;  // timed launches per candidate (after one untimed)
+
+int attend_tuned(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T,
+                 int H, int window, float scale, int64_t longest, void* out, float* lse, cudaStream_t stream) {
+  int rc = check_args(dtype, qkv, cos, sin, cu, S, T, H, window, out, lse);
+  if (rc != PK_OK || T == 0) return rc;
+  if (longest < 0) return PK_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PK_ERR_CUDA;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(dev, &di)) != PK_OK) return rc;
+  Workspace* ws = nullptr;
+  if ((rc = workspace(dev, stream, T, &ws)) != PK_OK) return rc;
+  auto run = [&](int kernel, cudaEvent_t* ev) {
+    return forward_launch(kernel, dtype, dtype, qkv, cos, sin, cu, S, static_cast<long long>(T), H, window, scale, out,
+                          lse, ws->ctl, ws->tiles, ws->cap, ws->stage, di->sms, timeout_ns(), stream, ev);
+  };
+  const TuneKey key = tune_key(dev, dtype, H, window, T, longest);
+  auto it = g_tune.find(key);
+  int kernel;
+  if (it != g_tune.end()) {
+    kernel = it->second;
+  } else {
+    int cand[3];
+    const int n = tune_candidates(dtype, window, cand);
+    kernel = cand[0];
+    if (n > 1) {
+      // timing needs the host to wait for the stream: not while it is being captured
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return PK_ERR_CUDA;
+      }
+      if (cs != cudaStreamCaptureStatusNone) return PK_ERR_CAPTURE;
+      cudaEvent_t e0, e1;
+      if (cudaEventCreate(&e0) != cudaSuccess) return PK_ERR_CUDA;
+      if (cudaEventCreate(&e1) != cudaSuccess) {
+        cudaEventDestroy(e0);
+        return PK_ERR_CUDA;
+      }
+      float best = 0.f;
+      for (int i = 0; i < n && rc == PK_OK; ++i) {
+        rc = run(cand[i], nullptr);
+        if (rc == PK_OK && cudaEventRecord(e0, stream) != cudaSuccess) rc = PK_ERR_CUDA;
+        for (int r = 0; r < kTuneReps && rc == PK_OK; ++r) rc = run(cand[i], nullptr);
+        float ms = 0.f;
+        if (rc == PK_OK && (cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                            cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess))
+          rc = PK_ERR_CUDA;
+        if (rc == PK_OK && (i == 0 || ms < best)) {
+          best = ms;
+          kernel = cand[i];
+        }
+      }
+      cudaEventDestroy(e0);
+      cudaEventDestroy(e1);
+      if (rc != PK_OK) return rc;
+    }
+    g_tune[key] = kernel;
+  }
+  cudaEvent_t* ev = nullptr;
+  if (g_prof.on && g_prof.dev == dev && g_prof.used < g_prof.cap) ev = g_prof.ev + 3 * g_prof.used++;
+  return run(kernel, ev);
 }
 
 // the backward scratch of a workspace, grown to `floats` (caller holds g_mu)
@@ -294,6 +409,57 @@ int attend_backward(int dtype, const void* qkv, const void* cos, const void* sin
 }
 
 }  // namespace
+
+int forward_launch(int kernel, int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin,
+                   const uint32_t* cu, int S, long long T, int H, int window, float scale, void* out, float* lse,
+                   Ctl* ctl, TileRec* tiles, long long cap, TileRec* stage, int sms, unsigned long long timeout,
+                   cudaStream_t stream, cudaEvent_t* ev) {
+  if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return PK_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (kernel == kKernelBand) {
+    // the band kernel needs no tile records: its block-to-sequence table goes where they would
+    if (band_first_words(T) * 4 > cap * static_cast<long long>(sizeof(TileRec))) return PK_ERR_INTERNAL;
+    uint32_t* first = reinterpret_cast<uint32_t*>(tiles);
+    if (band_prep_launch(cu, S, T, first, ctl, stream) != cudaSuccess) return PK_ERR_CUDA;
+    if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return PK_ERR_CUDA;
+    e = band_launch(dtype, out_dtype, qkv, cos, sin, cu, S, first, out, lse, ctl, H, T, window, scale, stream);
+    if (e != cudaSuccess) return PK_ERR_CUDA;
+    if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return PK_ERR_CUDA;
+    return PK_OK;
+  }
+  if (schedule_launch(cu, S, T, window, tiles, cap, stage, ctl, stream) != cudaSuccess) return PK_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return PK_ERR_CUDA;
+  if (kernel == kKernelF32) {
+    e = attend_f32_launch(static_cast<const float*>(qkv), static_cast<const float*>(cos),
+                          static_cast<const float*>(sin), cu, tiles, out, out_dtype, lse, ctl, H, T, window, scale,
+                          sms * 4, stream);
+  } else {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PK_ERR_CUDA;
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(3) * H * kD, static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(3) * H * kD * 2};
+    // box: one 128-row query tile (paired kernel) or one 64-row tile (four-chain kernel)
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kernel == kKernelQ4 ? 64 : kBR)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt =
+        dtype == PK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (enc(&tmap, dt, 2, const_cast<void*>(qkv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PK_ERR_CUDA;
+    if (kernel == kKernelQ4)
+      e = attend_q4_launch(dtype == PK_BF16, tmap, cos, sin, cu, tiles, out, lse, ctl, H, T, window, scale, timeout,
+                           sms, stream);
+    else
+      e = attend_tc_launch(dtype == PK_BF16, tmap, cos, sin, cu, tiles, out, lse, ctl, H, T, window, scale, timeout,
+                           sms, kernel == kKernelTcSingle, stream);
+  }
+  if (e != cudaSuccess) return PK_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return PK_ERR_CUDA;
+  return PK_OK;
+}
+
 }  // namespace pk
 
 using namespace pk;
@@ -336,6 +502,47 @@ int pk_attend_f32(const void* qkv, const void* cos, const void* sin, const uint3
                   int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
   return attend(PK_F32, PK_F32, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
 }
+
+int pk_attend_tuned(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S, int64_t T,
+                    int H, int window, float scale, int64_t longest, void* out, float* lse, struct CUstream_st* stream) {
+  return attend_tuned(dtype, qkv, cos, sin, cu, S, T, H, window, scale, longest, out, lse, stream);
+}
+
+int pk_tune_pick(int dtype, int H, int window, int64_t T, int64_t longest) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  auto it = g_tune.find(tune_key(dev, dtype, H, window, T, longest));
+  return it == g_tune.end() ? -1 : it->second;
+}
+
+int pk_tune_key(int dtype, int H, int window, int64_t T, int64_t longest, char* buf, int n) {
+  if (!buf || n < 1 || T < 0 || longest < 0 || window < 0 || H < 1) return PK_ERR_ARG;
+  const TuneKey k = tune_key(0, dtype, H, window, T, longest);
+  const char* dt = dtype == PK_F32 ? "f32" : dtype == PK_BF16 ? "bf16" : dtype == PK_F16 ? "f16" : "?";
+  const int w = std::snprintf(buf, static_cast<size_t>(n), "dtype=%s,heads=%d,window=%d,tokens=%lld,longest=%lld", dt,
+                              k.heads, k.window1, k.tokens, k.longest);
+  return (w < 0 || w >= n) ? PK_ERR_ARG : PK_OK;
+}
+
+int pk_tune_clear(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_tune.clear();
+  return PK_OK;
+}
+
+const char* pk_kernel_name(int kernel) {
+  switch (kernel) {
+    case kKernelBand: return "pk_attend_band_kernel";
+    case kKernelF32: return "pk_attend_f32_kernel";
+    case kKernelTc: return "pk_attend_tc_kernel";
+    case kKernelQ4: return "pk_attend_q4_kernel";
+    case kKernelTcSingle: return "pk_attend_tc_kernel (single-record items)";
+    default: return "";
+  }
+}
+
+int pk_forward_kernel(int dtype, int window) { return select_forward_kernel(dtype, window); }
 
 int64_t pk_schedule_capacity(int64_t T) { return T < 0 ? 0 : schedule_capacity(T); }
 
@@ -482,3 +689,7 @@ int pk_release(void) {
 }
 
 }  // extern "C"
+
+static_assert(pk::kKernelBand == PK_KERNEL_BAND && pk::kKernelF32 == PK_KERNEL_F32 && pk::kKernelTc == PK_KERNEL_TC &&
+                  pk::kKernelQ4 == PK_KERNEL_Q4 && pk::kKernelTcSingle == PK_KERNEL_TC_SINGLE,
+              "kernel ids match enum pk_kernel");

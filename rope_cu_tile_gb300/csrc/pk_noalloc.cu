@@ -28,17 +28,10 @@
 
 namespace pk {
 
-cudaError_t schedule_launch(const uint32_t* cu, int S, long long T, int window, TileRec* tiles, long long cap,
-                            TileRec* stage, Ctl* ctl, cudaStream_t stream);
 cudaError_t attend_tc_prepare();
+cudaError_t attend_q4_prepare();
+cudaError_t band_prepare();
 cudaError_t schedule_prepare();
-cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
-                             const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
-                             long long T, int window, float scale, unsigned long long timeout_ns, int grid,
-                             cudaStream_t stream);
-cudaError_t attend_f32_launch(const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu,
-                              const TileRec* tiles, void* out, int out_dtype, float* lse, Ctl* ctl, int H,
-                              long long T, int window, float scale, int grid, cudaStream_t stream);
 
 namespace {
 
@@ -63,10 +56,6 @@ struct Setup {
 std::mutex g_noalloc_mu;
 Setup g_noalloc_setup[kMaxDevices];
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 // once per device, with that device current
 int setup_device(int dev, Setup** out) {
   if (dev < 0 || dev >= kMaxDevices) return PK_ERR_UNSUPPORTED;
@@ -77,7 +66,9 @@ int setup_device(int dev, Setup** out) {
     s.supported = prop.major == 10 && prop.minor == 3;
     s.sms = prop.multiProcessorCount;
     if (s.supported) {
-      if (attend_tc_prepare() != cudaSuccess || schedule_prepare() != cudaSuccess) return PK_ERR_CUDA;
+      if (attend_tc_prepare() != cudaSuccess || attend_q4_prepare() != cudaSuccess || band_prepare() != cudaSuccess ||
+          schedule_prepare() != cudaSuccess)
+        return PK_ERR_CUDA;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PK_ERR_CUDA;
       s.scratch = static_cast<unsigned char*>(p);
@@ -87,19 +78,6 @@ int setup_device(int dev, Setup** out) {
   if (!s.supported) return PK_ERR_UNSUPPORTED;
   *out = &s;
   return PK_OK;
-}
-
-EncodeTiledFn noalloc_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
 }
 
 unsigned long long noalloc_timeout_ns() {
@@ -143,31 +121,11 @@ extern "C" int pk_attend_noalloc(int dtype, const void* qkv, const void* cos, co
 
   // the control block starts each call at zero (the last call's counter and status stay in it)
   if (cudaMemsetAsync(ctl, 0, sizeof(Ctl), st) != cudaSuccess) return PK_ERR_CUDA;
-  if (schedule_launch(cu, S, static_cast<long long>(T), window, tiles, kNoallocCap, stage, ctl, st) != cudaSuccess)
-    return PK_ERR_CUDA;
-  cudaError_t e;
-  if (dtype == PK_F32) {
-    e = attend_f32_launch(static_cast<const float*>(qkv), static_cast<const float*>(cos),
-                          static_cast<const float*>(sin), cu, tiles, out, PK_F32, lse, ctl, H,
-                          static_cast<long long>(T), window, scale, s->sms * 4, st);
-  } else {
-    EncodeTiledFn enc = noalloc_encode_fn();
-    if (!enc) return PK_ERR_CUDA;
-    CUtensorMap tmap;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(3) * H * kD, static_cast<cuuint64_t>(T)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(3) * H * kD * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBR)};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dt =
-        dtype == PK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (enc(&tmap, dt, 2, const_cast<void*>(qkv), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return PK_ERR_CUDA;
-    e = attend_tc_launch(dtype == PK_BF16, tmap, cos, sin, cu, tiles, out, lse, ctl, H, static_cast<long long>(T),
-                         window, scale, noalloc_timeout_ns(), s->sms, st);
-  }
-  if (e != cudaSuccess) return PK_ERR_CUDA;
+  // the same kernels as pk_attend would run for these arguments
+  rc = forward_launch(select_forward_kernel(dtype, window), dtype, dtype, qkv, cos, sin, cu, S,
+                      static_cast<long long>(T), H, window, scale, out, lse, ctl, tiles, kNoallocCap, stage, s->sms,
+                      noalloc_timeout_ns(), st, nullptr);
+  if (rc != PK_OK) return rc;
   if (status && cudaMemcpyAsync(status, &ctl->status, sizeof(int), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return PK_ERR_CUDA;
   return PK_OK;
