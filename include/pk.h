@@ -244,9 +244,10 @@ int pk_attend_noalloc(int dtype, const void *qkv, const void *cos, const void *s
  *   - out [T, H*64] (dtype) and lse [H, T] (fp32): the forward's outputs.
  *   - dout [T, H*64] (dtype): the gradient of the loss with respect to out.
  *   - dqkv [T, 3*H*64] (dtype): written with the gradients of q | k | v.
- *   - bf16 / fp16: tensor-core products with q', k', P and dS rounded to dtype as operands and
- *     fp32 accumulation; fp32: fp32 arithmetic on the CUDA cores. One rounding of dqkv to
- *     dtype.
+ *   - bf16 / fp16: tensor-core products (tcgen05, accumulators in tensor memory; with
+ *     PK_BWD_MMA_SYNC=1 in the environment the warp-level mma.sync kernel instead) with q',
+ *     k', P and dS rounded to dtype as operands and fp32 accumulation; fp32: fp32 arithmetic
+ *     on the CUDA cores. One rounding of dqkv to dtype.
  *   - Allocates, on first use per (device, stream) and when a larger H*T arrives, an fp32
  *     scratch of about H*T*(1 + 3*64) floats (kept with the workspace, freed by pk_release).
  *     The capture rule of the workspace applies to it: a captured call that would have to

@@ -1,6 +1,6 @@
 // pk_backward.cu -- the backward pass of packed RoPE attention (pk_attend_backward in
-// include/pk.h): 16-bit inputs on the tensor cores (mma.sync, fp32 accumulation), fp32 inputs on
-// the CUDA cores.
+// include/pk.h): 16-bit inputs on the tensor cores (the tcgen05 kernel of pk_backward_tc.cu;
+// the warp-level mma.sync kernel below when PK_BWD_MMA_SYNC=1), fp32 inputs on the CUDA cores.
 //
 // The pages' attend_back (hanzo-kernel packed.rs) computes, per query row i and visible key j of
 // its sequence, with q'_i = rot(q_i, i), k'_j = rot(k_j, j), s_ij = scale q'_i . k'_j and the
@@ -10,7 +10,8 @@
 //
 // Three kernels over the forward's tile records (the same device schedule):
 //   prep    D [H, T] = rowsum(dout * out), fp32
-//   main    for 16-bit inputs pk_bwd_mma_kernel (below); for fp32 inputs pk_bwd_main_kernel:
+//   main    for 16-bit inputs pk_bwd_tc_kernel (pk_backward_tc.cu), or pk_bwd_mma_kernel
+//           (below); for fp32 inputs pk_bwd_main_kernel:
 //           per work item (tile record, head), persistent CTAs of 128 threads (two per SM),
 //           thread r <-> query row r (dout in registers, q' and dout in shared memory). Keys go
 //           through shared memory 16 at a time (rotated once); each thread forms its row's P and
@@ -23,10 +24,18 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstdlib>
+
 #include "pk.h"
 #include "pk_dev.cuh"
 
 namespace pk {
+
+cudaError_t backward_tc_prepare();
+cudaError_t backward_tc_launch(bool bf16, const void* qkv, const void* cos_t, const void* sin_t, const uint32_t* cu,
+                               long long T, int H, int window, float scale, const float* lse, const void* dout,
+                               const float* D, float* dq, void* dqkv, const TileRec* tiles, Ctl* ctl, int sms,
+                               cudaStream_t stream);
 
 namespace {
 
@@ -718,9 +727,16 @@ cudaError_t launch_backward_t(const void* qkv, const void* cos_t, const void* si
   if (e != cudaSuccess) return e;
   const long long prep_blocks = min(static_cast<long long>(sms) * 8, (T * H + 31) / 32);
   pk_bwd_prep_kernel<DT><<<static_cast<unsigned int>(max(prep_blocks, 1ll)), 256, 0, stream>>>(out, dout, D, H, T);
-  if constexpr (kMma)
-    pk_bwd_mma_kernel<DT><<<sms * 2, kMmaThreads, kMmaSmem, stream>>>(qkv, cos_t, sin_t, cu, tiles, ctl, lse, dout, D,
-                                                                       dq, dqkv, H, T, window, scale);
+  if constexpr (kMma) {
+    // the tcgen05 kernel, or the mma.sync one for comparison (PK_BWD_MMA_SYNC=1)
+    const char* legacy = std::getenv("PK_BWD_MMA_SYNC");
+    if (legacy && legacy[0] == '1')
+      pk_bwd_mma_kernel<DT><<<sms * 2, kMmaThreads, kMmaSmem, stream>>>(qkv, cos_t, sin_t, cu, tiles, ctl, lse, dout,
+                                                                         D, dq, dqkv, H, T, window, scale);
+    else if ((e = backward_tc_launch(DT == PK_BF16, qkv, cos_t, sin_t, cu, T, H, window, scale, lse, dout, D, dq, dqkv,
+                                     tiles, ctl, sms, stream)) != cudaSuccess)
+      return e;
+  }
   else
     pk_bwd_main_kernel<DT><<<sms * 2, kBwdThreads, kBwdSmem, stream>>>(qkv, cos_t, sin_t, cu, tiles, ctl, lse, dout, D,
                                                                         dq, dk, dv, H, T, window, scale);
@@ -743,6 +759,7 @@ cudaError_t backward_prepare() {
     e = cudaFuncSetAttribute(pk_bwd_mma_kernel<PK_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(pk_bwd_mma_kernel<PK_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+  if (e == cudaSuccess) e = backward_tc_prepare();
   return e;
 }
 

@@ -1,0 +1,511 @@
+// pk_backward_tc.cu -- the backward pass's main kernel on the tensor cores (tcgen05), bf16 / fp16.
+//
+// The gradient of the packed RoPE attention (hanzo-kernel packed.rs, fn attend_back): per visible
+// (query a, key b) pair P = exp(scale q'_a . k'_b - lse_a), dS = P (dout_a . v_b - D_a), and
+// dv_b = sum_a P dout_a, dk'_b = scale sum_a dS q'_a, dq'_a = scale sum_b dS k'_b.
+//
+// Work: a tile record's rows are a tile of 128 keys (visibility is symmetric, so the record's
+// key range is exactly the queries that see those keys); one work item is (record, head), taken
+// from the scheduler's counter by persistent CTAs, one per SM. Per item the CTA rotates K' once
+// and walks the visible queries in chunks of 128:
+//   S^T = K' Q'^T and dP^T = V dout^T         (M = 128 keys, N = 128 queries, K = 64)  -> TMEM
+//   the row group (thread = key row) forms P^T and dS^T from both rows and writes them, and dS,
+//   to shared memory as 16-bit operands
+//   dV += P^T dout, dK' += dS^T Q'             (M = 128 keys, N = 64, K = 128 queries) -> TMEM
+//   dQ' = dS K'                                (M = 128 queries, N = 64, K = 128 keys)  -> TMEM
+// and the row group (thread = query row) adds scale dQ' to the fp32 dq accumulator. At the end of
+// the item dK' and dV are complete: dk = rot^T(scale dK') and dv are rounded once and written.
+//
+// Roles (256 threads): warp 0 lane 0 the TMA producer, warp 1 lane 0 the MMA issuer, warp 2 owns
+// the tensor memory (512 columns), warps 4-7 the row group (warp w reads TMEM lanes 32 (w - 4) ..).
+// Within an item the three roles step through the chunks in lockstep on mbarriers (each barrier
+// completes once per chunk and every waiter waits for every phase, so a parity test is never two
+// phases away from its barrier); items are separated by a CTA-wide barrier.
+//
+// Shared memory: K', V, Q', dout as 128 x 64 tiles, 128-byte swizzled as TMA lands them (row r
+// at 128 r, its 16-byte chunk c at (c ^ (r & 7)) 16); P^T, dS^T as [key][query] and dS as
+// [query][key], each two such tiles side by side (64 columns each). K-major operands advance 32
+// bytes per K step of 16 inside a tile; the MN-major ones (dout, Q', K' as the B side of the
+// products with N = 64) advance 2048 bytes (16 rows).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+
+#include "pk.h"
+#include "pk_dev.cuh"
+
+namespace pk {
+
+namespace {
+
+constexpr int kTcThreads = 256;
+constexpr int kRowWarp0 = 4;              // warps 4..7: the row group
+constexpr uint32_t kTile = 128u * 128u;   // 128 rows x 64 16-bit elements
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffV = kOffK + kTile;
+constexpr uint32_t kOffQ = kOffV + kTile;
+constexpr uint32_t kOffO = kOffQ + kTile;       // dout
+constexpr uint32_t kOffPt = kOffO + kTile;      // P^T  [key][query], two tiles
+constexpr uint32_t kOffSt = kOffPt + 2 * kTile; // dS^T [key][query], two tiles
+constexpr uint32_t kOffS = kOffSt + 2 * kTile;  // dS   [query][key], two tiles
+constexpr uint32_t kOffRow = kOffS + 2 * kTile; // per query of the chunk: lse log2(e), D
+struct TcBars {
+  uint64_t kv_full, kv_ready, q_full, q_ready, s_full, p_ready, c_done, drain;
+};
+constexpr uint32_t kOffBar = kOffRow + 2 * 128 * 4;
+constexpr uint32_t kTcSmemUsed = kOffBar + sizeof(TcBars) + 16;
+constexpr uint32_t kTcSmem = kTcSmemUsed + 1024;  // alignment slack
+static_assert(kTcSmem <= 227u * 1024u, "fits the 227 KB a block may use");
+// tensor-memory columns
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+constexpr float kLog2eTc = 1.4426950408889634f;
+
+struct TcParams {
+  const uint16_t* cos_t;
+  const uint16_t* sin_t;
+  const uint32_t* cu;
+  const TileRec* tiles;
+  Ctl* ctl;
+  const float* lse;
+  const float* D;
+  float* dq;
+  uint16_t* dqkv;
+  int H;
+  long long T;
+  int window;
+  float scale;
+  unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ float ex2_tc(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// the 16-byte chunk c of row r of a 128-byte-swizzled tile
+__device__ __forceinline__ uint8_t* chunk_at(uint8_t* tile, int r, int c) {
+  return tile + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+// Row r of a landed [128][64] tile rotated in place at position pos (pairs u, u + 32: chunk c
+// with chunk c + 4), tables in the element type.
+template <bool BF16>
+__device__ __forceinline__ void rotate_row(uint8_t* tile, int r, const uint16_t* cos_t, const uint16_t* sin_t,
+                                           uint32_t pos) {
+  const uint4* cr = reinterpret_cast<const uint4*>(cos_t + static_cast<int64_t>(pos) * 32);
+  const uint4* sr = reinterpret_cast<const uint4*>(sin_t + static_cast<int64_t>(pos) * 32);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4* p1 = reinterpret_cast<uint4*>(chunk_at(tile, r, c));
+    uint4* p2 = reinterpret_cast<uint4*>(chunk_at(tile, r, c + 4));
+    const uint4 x1 = *p1, x2 = *p2, tc = __ldg(cr + c), ts = __ldg(sr + c);
+    const uint32_t a1[4] = {x1.x, x1.y, x1.z, x1.w}, a2[4] = {x2.x, x2.y, x2.z, x2.w};
+    const uint32_t ac[4] = {tc.x, tc.y, tc.z, tc.w}, as[4] = {ts.x, ts.y, ts.z, ts.w};
+    uint32_t y1[4], y2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 u = Elem<BF16>::unpack(a1[i]), w = Elem<BF16>::unpack(a2[i]);
+      const float2 co = Elem<BF16>::unpack(ac[i]), si = Elem<BF16>::unpack(as[i]);
+      y1[i] = Elem<BF16>::pack(u.x * co.x - w.x * si.x, u.y * co.y - w.y * si.y);
+      y2[i] = Elem<BF16>::pack(u.x * si.x + w.x * co.x, u.y * si.y + w.y * co.y);
+    }
+    *p1 = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+    *p2 = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+  }
+}
+
+// bounded wait shared by the roles; on a timeout it records the error and raises the CTA's flag
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, const TcParams& p, volatile int* abort) {
+  if (*abort) return false;
+  if (mbar_wait(smem_u32(bar), parity, p.timeout_ns)) return true;
+  *abort = 1;
+  set_status(p.ctl, kErrTimeout);
+  return false;
+}
+
+// The row group's decision to give up, taken together: a barrier over its 128 threads (named
+// barrier 1) that ORs their flags, so that no warp waits at a later group barrier for a warp
+// that has left.
+__device__ __forceinline__ bool group_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kTcThreads, 1)
+pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_constant__ CUtensorMap tmap_dout,
+                 const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  TcBars& B = *reinterpret_cast<TcBars*>(smem + kOffBar);
+  float* sL2 = reinterpret_cast<float*>(smem + kOffRow);  // lse log2(e) per query of the chunk
+  float* sD = sL2 + 128;
+  __shared__ uint32_t s_tmem;
+  __shared__ unsigned int s_item;
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.H;
+  const int64_t hd = static_cast<int64_t>(H) * 64;
+  const int64_t ldq = 3 * hd;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&B.kv_full), 1);
+    mbar_init(smem_u32(&B.kv_ready), 4);
+    mbar_init(smem_u32(&B.q_full), 1);
+    mbar_init(smem_u32(&B.q_ready), 4);
+    mbar_init(smem_u32(&B.s_full), 1);
+    mbar_init(smem_u32(&B.p_ready), 4);
+    mbar_init(smem_u32(&B.c_done), 1);
+    mbar_init(smem_u32(&B.drain), 1);
+    s_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_qkv);
+    tma_prefetch_desc(&tmap_dout);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&s_tmem), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const unsigned int n_items = __ldcg(&p.ctl->ntiles) * static_cast<unsigned int>(H);
+
+  // running counts: items (kv barriers) and chunks (the chunk barriers) this CTA has stepped through
+  uint32_t n_it = 0, n_ch = 0;
+  // the producer's loads so far; when the CTA gives up, the last of each is the only one that
+  // may still be in flight (a chunk's load follows the previous chunk's completed products)
+  uint32_t kv_loads = 0, q_loads = 0;
+
+  const uint32_t idS = idesc_f16(BF16, 128, 128, false, false);
+  const uint32_t idG = idesc_f16(BF16, 128, 64, false, true);
+
+  for (;;) {
+    if (tid == 0) s_item = atomicAdd(&p.ctl->next, 1u);
+    __syncthreads();
+    tc_fence_after();
+    const unsigned int item = s_item;
+    const bool stop = item >= n_items || s_abort;
+    __syncthreads();
+    if (stop) break;
+    const unsigned int ti = item / static_cast<unsigned int>(H);
+    const int h = static_cast<int>(item % static_cast<unsigned int>(H));
+    const TileRec rec = p.tiles[ti];
+    const uint32_t qend = rec.k0 + rec.nk;
+    const uint32_t nchunks = (rec.nk + 127u) / 128u;
+
+    if (warp == 0 && lane == 0) {
+      // producer: K and V of the key tile, then Q and dout of each chunk once the previous
+      // chunk's products (which read those buffers) have completed
+      mbar_arrive_expect_tx(smem_u32(&B.kv_full), 2 * kTile);
+      tma_load_2d(smem_u32(smem + kOffK), &tmap_qkv, smem_u32(&B.kv_full), static_cast<int32_t>(hd + h * 64),
+                  static_cast<int32_t>(rec.q0));
+      tma_load_2d(smem_u32(smem + kOffV), &tmap_qkv, smem_u32(&B.kv_full), static_cast<int32_t>(2 * hd + h * 64),
+                  static_cast<int32_t>(rec.q0));
+      ++kv_loads;
+      for (uint32_t c = 0; c < nchunks; ++c) {
+        if (c > 0) {
+          if (!tc_wait(&B.c_done, (n_ch + c - 1) & 1u, p, &s_abort)) break;
+        }
+        const int32_t qb = static_cast<int32_t>(rec.k0 + 128u * c);
+        mbar_arrive_expect_tx(smem_u32(&B.q_full), 2 * kTile);
+        tma_load_2d(smem_u32(smem + kOffQ), &tmap_qkv, smem_u32(&B.q_full), static_cast<int32_t>(h * 64), qb);
+        tma_load_2d(smem_u32(smem + kOffO), &tmap_dout, smem_u32(&B.q_full), static_cast<int32_t>(h * 64), qb);
+        ++q_loads;
+      }
+    } else if (warp == 1 && lane == 0) {
+      // MMA issuer
+      const uint64_t aK = sdesc_sw128(smem_u32(smem + kOffK), 16, 1024);
+      const uint64_t aV = sdesc_sw128(smem_u32(smem + kOffV), 16, 1024);
+      const uint64_t bQ = sdesc_sw128(smem_u32(smem + kOffQ), 16, 1024);
+      const uint64_t bO = sdesc_sw128(smem_u32(smem + kOffO), 16, 1024);
+      const uint64_t mO = sdesc_sw128(smem_u32(smem + kOffO), 8192, 1024);  // dout as MN-major B
+      const uint64_t mQ = sdesc_sw128(smem_u32(smem + kOffQ), 8192, 1024);  // Q' as MN-major B
+      const uint64_t mK = sdesc_sw128(smem_u32(smem + kOffK), 8192, 1024);  // K' as MN-major B
+      const uint64_t aPt0 = sdesc_sw128(smem_u32(smem + kOffPt), 16, 1024);
+      const uint64_t aPt1 = sdesc_sw128(smem_u32(smem + kOffPt + kTile), 16, 1024);
+      const uint64_t aSt0 = sdesc_sw128(smem_u32(smem + kOffSt), 16, 1024);
+      const uint64_t aSt1 = sdesc_sw128(smem_u32(smem + kOffSt + kTile), 16, 1024);
+      const uint64_t aS0 = sdesc_sw128(smem_u32(smem + kOffS), 16, 1024);
+      const uint64_t aS1 = sdesc_sw128(smem_u32(smem + kOffS + kTile), 16, 1024);
+      bool ok = tc_wait(&B.kv_ready, n_it & 1u, p, &s_abort);
+      for (uint32_t c = 0; ok && c < nchunks; ++c) {
+        const uint32_t ph = (n_ch + c) & 1u;
+        if (!(ok = tc_wait(&B.q_ready, ph, p, &s_abort))) break;
+        tc_fence_after();
+#pragma unroll
+        for (uint32_t ks = 0; ks < 4; ++ks) umma_f16_ss(tmem + kColS, aK + 2 * ks, bQ + 2 * ks, idS, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (uint32_t ks = 0; ks < 4; ++ks) umma_f16_ss(tmem + kColDP, aV + 2 * ks, bO + 2 * ks, idS, ks > 0 ? 1u : 0u);
+        umma_commit(smem_u32(&B.s_full));
+        if (!(ok = tc_wait(&B.p_ready, ph, p, &s_abort))) break;
+        tc_fence_after();
+#pragma unroll
+        for (uint32_t ks = 0; ks < 8; ++ks) {
+          const uint64_t aP = (ks < 4 ? aPt0 : aPt1) + 2 * (ks & 3u);
+          const uint64_t aT = (ks < 4 ? aSt0 : aSt1) + 2 * (ks & 3u);
+          const uint64_t aD = (ks < 4 ? aS0 : aS1) + 2 * (ks & 3u);
+          const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
+          umma_f16_ss(tmem + kColDV, aP, mO + 128 * ks, idG, acc);
+          umma_f16_ss(tmem + kColDK, aT, mQ + 128 * ks, idG, acc);
+          umma_f16_ss(tmem + kColDQ, aD, mK + 128 * ks, idG, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(smem_u32(&B.c_done));
+      }
+      // every product issued has completed before the item ends (and before tensor memory is freed)
+      umma_commit(smem_u32(&B.drain));
+      mbar_wait(smem_u32(&B.drain), n_it & 1u, p.timeout_ns);
+    } else if (warp >= kRowWarp0) {
+      // the row group: thread t is key row t (rotation, P^T / dS^T, dK / dV) and query row t
+      // of each chunk (rotation of Q', lse and D, dQ')
+      const int t = tid - kRowWarp0 * 32;
+      const uint32_t lanes = static_cast<uint32_t>((warp - kRowWarp0) * 32) << 16;
+      const bool kok = t < static_cast<int>(rec.rows);
+      const uint32_t b = rec.q0 + static_cast<uint32_t>(t);
+      int64_t klo = 0, khi = 0, kstart = 0;
+      if (kok) {
+        const uint32_t sb = rec.kind == 0 ? rec.seq : seq_of_token(p.cu, rec.seq, rec.nseq, b);
+        const int64_t ss = __ldg(p.cu + sb), se = __ldg(p.cu + sb + 1);
+        kstart = klo = ss;
+        khi = se;
+        if (p.window > 0) {
+          klo = max(ss, static_cast<int64_t>(b) - p.window);
+          khi = min(se, static_cast<int64_t>(b) + p.window + 1);
+        }
+      }
+      bool bad = group_any(!tc_wait(&B.kv_full, n_it & 1u, p, &s_abort));
+      if (!bad) {
+        if (kok) rotate_row<BF16>(smem + kOffK, t, p.cos_t, p.sin_t, static_cast<uint32_t>(b - kstart));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&B.kv_ready));
+      }
+      const float c1 = p.scale * kLog2eTc;
+      for (uint32_t c = 0; !bad && c < nchunks; ++c) {
+        const uint32_t ph = (n_ch + c) & 1u;
+        const uint32_t qb = rec.k0 + 128u * c;
+        // Q' row t of the chunk, its lse and D
+        bad = group_any(!tc_wait(&B.q_full, ph, p, &s_abort));
+        if (bad) break;
+        {
+          const uint32_t a = qb + static_cast<uint32_t>(t);
+          float l2 = 0.f, d = 0.f;
+          if (a < qend) {
+            const uint32_t sa = rec.kind == 0 ? rec.seq : seq_of_token(p.cu, rec.seq, rec.nseq, a);
+            rotate_row<BF16>(smem + kOffQ, t, p.cos_t, p.sin_t, a - __ldg(p.cu + sa));
+            l2 = __ldg(p.lse + static_cast<int64_t>(h) * p.T + a) * kLog2eTc;
+            d = __ldg(p.D + static_cast<int64_t>(h) * p.T + a);
+          }
+          sL2[t] = l2;
+          sD[t] = d;
+        }
+        fence_proxy_async_smem();
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the row group's lse / D are in place
+        if (lane == 0) mbar_arrive(smem_u32(&B.q_ready));
+        // P^T and dS^T of key row t (32 queries at a time), and dS's column t
+        bad = group_any(!tc_wait(&B.s_full, ph, p, &s_abort));
+        if (bad) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+          float s[32], dp[32];
+          tmem_ld32(tmem + lanes + kColS + 32 * cb, s);
+          tmem_ld32(tmem + lanes + kColDP + 32 * cb, dp);
+          uint32_t pw[16], dw[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int q = 32 * cb + i + e;
+              const int64_t a = static_cast<int64_t>(qb) + q;
+              const bool vis = kok && a < static_cast<int64_t>(qend) && a >= klo && a < khi;
+              pv[e] = vis ? ex2_tc(s[i + e] * c1 - sL2[q]) : 0.f;
+              dv[e] = pv[e] * (dp[i + e] - sD[q]);
+            }
+            pw[i / 2] = Elem<BF16>::pack(pv[0], pv[1]);
+            dw[i / 2] = Elem<BF16>::pack(dv[0], dv[1]);
+          }
+          // rows of P^T and dS^T: queries 32 cb .. 32 cb + 31 are chunks 4 (cb & 1) .. + 3 of tile cb / 2
+          uint8_t* tp = smem + kOffPt + (cb >> 1) * kTile;
+          uint8_t* tt = smem + kOffSt + (cb >> 1) * kTile;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int ch = 4 * (cb & 1) + j;
+            *reinterpret_cast<uint4*>(chunk_at(tp, t, ch)) = make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
+            *reinterpret_cast<uint4*>(chunk_at(tt, t, ch)) = make_uint4(dw[4 * j], dw[4 * j + 1], dw[4 * j + 2], dw[4 * j + 3]);
+          }
+          // dS [query][key]: column t of rows 32 cb .. 32 cb + 31 (key t sits in tile t / 64, chunk
+          // (t % 64) / 8, element t % 8)
+          uint8_t* ts = smem + kOffS + (t >> 6) * kTile;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int q = 32 * cb + i;
+            const uint32_t w = dw[i >> 1];
+            const uint16_t v16 = static_cast<uint16_t>((i & 1) ? (w >> 16) : (w & 0xFFFFu));
+            *reinterpret_cast<uint16_t*>(chunk_at(ts, q, (t & 63) >> 3) + 2 * (t & 7)) = v16;
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // every column of dS is written
+        if (lane == 0) mbar_arrive(smem_u32(&B.p_ready));
+        // dQ' of query row t, added to the fp32 accumulator
+        bad = group_any(!tc_wait(&B.c_done, ph, p, &s_abort));
+        if (bad) break;
+        tc_fence_after();
+        {
+          float v[64];
+          tmem_ld64(tmem + lanes + kColDQ, v);
+          const uint32_t a = qb + static_cast<uint32_t>(t);
+          if (a < qend) {
+            float4* dst = reinterpret_cast<float4*>(p.dq + static_cast<int64_t>(a) * hd + h * 64);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              atomicAdd(dst + j, make_float4(p.scale * v[4 * j], p.scale * v[4 * j + 1], p.scale * v[4 * j + 2],
+                                             p.scale * v[4 * j + 3]));
+          }
+        }
+        tc_fence_before();
+      }
+      // dk = rot^T(scale dK') and dv of key row t, rounded once
+      if (!bad) {
+        float k2[64], v2[64];
+        tmem_ld64(tmem + lanes + kColDK, k2);
+        tmem_ld64(tmem + lanes + kColDV, v2);
+        if (kok) {
+          const uint32_t pos = static_cast<uint32_t>(b - kstart);
+          const uint16_t* cr = p.cos_t + static_cast<int64_t>(pos) * 32;
+          const uint16_t* sr = p.sin_t + static_cast<int64_t>(pos) * 32;
+          uint16_t* rowk = p.dqkv + static_cast<int64_t>(b) * ldq + hd + h * 64;
+          uint16_t* rowv = p.dqkv + static_cast<int64_t>(b) * ldq + 2 * hd + h * 64;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 tc4 = __ldg(reinterpret_cast<const uint4*>(cr) + c);
+            const uint4 ts4 = __ldg(reinterpret_cast<const uint4*>(sr) + c);
+            const uint32_t ac[4] = {tc4.x, tc4.y, tc4.z, tc4.w}, as[4] = {ts4.x, ts4.y, ts4.z, ts4.w};
+            uint32_t ya[4], yb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 co = Elem<BF16>::unpack(ac[i]), si = Elem<BF16>::unpack(as[i]);
+              const int u = 8 * c + 2 * i;
+              const float xa0 = p.scale * k2[u], xb0 = p.scale * k2[u + 32];
+              const float xa1 = p.scale * k2[u + 1], xb1 = p.scale * k2[u + 33];
+              ya[i] = Elem<BF16>::pack(fmaf(xa0, co.x, xb0 * si.x), fmaf(xa1, co.y, xb1 * si.y));
+              yb[i] = Elem<BF16>::pack(fmaf(xb0, co.x, -xa0 * si.x), fmaf(xb1, co.y, -xa1 * si.y));
+            }
+            reinterpret_cast<uint4*>(rowk)[c] = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+            reinterpret_cast<uint4*>(rowk)[c + 4] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            reinterpret_cast<uint4*>(rowv)[c] =
+                make_uint4(Elem<BF16>::pack(v2[8 * c], v2[8 * c + 1]), Elem<BF16>::pack(v2[8 * c + 2], v2[8 * c + 3]),
+                           Elem<BF16>::pack(v2[8 * c + 4], v2[8 * c + 5]), Elem<BF16>::pack(v2[8 * c + 6], v2[8 * c + 7]));
+        }
+        tc_fence_before();
+      }
+    }
+    ++n_it;
+    n_ch += nchunks;
+  }
+
+  // the producer's copies in flight land before the CTA's shared memory goes away
+  if (warp == 0 && lane == 0 && s_abort) {
+    if (kv_loads) mbar_wait(smem_u32(&B.kv_full), (kv_loads - 1u) & 1u, p.timeout_ns);
+    if (q_loads) mbar_wait(smem_u32(&B.q_full), (q_loads - 1u) & 1u, p.timeout_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, 512);
+}
+
+typedef CUresult (*EncodeTiledTc)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledTc encode_tc() {
+  static EncodeTiledTc fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* q = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) == cudaSuccess &&
+        r == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledTc>(q);
+  }
+  return fn;
+}
+
+bool tile_map(CUtensorMap* m, bool bf16, const void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledTc enc = encode_tc();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+unsigned long long tc_timeout_ns() {
+  const char* e = std::getenv("PK_TIMEOUT_MS");
+  const long long ms = e ? std::atoll(e) : 0;
+  return static_cast<unsigned long long>(ms > 0 ? ms : 2000) * 1000000ull;
+}
+
+}  // namespace
+
+cudaError_t backward_tc_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(pk_bwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pk_bwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  return e;
+}
+
+// The main kernel for 16-bit types: dq' added to `dq` (zeroed by the caller), dk and dv written to dqkv.
+cudaError_t backward_tc_launch(bool bf16, const void* qkv, const void* cos_t, const void* sin_t, const uint32_t* cu,
+                               long long T, int H, int window, float scale, const float* lse, const void* dout,
+                               const float* D, float* dq, void* dqkv, const TileRec* tiles, Ctl* ctl, int sms,
+                               cudaStream_t stream) {
+  CUtensorMap mq, mo;
+  if (!tile_map(&mq, bf16, qkv, 3ull * H * 64, static_cast<uint64_t>(T)) ||
+      !tile_map(&mo, bf16, dout, 1ull * H * 64, static_cast<uint64_t>(T)))
+    return cudaErrorInvalidValue;
+  TcParams p;
+  p.cos_t = static_cast<const uint16_t*>(cos_t);
+  p.sin_t = static_cast<const uint16_t*>(sin_t);
+  p.cu = cu;
+  p.tiles = tiles;
+  p.ctl = ctl;
+  p.lse = lse;
+  p.D = D;
+  p.dq = dq;
+  p.dqkv = static_cast<uint16_t*>(dqkv);
+  p.H = H;
+  p.T = T;
+  p.window = window;
+  p.scale = scale;
+  p.timeout_ns = tc_timeout_ns();
+  if (bf16)
+    pk_bwd_tc_kernel<true><<<sms, kTcThreads, kTcSmem, stream>>>(mq, mo, p);
+  else
+    pk_bwd_tc_kernel<false><<<sms, kTcThreads, kTcSmem, stream>>>(mq, mo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace pk
