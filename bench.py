@@ -73,11 +73,19 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def kernel_source_hash() -> str:
-    """sha1 over what the attention kernel is built from: its source, the device header and
-    the build flags."""
+KERNEL_NAMES = {0: "pk_attend_band_kernel", 1: "pk_attend_f32_kernel", 2: "pk_attend_tc_kernel",
+                3: "pk_attend_q4_kernel", 4: "pk_attend_tc_kernel (single-record items)"}
+# the source file of each forward kernel (enum pk_kernel)
+KERNEL_SOURCES = {0: "pk_attend_band.cu", 1: "pk_attend_f32.cu", 2: "pk_attend_tc.cu", 3: "pk_attend_q4.cu",
+                  4: "pk_attend_tc.cu"}
+
+
+def kernel_source_hash(kernel: int = 2) -> str:
+    """sha1 over what a forward kernel is built from: its source, the device headers and the
+    build flags."""
     h = hashlib.sha1()
-    for rel in (("csrc", "pk_attend_tc.cu"), ("csrc", "pk_dev.cuh"), ("build.py",)):
+    for rel in (("csrc", KERNEL_SOURCES[kernel]), ("csrc", "pk_dev.cuh"), ("csrc", "pk_attn_common.cuh"),
+                ("build.py",)):
         with open(os.path.join(ROOT, "rope_cu_tile_gb300", *rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -252,7 +260,8 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
 
     def step(i):
         q, o, l = sets[i % nsets]
-        pk.attend(q, cos, sin, cu, wl.H, wl.window, wl.scale, out=o, lse=l, stream=stream, max_len=max_len)
+        pk.attend(q, cos, sin, cu, wl.H, wl.window, wl.scale, out=o, lse=l, stream=stream, max_len=max_len,
+                  tuned=True)
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -260,6 +269,7 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
     torch.cuda.synchronize()
     if pk.last_status(stream) != 0:
         raise RuntimeError("device error during warm-up")
+    kernel = pk.pk_tune_pick(pk.dtype_code(qkv0), wl.H, wl.window, wl.T, max_len)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -326,11 +336,11 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
             b["copied"].record(s_in)
         stream.wait_event(b["copied"])
         stream.wait_event(b["read"])  # its results of two steps ago have been read out
-        rc = pk.pk_attend_dt(code, b["qkv"].data_ptr(), b["cos"].data_ptr(), b["sin"].data_ptr(),
-                             b["cu"].data_ptr(), wl.S, wl.T, wl.H, wl.window, float(wl.scale),
-                             b["out"].data_ptr(), b["lse"].data_ptr(), sh)
+        rc = pk.pk_attend_tuned(code, b["qkv"].data_ptr(), b["cos"].data_ptr(), b["sin"].data_ptr(),
+                                b["cu"].data_ptr(), wl.S, wl.T, wl.H, wl.window, float(wl.scale), max_len,
+                                b["out"].data_ptr(), b["lse"].data_ptr(), sh)
         if rc:
-            raise RuntimeError(f"pk_attend_dt -> {rc}")
+            raise RuntimeError(f"pk_attend_tuned -> {rc}")
         b["computed"].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(b["computed"])
@@ -354,7 +364,8 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
 
     return {"ms_per_step": ms / steps, "attend_ms": attend_ms / max(calls, 1),
             "schedule_ms": sched_ms / max(calls, 1), "calls": calls, "flops": flops, "bytes": abytes,
-            "nsets": nsets, "clocks": clk.summary(), "e2e_ms": e2e_ms, "h2d": int(h2d), "d2h": int(d2h)}
+            "nsets": nsets, "clocks": clk.summary(), "e2e_ms": e2e_ms, "h2d": int(h2d), "d2h": int(d2h),
+            "kernel": kernel}
 
 
 def run_rope(wl, steps, warmup, dev_index, dims=64):
@@ -443,7 +454,7 @@ def run_backward(wl, steps, warmup, dev_index):
     return {"ms": ev0.elapsed_time(ev1) / steps, "clocks": clk.summary()}
 
 
-def roofline(wl, attend_ms, peaks, peak_src):
+def roofline(wl, attend_ms, peaks, peak_src, kernel=2):
     flops, abytes = work(wl)
     t_bw = abytes / (peaks["hbm_gbs"] * 1e9)
     t_fl = flops / (peaks["bf16_tflops"] * 1e12)
@@ -458,9 +469,9 @@ def roofline(wl, attend_ms, peaks, peak_src):
     r["frac"] = achieved / peak
     r["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     h, tr = NCU_TRAFFIC.get(wl.name, (None, None))
-    r["traffic"] = tr if (h is not None and h == kernel_source_hash()) else None
+    r["traffic"] = tr if (h is not None and h == kernel_source_hash(kernel)) else None
     r["t_roof_us"] = max(t_bw, t_fl) * 1e6
-    r["kernel"] = "pk_attend_tc_kernel" if wl.dtype != "f32" else "pk_attend_f32_kernel"
+    r["kernel"] = KERNEL_NAMES.get(kernel, str(kernel))
     return r
 
 
@@ -566,10 +577,12 @@ def main():
             "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic", "config": cfg,
             "tokens_per_s": tokens_s,
-            "roofline": roofline(wl, r["attend_ms"], peaks, psrc),
+            "roofline": roofline(wl, r["attend_ms"], peaks, psrc, r["kernel"]),
+            "kernel": {"picked": KERNEL_NAMES.get(r["kernel"], str(r["kernel"])),
+                       "by": "pk_attend_tuned (timed once per shape key during warm-up)"},
             "step_roofline_frac": (max(abytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
                                    / (r["ms_per_step"] * 1e-3)),
-            "kernel_ms": {"pk_schedule_kernel": r["schedule_ms"], "attention": r["attend_ms"],
+            "kernel_ms": {"preparation (tile scheduler or cu check)": r["schedule_ms"], "attention": r["attend_ms"],
                           "timing": "a second pass of the same steps with CUDA events around each kernel"},
             "e2e": {"value": world * flops / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms_per_step": r["e2e_ms"]},

@@ -273,6 +273,26 @@ int pk_attend_mixed(int out_dtype, const float *qkv, const float *cos, const flo
                     void *out, float *lse, struct CUstream_st *stream);
 
 /*
+ * pk_attend_mixed_ops -- fp32 storage with 16-bit tensor-core operands (the pages' generic
+ * attend with storage type F = f32 and operand type M = f16 or bf16, as packed.rs's tests run
+ * it): q and k are rotated in fp32 from the fp32 qkv and tables, q', k', v and the
+ * probabilities are rounded to op_dtype as the operands of the products, which accumulate in
+ * fp32, and out is written in fp32.
+ *   - op_dtype: PK_F16 or PK_BF16 (otherwise PK_ERR_ARG).
+ *   - qkv, cos, sin: fp32 as pk_attend_f32; out [T, H*64] fp32; lse [H, T] fp32; the other
+ *     arguments, alignment, capture and errors as pk_attend.
+ *   - For fp32 inputs whose values are representable in op_dtype the result equals the
+ *     op_dtype path's (pk_attend_dt with op_dtype inputs and PK_KERNEL_TC), out before its
+ *     rounding to op_dtype, bit for bit.
+ *   - Allocates, on first use per (device, stream) and when a larger T*H arrives, the rotated
+ *     16-bit copy of qkv (T*3*H*64 elements, kept with the workspace, freed by pk_release).
+ *   - Kernels: the tile scheduler, the rotation into the copy, PK_KERNEL_TC (fp32 output).
+ */
+int pk_attend_mixed_ops(int op_dtype, const float *qkv, const float *cos, const float *sin,
+                        const uint32_t *cu, int S, int64_t T, int H, int window, float scale,
+                        float *out, float *lse, struct CUstream_st *stream);
+
+/*
  * pk_rope -- the standalone rotary embedding of a packed qkv: the pages' rope op
  * (hanzo-kernel fast ops, FastOp::Rope and its graph fallback), applied as kime's rope step
  * applies it, to every q and k head vector of qkv.

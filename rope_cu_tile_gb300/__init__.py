@@ -32,7 +32,7 @@ EXPORTS = ("pk_attend", "pk_attend_bf16", "pk_attend_f16", "pk_attend_f32", "pk_
            "pk_schedule", "pk_schedule_capacity", "pk_last_status", "pk_status_string",
            "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop", "pk_attend_noalloc", "pk_rope", "pk_attend_mixed",
            "pk_attend_backward", "pk_attend_tuned", "pk_tune_pick", "pk_tune_key", "pk_tune_clear",
-           "pk_forward_kernel", "pk_kernel_name")
+           "pk_forward_kernel", "pk_kernel_name", "pk_attend_mixed_ops")
 KERNELS = {0: "band", 1: "f32", 2: "tc", 3: "q4", 4: "tc_single"}
 
 _lib = None
@@ -67,6 +67,8 @@ def load(path: str | None = None):
     L.pk_attend_backward.restype = i32
     L.pk_attend_mixed.argtypes = [i32] + sig
     L.pk_attend_mixed.restype = i32
+    L.pk_attend_mixed_ops.argtypes = [i32] + sig
+    L.pk_attend_mixed_ops.restype = i32
     L.pk_attend_tuned.argtypes = [i32, vp, vp, vp, vp, i32, i64, i32, i32, f32, i64, vp, vp, vp]
     L.pk_attend_tuned.restype = i32
     L.pk_tune_pick.argtypes = [i32, i32, i32, i64, i64]
@@ -127,6 +129,43 @@ def pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse
     """The allocation-free variant (see include/pk.h): for callers that cannot let the library
     cudaMalloc a workspace; `status` is an optional device pointer to one int."""
     return load().pk_attend_noalloc(dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, status, stream)
+
+
+def pk_attend_mixed_ops(op_dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream) -> int:
+    """fp32 storage, 16-bit tensor-core operands, fp32 out (see include/pk.h)."""
+    return load().pk_attend_mixed_ops(op_dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream)
+
+
+def attend_mixed_ops(qkv, cos, sin, cu, H: int, window: int, scale: float, op_dtype, out=None, lse=None,
+                     stream=None, max_len=None):
+    """out [T, H*64] and lse [H, T], both float32, for float32 device tensors qkv [T, 3*H*64] and
+    cos/sin [P, 32], the products on the tensor cores with operands of op_dtype
+    (torch.float16 or torch.bfloat16)."""
+    torch = _torch()
+    if qkv.dtype != torch.float32:
+        raise TypeError("qkv must be float32")
+    _check_inputs(qkv, cos, sin, cu, H, 32)
+    _check_stream(stream, qkv.device)
+    code = {torch.float16: PK_F16, torch.bfloat16: PK_BF16}.get(op_dtype)
+    if code is None:
+        raise TypeError("op_dtype must be torch.float16 or torch.bfloat16")
+    T = qkv.shape[0]
+    with torch.cuda.device(qkv.device):
+        _check_table_rows(cu, cos.shape[0], max_len)
+        if out is None:
+            out = torch.empty((T, H * 64), dtype=torch.float32, device=qkv.device)
+        else:
+            _need(out, (T, H * 64), torch.float32, "out")
+        if lse is None:
+            lse = torch.empty((H, T), dtype=torch.float32, device=qkv.device)
+        else:
+            _need(lse, (H, T), torch.float32, "lse")
+        _same_device(qkv, out, lse)
+        rc = pk_attend_mixed_ops(code, qkv.data_ptr(), cos.data_ptr(), sin.data_ptr(), cu.data_ptr(),
+                                 cu.shape[0] - 1, T, H, window, float(scale), out.data_ptr(), lse.data_ptr(),
+                                 _stream_handle(stream))
+        _check(rc, "pk_attend_mixed_ops")
+    return out, lse
 
 
 def pk_attend_tuned(dtype, qkv, cos, sin, cu, S, T, H, window, scale, longest, out, lse, stream) -> int:

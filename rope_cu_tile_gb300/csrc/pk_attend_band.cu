@@ -13,13 +13,16 @@
 // the stored values (no rounding of the rotated q and k, or of the probabilities, to the
 // storage type), which also keeps fp16 inputs of large magnitude inside their tolerance.
 //
-// Launch: one 128-thread CTA per block of 32 tokens and group of four heads (warp w: head
-// 4 g + w). A warp stages the rows [t0 - w, t0 + 32 + w) of its head: k rotated to fp32, v
-// as stored, each row padded so that consecutive rows start four banks apart. Lane l owns
-// query row t0 + l: q' in registers, the 2 w + 1 scores, the softmax, and 64 fp32 output
-// accumulators. The sequence of every staged token comes from the offsets cu[s0 ..] staged
-// once per CTA, s0 being the sequence of the block's first staged token; pk_band_prep_kernel
-// (launched just before, on the same stream) checks cu and writes s0 for every block.
+// Launch: one CTA per block of 32 tokens and group of four, two or one heads (one warp per
+// head: as many as let two CTAs share an SM). Every global read is an asynchronous copy into shared memory, all of a CTA's in
+// flight at once: each warp's raw q, k and v rows of its head over the staged tokens
+// [t0 - W, t0 + 32 + W), and the CTA's cos / sin rows of those tokens' positions. Then a
+// warp rotates its k rows to fp32 (rows padded so that consecutive rows start four banks
+// apart) and lane l takes query row t0 + l: q' in registers, the 2 w + 1 scores (kept in
+// shared memory), the softmax, and 64 fp32 output accumulators. The sequence of every staged
+// token comes from the offsets cu[s0 ..] staged once per CTA, s0 being the sequence of the
+// block's first staged token; pk_band_prep_kernel (launched just before, on the same stream)
+// checks cu and writes s0 for every block.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -31,7 +34,6 @@ namespace pk {
 namespace {
 
 constexpr int kBandRows = 32;     // query tokens per block
-constexpr int kBandHeads = 4;     // heads per CTA (one warp each)
 constexpr int kBandCu = 96;       // staged sequence offsets per CTA
 constexpr int kKStride = 68;      // floats per staged k' row (64 + 4: rows 4 banks apart)
 
@@ -141,22 +143,58 @@ __global__ void __launch_bounds__(1024) pk_band_prep_kernel(const uint32_t* __re
   }
 }
 
+// 16-byte asynchronous copy global -> shared (through L1: table rows repeat across tokens)
+__device__ __forceinline__ void band_cp16(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// Shared-memory layout of a CTA (W: the instance's largest window; rows: 32 + 2 W staged
+// tokens; VS: elements per staged 16-bit or fp32 row, padded so rows start 4 banks apart):
+//   k'   [4][rows][68] fp32        rotated keys
+//   v    [4][rows][VS] stored      values
+//   q    [4][32][VS]   stored      raw queries (then the scores [4][2 W + 1][32] fp32)
+//   kraw [4][rows][VS] stored      raw keys
+//   tab  [rows][2][32] stored      cos and sin rows of each staged token's position
+template <typename F, int W>
+struct BandSmem {
+  static constexpr int kRows = kBandRows + 2 * W;
+  static constexpr int kVS = Store<F>::kVStride;
+  // bytes of one head's rows (k', v, q, raw k) and of the CTA's table rows
+  static constexpr size_t kPerHead = sizeof(float) * kRows * kKStride + sizeof(F) * kRows * kVS +
+                                     sizeof(F) * kBandRows * kVS + sizeof(F) * kRows * kVS;
+  static constexpr size_t kTabBytes = sizeof(F) * kRows * 2 * kHalf;
+  // heads per CTA (one warp each): four, two or one, whichever lets two CTAs share an SM
+  static constexpr size_t kTwoPerSm = 113 * 1024;
+  static constexpr int kHeads = 4 * kPerHead + kTabBytes <= kTwoPerSm ? 4 : 2 * kPerHead + kTabBytes <= kTwoPerSm ? 2 : 1;
+  static constexpr size_t kK = 0;
+  static constexpr size_t kV = kK + sizeof(float) * kHeads * kRows * kKStride;
+  static constexpr size_t kQ = kV + sizeof(F) * kHeads * kRows * kVS;
+  static constexpr size_t kKraw = kQ + sizeof(F) * kHeads * kBandRows * kVS;
+  static constexpr size_t kTab = kKraw + sizeof(F) * kHeads * kRows * kVS;
+  static constexpr size_t kBytes = kTab + kTabBytes;
+  static_assert(kBytes <= 227 * 1024, "fits the shared memory a block may use");
+  static_assert(sizeof(float) * (2 * W + 1) * 32 <= sizeof(F) * kBandRows * kVS, "scores fit the q area");
+};
+
 // W: the largest window this instance serves (4, 8 or 16); the call's window is 1 .. W.
 template <typename F, int OUT, int W>
-__global__ void __launch_bounds__(kBandRows * kBandHeads)
+__global__ void __launch_bounds__(kBandRows * BandSmem<F, W>::kHeads)
 pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, const F* __restrict__ sin_t,
                       const uint32_t* __restrict__ cu, int S, const uint32_t* __restrict__ first,
                       void* __restrict__ out, float* __restrict__ lse, const Ctl* ctl, int H, long long T,
                       int window, float scale) {
-  constexpr int kRowsSt = kBandRows + 2 * W;  // staged token rows
-  constexpr int kVS = Store<F>::kVStride;
-  // dynamic shared memory: k' [head][row][kKStride] fp32, v [head][row][kVS] stored type,
-  // then the scores [head][2 W + 1][lane] fp32
+  using L = BandSmem<F, W>;
+  constexpr int kRowsSt = L::kRows;
+  constexpr int kVS = L::kVS;
+  constexpr int kChunk = 16 / sizeof(F);          // elements per 16-byte chunk
+  constexpr int kRowChunks = kD / kChunk;         // chunks per 64-element row
+  constexpr int kTabChunks = kHalf / kChunk;      // chunks per 32-element table row
   extern __shared__ __align__(16) unsigned char band_smem[];
-  auto s_k = reinterpret_cast<float (*)[kRowsSt][kKStride]>(band_smem);
-  auto s_v = reinterpret_cast<F (*)[kRowsSt][kVS]>(band_smem + sizeof(float) * kBandHeads * kRowsSt * kKStride);
-  float* s_p = reinterpret_cast<float*>(band_smem + sizeof(float) * kBandHeads * kRowsSt * kKStride +
-                                        sizeof(F) * kBandHeads * kRowsSt * kVS);  // [head][2 W + 1][lane]
+  auto s_k = reinterpret_cast<float (*)[kRowsSt][kKStride]>(band_smem + L::kK);
+  auto s_v = reinterpret_cast<F (*)[kRowsSt][kVS]>(band_smem + L::kV);
+  auto s_q = reinterpret_cast<F (*)[kBandRows][kVS]>(band_smem + L::kQ);
+  auto s_kr = reinterpret_cast<F (*)[kRowsSt][kVS]>(band_smem + L::kKraw);
+  auto s_tab = reinterpret_cast<F (*)[2][kHalf]>(band_smem + L::kTab);
   __shared__ uint32_t s_cu[kBandCu + 1];
   __shared__ int s_ncu;
   __shared__ int s_seq_lo[kRowsSt], s_seq_hi[kRowsSt];  // sequence [start, end) of each staged token
@@ -166,14 +204,42 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
   const long long b = blockIdx.x;
   const long long t0 = b * kBandRows;
   const long long base = t0 - W;  // token of staged row 0
-  const int h = blockIdx.y * kBandHeads + warp;
+  const int h = blockIdx.y * L::kHeads + warp;
+  const int64_t ldq = 3ll * H * kD;
   // the offsets were checked (and `first` written) by the kernel launched just before
   griddep_wait();
   if (__ldcg(&ctl->ntiles) == 0u) return;
 
+  // raw q, k and v rows of this warp's head: asynchronous copies, all in flight at once
+  if (h < H) {
+    for (int i = lane; i < kRowsSt * kRowChunks; i += 32) {
+      const int r = i / kRowChunks, c = i % kRowChunks;
+      const long long a = base + r;
+      F* kd = s_kr[warp][r] + c * kChunk;
+      F* vd = s_v[warp][r] + c * kChunk;
+      if (a >= 0 && a < T) {
+        const F* row = qkv + a * ldq;
+        band_cp16(kd, row + static_cast<int64_t>(H + h) * kD + c * kChunk);
+        band_cp16(vd, row + static_cast<int64_t>(2 * H + h) * kD + c * kChunk);
+      } else {
+        *reinterpret_cast<uint4*>(kd) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(vd) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    for (int i = lane; i < kBandRows * kRowChunks; i += 32) {
+      const int r = i / kRowChunks, c = i % kRowChunks;
+      const long long a = t0 + r;
+      F* qd = s_q[warp][r] + c * kChunk;
+      if (a < T)
+        band_cp16(qd, qkv + a * ldq + static_cast<int64_t>(h) * kD + c * kChunk);
+      else
+        *reinterpret_cast<uint4*>(qd) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   // stage cu[s0 .. s0 + kBandCu] (the block's staged tokens start in sequence s0)
   const uint32_t s0 = __ldg(first + b);
-  for (int i = tid; i <= kBandCu; i += blockDim.x) s_cu[i] = s0 + i <= static_cast<uint32_t>(S) ? __ldg(cu + s0 + i) : 0xFFFFFFFFu;
+  for (int i = tid; i <= kBandCu; i += blockDim.x)
+    s_cu[i] = s0 + i <= static_cast<uint32_t>(S) ? __ldg(cu + s0 + i) : 0xFFFFFFFFu;
   if (tid == 0) s_ncu = min(kBandCu, S - static_cast<int>(s0));
   __syncthreads();
   // the sequence bounds of every staged token (from the staged offsets when they reach it)
@@ -196,61 +262,37 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
     s_seq_hi[r] = hi;
   }
   __syncthreads();
+  // the cos and sin rows of every staged token's position
+  for (int i = tid; i < kRowsSt * 2 * kTabChunks; i += blockDim.x) {
+    const int r = i / (2 * kTabChunks), rest = i % (2 * kTabChunks);
+    const int which = rest / kTabChunks, c = rest % kTabChunks;
+    const long long a = base + r;
+    if (a >= 0 && a < T) {
+      const int64_t pos = a - s_seq_lo[r];
+      band_cp16(&s_tab[r][which][c * kChunk], (which ? sin_t : cos_t) + pos * kHalf + c * kChunk);
+    } else {
+      *reinterpret_cast<uint4*>(&s_tab[r][which][c * kChunk]) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
   if (h >= H) return;
 
-  const int64_t ldq = 3ll * H * kD;
-  // stage k' (rotated, fp32) and v of the rows [base, base + kRowsSt) of head h: eight lanes
-  // per row, lane chunk c holding elements 8 c .. 8 c + 7 (chunk c < 4: first half u = 8 c;
-  // c >= 4: second half u = 8 (c - 4) + 32, paired with chunk c - 4 through a shuffle)
-  {
-    const int c = lane & 7;
-    const int u = 8 * (c & 3);
-#pragma unroll 1
-    for (int r0 = 0; r0 < kRowsSt; r0 += 4) {
-      const int r = r0 + (lane >> 3);
-      const long long a = base + r;
-      const bool in = r < kRowsSt && a >= 0 && a < T;
-      float x[8], tc[8], ts[8];
-      if (in) {
-        const F* row = qkv + a * ldq;
-        const int64_t pos = a - s_seq_lo[r];
-        load8(row + static_cast<int64_t>(H + h) * kD + 8 * c, x);
-        load8(cos_t + pos * kHalf + u, tc);
-        load8(sin_t + pos * kHalf + u, ts);
-        F* vd = s_v[warp][r] + 8 * c;
-        if constexpr (sizeof(F) == 4) {
-          const float4* vs = reinterpret_cast<const float4*>(row + static_cast<int64_t>(2 * H + h) * kD + 8 * c);
-          reinterpret_cast<float4*>(vd)[0] = __ldg(vs);
-          reinterpret_cast<float4*>(vd)[1] = __ldg(vs + 1);
-        } else {
-          *reinterpret_cast<uint4*>(vd) =
-              __ldg(reinterpret_cast<const uint4*>(row + static_cast<int64_t>(2 * H + h) * kD + 8 * c));
-        }
-      } else {
+  // k' = rot(k) in fp32: four lanes per row, lane chunk c < 4 holding elements 8 c .. 8 c + 7
+  // of each half (the rotary pairs (u, u + 32))
+  for (int i = lane; i < kRowsSt * 4; i += 32) {
+    const int r = i >> 2, c = i & 3;
+    const F* kr = s_kr[warp][r];
+    const F* tc = s_tab[r][0];
+    const F* ts = s_tab[r][1];
+    float* kd = s_k[warp][r];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = tc[k] = ts[k] = 0.f;
-        if (r < kRowsSt) {
-          F* vd = s_v[warp][r] + 8 * c;
-          if constexpr (sizeof(F) == 4) {
-            reinterpret_cast<float4*>(vd)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-            reinterpret_cast<float4*>(vd)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-          } else {
-            *reinterpret_cast<uint4*>(vd) = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-      }
-      // the partner chunk (c ^ 4) holds the other element of each rotary pair
-      float y[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float xo = __shfl_xor_sync(0xffffffffu, x[k], 4);
-        y[k] = c < 4 ? x[k] * tc[k] - xo * ts[k] : xo * ts[k] + x[k] * tc[k];
-      }
-      if (r < kRowsSt) {
-        float* kd = s_k[warp][r] + 8 * c;
-        reinterpret_cast<float4*>(kd)[0] = make_float4(y[0], y[1], y[2], y[3]);
-        reinterpret_cast<float4*>(kd)[1] = make_float4(y[4], y[5], y[6], y[7]);
-      }
+    for (int e = 0; e < 8; ++e) {
+      const int u = 8 * c + e;
+      const float x1 = Store<F>::to_f(kr[u]), x2 = Store<F>::to_f(kr[u + kHalf]);
+      const float cc = Store<F>::to_f(tc[u]), ss = Store<F>::to_f(ts[u]);
+      kd[u] = x1 * cc - x2 * ss;
+      kd[u + kHalf] = x1 * ss + x2 * cc;
     }
   }
   // this lane's query row: q' = rot(q, pos) * scale in fp32
@@ -258,36 +300,29 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
   const bool row_ok = a < T;
   float q[kD];
   int lo = 0, hi = 0;
-  if (row_ok) {
+  {
     const int r = lane + W;
-    lo = max(s_seq_lo[r], static_cast<int>(a) - window);
-    hi = min(s_seq_hi[r], static_cast<int>(a) + window + 1);
-    const int64_t pos = a - s_seq_lo[r];
-    const F* qx = qkv + a * ldq + static_cast<int64_t>(h) * kD;
-    const F* cr = cos_t + pos * kHalf;
-    const F* sr = sin_t + pos * kHalf;
+    const F* qr = s_q[warp][lane];
+    const F* tc = s_tab[r][0];
+    const F* ts = s_tab[r][1];
 #pragma unroll
-    for (int u = 0; u < kHalf; u += 8) {
-      float x1[8], x2[8], c[8], s[8];
-      load8(qx + u, x1);
-      load8(qx + u + kHalf, x2);
-      load8(cr + u, c);
-      load8(sr + u, s);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        q[u + k] = (x1[k] * c[k] - x2[k] * s[k]) * scale;
-        q[u + kHalf + k] = (x1[k] * s[k] + x2[k] * c[k]) * scale;
-      }
+    for (int u = 0; u < kHalf; ++u) {
+      const float x1 = Store<F>::to_f(qr[u]), x2 = Store<F>::to_f(qr[u + kHalf]);
+      const float cc = Store<F>::to_f(tc[u]), ss = Store<F>::to_f(ts[u]);
+      q[u] = (x1 * cc - x2 * ss) * scale;
+      q[u + kHalf] = (x1 * ss + x2 * cc) * scale;
     }
-  } else {
-#pragma unroll
-    for (int d = 0; d < kD; ++d) q[d] = 0.f;
+    if (row_ok) {
+      lo = max(s_seq_lo[r], static_cast<int>(a) - window);
+      hi = min(s_seq_hi[r], static_cast<int>(a) + window + 1);
+    }
   }
   __syncwarp();
 
   // scores of the keys a - W .. a + W (staged rows lane .. lane + 2 W), kept per lane in shared
   // memory; invisible ones -inf. The key loops stay rolled (a small register footprint).
-  float* sc = s_p + warp * (2 * W + 1) * 32 + lane;  // score d of this lane at sc[32 d]
+  // (the raw q rows are read: their area holds the scores now)
+  float* sc = reinterpret_cast<float*>(s_q[warp]) + lane;  // score d of this lane at sc[32 d]
   float m = -INFINITY;
 #pragma unroll 1
   for (int d = 0; d <= 2 * W; ++d) {
@@ -357,9 +392,7 @@ namespace {
 
 template <typename F, int W>
 constexpr size_t band_smem_bytes() {
-  return sizeof(float) * kBandHeads * (kBandRows + 2 * W) * kKStride +
-         sizeof(F) * kBandHeads * (kBandRows + 2 * W) * Store<F>::kVStride +
-         sizeof(float) * kBandHeads * (2 * W + 1) * 32;
+  return BandSmem<F, W>::kBytes;
 }
 
 template <typename F, int OUT, int W>
@@ -381,9 +414,7 @@ cudaError_t band_launch_w(const void* qkv, const void* cos_t, const void* sin_t,
                           const uint32_t* first, void* out, float* lse, const Ctl* ctl, int H, long long T, int window,
                           float scale, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((T + kBandRows - 1) / kBandRows),
-                     static_cast<unsigned>((H + kBandHeads - 1) / kBandHeads));
-  cfg.blockDim = dim3(kBandRows * kBandHeads);
+  cfg.gridDim = dim3(static_cast<unsigned>((T + kBandRows - 1) / kBandRows));
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -393,16 +424,23 @@ cudaError_t band_launch_w(const void* qkv, const void* cos_t, const void* sin_t,
   const F* q = static_cast<const F*>(qkv);
   const F* c = static_cast<const F*>(cos_t);
   const F* s = static_cast<const F*>(sin_t);
+  auto shape = [&](int heads) {
+    cfg.gridDim.y = static_cast<unsigned>((H + heads - 1) / heads);
+    cfg.blockDim = dim3(kBandRows * heads);
+  };
   if (window <= 4) {
+    shape(BandSmem<F, 4>::kHeads);
     cfg.dynamicSmemBytes = band_smem_bytes<F, 4>();
     return cudaLaunchKernelEx(&cfg, pk_attend_band_kernel<F, OUT, 4>, q, c, s, cu, S, first, out, lse, ctl, H, T,
                               window, scale);
   }
   if (window <= 8) {
+    shape(BandSmem<F, 8>::kHeads);
     cfg.dynamicSmemBytes = band_smem_bytes<F, 8>();
     return cudaLaunchKernelEx(&cfg, pk_attend_band_kernel<F, OUT, 8>, q, c, s, cu, S, first, out, lse, ctl, H, T,
                               window, scale);
   }
+  shape(BandSmem<F, 16>::kHeads);
   cfg.dynamicSmemBytes = band_smem_bytes<F, 16>();
   return cudaLaunchKernelEx(&cfg, pk_attend_band_kernel<F, OUT, 16>, q, c, s, cu, S, first, out, lse, ctl, H, T,
                             window, scale);

@@ -224,7 +224,7 @@ struct Params {
   const uint16_t* sin_t;
   const uint32_t* cu;
   const TileRec* tiles;
-  uint16_t* out;
+  void* out;    // 16-bit of the element type, or fp32 (OUT32)
   float* lse;
   Ctl* ctl;
   int H;
@@ -235,6 +235,7 @@ struct Params {
   unsigned long long timeout_ns;
   int skip_first_item_arrive;  // test hook: the producer withholds its first item hand-off
   int singles;                 // 1: a work item is one tile record (no B), 0: a pair of records
+  int prerotated;              // 1: q and k arrive rotated (and q multiplied): no rotation here
 };
 
 // The member sequence offsets cu[rec.seq .. rec.seq + rec.nseq] of a record, copied by the
@@ -668,7 +669,7 @@ __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
     // the first job's table rows
     {
       const bool ok0 = qok_a;
-      if (ok0) fetch_table_row(p, tbl0 + buf * kRowTblBytes, qpos_a, t);
+      if (ok0 && !p.prerotated) fetch_table_row(p, tbl0 + buf * kRowTblBytes, qpos_a, t);
       cp_async_commit();
     }
 #pragma unroll 1
@@ -708,14 +709,14 @@ __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
         } else {
           ok_n = krow(i + 1 - nq, pos_n);
         }
-        if (ok_n) fetch_table_row(p, tbl0 + (buf ^ 1u) * kRowTblBytes, pos_n, t);
+        if (ok_n && !p.prerotated) fetch_table_row(p, tbl0 + (buf ^ 1u) * kRowTblBytes, pos_n, t);
       }
       cp_async_commit();
       cp_async_wait1();  // this job's rows have landed (the next one's may still be in flight)
       bad |= !wait_bar(meta, p.ctl, full, phase, p.timeout_ns);
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
-      if (ok) rope_row<BF16>(tile, t, tblp + buf * kRowTblBytes, t, isq ? p.q_mul : 1.0f);
+      if (ok && !p.prerotated) rope_row<BF16>(tile, t, tblp + buf * kRowTblBytes, t, isq ? p.q_mul : 1.0f);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(ready));
@@ -742,7 +743,7 @@ __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
 // is voted across the warp before any warp-collective TMEM access, so a warp leaves
 // together.
 
-template <bool BF16>
+template <bool BF16, bool OUT32>
 __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
   Bars& B = meta->bars;
   const int tid = threadIdx.x;
@@ -926,13 +927,21 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
     tc_fence_before();
     if (row_ok) {
       const float inv = 1.0f / l;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(a) * hd + h * kD));
+      if constexpr (OUT32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + (static_cast<int64_t>(a) * hd + h * kD));
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        dst[q] = make_uint4(Elem<BF16>::pack(ov[8 * q + 0] * inv, ov[8 * q + 1] * inv),
-                            Elem<BF16>::pack(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv),
-                            Elem<BF16>::pack(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
-                            Elem<BF16>::pack(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
+        for (int q = 0; q < 16; ++q)
+          dst[q] = make_float4(ov[4 * q + 0] * inv, ov[4 * q + 1] * inv, ov[4 * q + 2] * inv, ov[4 * q + 3] * inv);
+      } else {
+        uint4* dst =
+            reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(a) * hd + h * kD));
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_uint4(Elem<BF16>::pack(ov[8 * q + 0] * inv, ov[8 * q + 1] * inv),
+                              Elem<BF16>::pack(ov[8 * q + 2] * inv, ov[8 * q + 3] * inv),
+                              Elem<BF16>::pack(ov[8 * q + 4] * inv, ov[8 * q + 5] * inv),
+                              Elem<BF16>::pack(ov[8 * q + 6] * inv, ov[8 * q + 7] * inv));
+      }
       p.lse[static_cast<int64_t>(h) * p.T + a] = (m_ref * k2 + lg2(l)) * kLn2;
     }
   }
@@ -941,7 +950,7 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
 
 }  // namespace
 
-template <bool BF16>
+template <bool BF16, bool OUT32>
 __global__ void __launch_bounds__(kThreads, 1)
 pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -1015,7 +1024,7 @@ pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_c
     rotator<BF16>(p, smem, meta, tid - kWarpRot * 32);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
-    softmax_wg<BF16>(p, meta, (warp - kWarpSm) >> 2, meta->tmem);
+    softmax_wg<BF16, OUT32>(p, meta, (warp - kWarpSm) >> 2, meta->tmem);
   }
 
   tc_fence_before();
@@ -1029,17 +1038,22 @@ pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_c
 uint32_t attend_tc_smem_bytes() { return kSmemUsed + 1024; }
 
 // Host side: opt in to the dynamic shared memory once per device.
+template <bool BF16, bool OUT32>
+cudaError_t attend_tc_attrs(int smem) {
+  cudaError_t e =
+      cudaFuncSetAttribute(pk_attend_tc_kernel<BF16, OUT32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pk_attend_tc_kernel<BF16, OUT32>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
 cudaError_t attend_tc_prepare() {
   const int smem = static_cast<int>(attend_tc_smem_bytes());
-  cudaError_t e = cudaFuncSetAttribute(pk_attend_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(pk_attend_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(pk_attend_tc_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(pk_attend_tc_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
+  cudaError_t e = attend_tc_attrs<true, false>(smem);
+  if (e == cudaSuccess) e = attend_tc_attrs<false, false>(smem);
+  if (e == cudaSuccess) e = attend_tc_attrs<true, true>(smem);
+  if (e == cudaSuccess) e = attend_tc_attrs<false, true>(smem);
   return e;
 }
 
@@ -1048,13 +1062,13 @@ cudaError_t attend_tc_prepare() {
 cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
                              const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
                              long long T, int window, float scale, unsigned long long timeout_ns, int grid,
-                             bool singles, cudaStream_t stream) {
+                             bool singles, bool out32, bool prerotated, cudaStream_t stream) {
   Params p;
   p.cos_t = static_cast<const uint16_t*>(cos_t);
   p.sin_t = static_cast<const uint16_t*>(sin_t);
   p.cu = cu;
   p.tiles = tiles;
-  p.out = static_cast<uint16_t*>(out);
+  p.out = out;
   p.lse = lse;
   p.ctl = ctl;
   p.H = H;
@@ -1066,6 +1080,7 @@ cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos
   p.s_mul = scale > 0.0f ? scale : 1.0f;
   p.timeout_ns = timeout_ns;
   p.singles = singles ? 1 : 0;
+  p.prerotated = prerotated ? 1 : 0;
   // test hook for the bounded waits (PK_DEBUG_SKIP_ARRIVE=1): every CTA's producer withholds
   // its first work-item hand-off, so the consumers' waits run out and the call ends with
   // PK_ERR_TIMEOUT in the stream's status word; nothing faults and the context stays usable
@@ -1085,8 +1100,12 @@ cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (bf16) return cudaLaunchKernelEx(&cfg, pk_attend_tc_kernel<true>, tmap, p);
-  return cudaLaunchKernelEx(&cfg, pk_attend_tc_kernel<false>, tmap, p);
+  if (out32) {
+    if (bf16) return cudaLaunchKernelEx(&cfg, pk_attend_tc_kernel<true, true>, tmap, p);
+    return cudaLaunchKernelEx(&cfg, pk_attend_tc_kernel<false, true>, tmap, p);
+  }
+  if (bf16) return cudaLaunchKernelEx(&cfg, pk_attend_tc_kernel<true, false>, tmap, p);
+  return cudaLaunchKernelEx(&cfg, pk_attend_tc_kernel<false, false>, tmap, p);
 }
 
 }  // namespace pk

@@ -29,7 +29,10 @@ cudaError_t backward_launch(int dtype, const void* qkv, const void* cos_t, const
 cudaError_t attend_tc_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
                              const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
                              long long T, int window, float scale, unsigned long long timeout_ns, int grid,
-                             bool singles, cudaStream_t stream);
+                             bool singles, bool out32, bool prerotated, cudaStream_t stream);
+cudaError_t rotate16_launch(int op_dtype, const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu,
+                            int S, long long T, int H, float q_mul, const Ctl* ctl, void* y, int sms,
+                            cudaStream_t stream);
 cudaError_t attend_q4_prepare();
 cudaError_t attend_q4_launch(bool bf16, const CUtensorMap& tmap, const void* cos_t, const void* sin_t,
                              const uint32_t* cu, const TileRec* tiles, void* out, float* lse, Ctl* ctl, int H,
@@ -58,6 +61,8 @@ struct Workspace {
   int64_t room = 0;  // tokens the workspace is sized for
   float* bwd = nullptr;    // the backward pass's fp32 scratch (allocated on its first use)
   int64_t bwd_floats = 0;
+  void* ops16 = nullptr;   // pk_attend_mixed_ops: the rotated 16-bit copy of qkv (first use)
+  int64_t ops16_bytes = 0;
 };
 
 struct DeviceInfo {
@@ -198,6 +203,7 @@ int workspace(int dev, cudaStream_t stream, int64_t T, Workspace** out) {
       return PK_ERR_CUDA;
     cudaFree(ws.base);
     if (ws.bwd) cudaFree(ws.bwd);
+    if (ws.ops16) cudaFree(ws.ops16);
     ws = Workspace();
   }
   int64_t room = T < 65536 ? 65536 : T;
@@ -386,6 +392,76 @@ int backward_scratch(Workspace* ws, cudaStream_t stream, int64_t floats) {
   return PK_OK;
 }
 
+// the rotated 16-bit copy of qkv of a workspace, grown to `bytes` (caller holds g_mu)
+int ops16_scratch(Workspace* ws, cudaStream_t stream, int64_t bytes) {
+  if (ws->ops16 && ws->ops16_bytes >= bytes) return PK_OK;
+  cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap_status) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_CUDA;
+  }
+  if (cap_status != cudaStreamCaptureStatusNone) return PK_ERR_CAPTURE;
+  if (ws->ops16) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PK_ERR_CUDA;
+    cudaFree(ws->ops16);
+    ws->ops16 = nullptr;
+    ws->ops16_bytes = 0;
+  }
+  const int64_t want = bytes + bytes / 4;
+  void* p = nullptr;
+  if (cudaMalloc(&p, static_cast<size_t>(want)) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_NOMEM;
+  }
+  ws->ops16 = p;
+  ws->ops16_bytes = want;
+  return PK_OK;
+}
+
+// fp32 storage, 16-bit operands: the scheduler, the rotated 16-bit copy, then the paired
+// tensor-core kernel on that copy (no rotation of its own) with an fp32 output
+int attend_mixed_ops(int op_dtype, const float* qkv, const float* cos, const float* sin, const uint32_t* cu, int S,
+                     int64_t T, int H, int window, float scale, float* out, float* lse, cudaStream_t stream) {
+  if (op_dtype != PK_BF16 && op_dtype != PK_F16) return PK_ERR_ARG;
+  int rc = check_args(PK_F32, qkv, cos, sin, cu, S, T, H, window, out, lse);
+  if (rc != PK_OK || T == 0) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PK_ERR_CUDA;
+  DeviceInfo* di = nullptr;
+  if ((rc = device_info(dev, &di)) != PK_OK) return rc;
+  Workspace* ws = nullptr;
+  if ((rc = workspace(dev, stream, T, &ws)) != PK_OK) return rc;
+  const int64_t elems = static_cast<int64_t>(T) * 3 * H * kD;
+  if ((rc = ops16_scratch(ws, stream, elems * 2)) != PK_OK) return rc;
+  cudaEvent_t* ev = nullptr;
+  if (g_prof.on && g_prof.dev == dev && g_prof.used < g_prof.cap) ev = g_prof.ev + 3 * g_prof.used++;
+  if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return PK_ERR_CUDA;
+  if ((rc = launch_schedule(cu, S, T, window, ws, stream)) != PK_OK) return rc;
+  // a positive scale multiplies the scores in the attention kernel; any other the rotated q here
+  if (rotate16_launch(op_dtype, qkv, cos, sin, cu, S, static_cast<long long>(T), H, scale > 0.0f ? 1.0f : scale,
+                      ws->ctl, ws->ops16, di->sms, stream) != cudaSuccess)
+    return PK_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return PK_ERR_CUDA;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return PK_ERR_CUDA;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(3) * H * kD, static_cast<cuuint64_t>(T)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(3) * H * kD * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBR)};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&tmap, op_dtype == PK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ws->ops16,
+          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PK_ERR_CUDA;
+  if (attend_tc_launch(op_dtype == PK_BF16, tmap, cos, sin, cu, ws->tiles, out, lse, ws->ctl, H,
+                       static_cast<long long>(T), window, scale, timeout_ns(), di->sms, false, true, true,
+                       stream) != cudaSuccess)
+    return PK_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return PK_ERR_CUDA;
+  return PK_OK;
+}
+
 int attend_backward(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S,
                     int64_t T, int H, int window, float scale, const void* out, const float* lse, const void* dout,
                     void* dqkv, cudaStream_t stream) {
@@ -453,7 +529,7 @@ int forward_launch(int kernel, int dtype, int out_dtype, const void* qkv, const 
                            sms, stream);
     else
       e = attend_tc_launch(dtype == PK_BF16, tmap, cos, sin, cu, tiles, out, lse, ctl, H, T, window, scale, timeout,
-                           sms, kernel == kKernelTcSingle, stream);
+                           sms, kernel == kKernelTcSingle, false, false, stream);
   }
   if (e != cudaSuccess) return PK_ERR_CUDA;
   if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return PK_ERR_CUDA;
@@ -475,6 +551,11 @@ int pk_attend_mixed(int out_dtype, const float* qkv, const float* cos, const flo
                     int64_t T, int H, int window, float scale, void* out, float* lse, struct CUstream_st* stream) {
   if (out_dtype != PK_F32 && out_dtype != PK_BF16 && out_dtype != PK_F16) return PK_ERR_ARG;
   return attend(PK_F32, out_dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
+}
+
+int pk_attend_mixed_ops(int op_dtype, const float* qkv, const float* cos, const float* sin, const uint32_t* cu, int S,
+                        int64_t T, int H, int window, float scale, float* out, float* lse, struct CUstream_st* stream) {
+  return attend_mixed_ops(op_dtype, qkv, cos, sin, cu, S, T, H, window, scale, out, lse, stream);
 }
 
 int pk_attend_backward(int dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S,
@@ -682,6 +763,7 @@ int pk_release(void) {
     }
     cudaFree(kv.second.base);
     if (kv.second.bwd) cudaFree(kv.second.bwd);
+    if (kv.second.ops16) cudaFree(kv.second.ops16);
   }
   g_ws.clear();
   cudaSetDevice(cur);

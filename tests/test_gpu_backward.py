@@ -48,3 +48,28 @@ def test_backward_parity(pk, orc, dt, case):
         err = float(np.max(np.abs(got[:, a] - want[:, a])))
         ref = float(np.max(np.abs(want[:, a])))
         assert err <= REL[dt] * max(ref, 1e-3), f"{nm}: max|delta| {err:.3e}, max|ref| {ref:.3e}"
+
+
+def test_backward_global_config_full_size(pk, orc):
+    """The encoder-base global layer (64 sequences of 32..512 tokens, H = 12, bf16) at full size:
+    every element of dq, dk, dv against the fp64 gradient."""
+    import torch
+
+    wl = synth.make_config("global")
+    H = wl.H
+    qkv, cos, sin, cu = device_inputs(wl)
+    out, lse = pk.attend(qkv, cos, sin, cu, H, 0, wl.scale)
+    rng = np.random.default_rng(11)
+    dout_np = synth.to_storage(rng.standard_normal((wl.T, H * 64)).astype(np.float32), "bf16")
+    dout = to_device(dout_np, "bf16")
+    dqkv = pk.attend_backward(qkv, cos, sin, cu, H, 0, wl.scale, out, lse, dout)
+    torch.cuda.synchronize()
+    assert pk.last_status() == 0
+    got = out_to_f64(dqkv)
+    want = orc.attend_backward(wl.qkv, wl.cos, wl.sin, wl.cu, H, 0, wl.scale, dout_np, dtype="bf16")
+    assert np.all(np.isfinite(got))
+    for part, nm in ((0, "dq"), (1, "dk"), (2, "dv")):
+        a = slice(part * H * 64, (part + 1) * H * 64)
+        err = float(np.max(np.abs(got[:, a] - want[:, a])))
+        ref = float(np.max(np.abs(want[:, a])))
+        assert err <= REL["bf16"] * max(ref, 1e-3), f"{nm}: max|delta| {err:.3e}, max|ref| {ref:.3e}"
