@@ -236,7 +236,7 @@ def device_tensors(wl, torch, dev):
     return t(wl.qkv), t(wl.cos), t(wl.sin), torch.from_numpy(wl.cu.astype(np.int64).astype(np.int32)).to(dev)
 
 
-def run_gpu(wl, steps, warmup, rank, world, dev_index):
+def run_gpu(wl, steps, warmup, rank, world, dev_index, tuned=True):
     import torch
 
     import rope_cu_tile_gb300 as pk
@@ -261,7 +261,7 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
     def step(i):
         q, o, l = sets[i % nsets]
         pk.attend(q, cos, sin, cu, wl.H, wl.window, wl.scale, out=o, lse=l, stream=stream, max_len=max_len,
-                  tuned=True)
+                  tuned=tuned)
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -269,7 +269,8 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
     torch.cuda.synchronize()
     if pk.last_status(stream) != 0:
         raise RuntimeError("device error during warm-up")
-    kernel = pk.pk_tune_pick(pk.dtype_code(qkv0), wl.H, wl.window, wl.T, max_len)
+    kernel = (pk.pk_tune_pick(pk.dtype_code(qkv0), wl.H, wl.window, wl.T, max_len) if tuned
+              else pk.pk_forward_kernel(pk.dtype_code(qkv0), wl.window))
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -336,11 +337,16 @@ def run_gpu(wl, steps, warmup, rank, world, dev_index):
             b["copied"].record(s_in)
         stream.wait_event(b["copied"])
         stream.wait_event(b["read"])  # its results of two steps ago have been read out
-        rc = pk.pk_attend_tuned(code, b["qkv"].data_ptr(), b["cos"].data_ptr(), b["sin"].data_ptr(),
-                                b["cu"].data_ptr(), wl.S, wl.T, wl.H, wl.window, float(wl.scale), max_len,
-                                b["out"].data_ptr(), b["lse"].data_ptr(), sh)
+        if tuned:
+            rc = pk.pk_attend_tuned(code, b["qkv"].data_ptr(), b["cos"].data_ptr(), b["sin"].data_ptr(),
+                                    b["cu"].data_ptr(), wl.S, wl.T, wl.H, wl.window, float(wl.scale), max_len,
+                                    b["out"].data_ptr(), b["lse"].data_ptr(), sh)
+        else:
+            rc = pk.pk_attend_dt(code, b["qkv"].data_ptr(), b["cos"].data_ptr(), b["sin"].data_ptr(),
+                                 b["cu"].data_ptr(), wl.S, wl.T, wl.H, wl.window, float(wl.scale),
+                                 b["out"].data_ptr(), b["lse"].data_ptr(), sh)
         if rc:
-            raise RuntimeError(f"pk_attend_tuned -> {rc}")
+            raise RuntimeError(f"forward call -> {rc}")
         b["computed"].record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(b["computed"])
@@ -483,6 +489,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="long", choices=list(synth.CONFIG_NAMES))
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "tc_single", "q4"],
+                    help="auto: pk_attend_tuned picks (default); otherwise pk_attend with that tensor-core "
+                         "kernel (windows of 1..16 always run the band kernel)")
     ap.add_argument("--op", default="attend", choices=["attend", "rope", "backward"],
                     help="attend: the attention path (default); rope: the standalone rotation; "
                          "backward: pk_attend_backward")
@@ -569,7 +578,9 @@ def main():
         import torch.distributed as dist
         import torch
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    r = run_gpu(wl, args.steps, args.warmup, rank, world, local)
+    if args.kernel != "auto":
+        os.environ["PK_ATTN"] = args.kernel
+    r = run_gpu(wl, args.steps, args.warmup, rank, world, local, tuned=args.kernel == "auto")
     peaks, psrc = load_peaks()
     value = world * flops / (r["ms_per_step"] * 1e-3) / 1e12
     tokens_s = world * wl.T / (r["ms_per_step"] * 1e-3)
@@ -579,7 +590,8 @@ def main():
             "tokens_per_s": tokens_s,
             "roofline": roofline(wl, r["attend_ms"], peaks, psrc, r["kernel"]),
             "kernel": {"picked": KERNEL_NAMES.get(r["kernel"], str(r["kernel"])),
-                       "by": "pk_attend_tuned (timed once per shape key during warm-up)"},
+                       "by": ("pk_attend_tuned (timed once per shape key during warm-up)" if args.kernel == "auto"
+                              else f"--kernel {args.kernel}")},
             "step_roofline_frac": (max(abytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
                                    / (r["ms_per_step"] * 1e-3)),
             "kernel_ms": {"preparation (tile scheduler or cu check)": r["schedule_ms"], "attention": r["attend_ms"],

@@ -141,9 +141,9 @@ int pk_attend_dt(int dtype, const void *qkv, const void *cos, const void *sin,
  *     inputs of large magnitude in tolerance), PK_KERNEL_F32 for other fp32 calls, and
  *     PK_KERNEL_TC, PK_KERNEL_TC_SINGLE and PK_KERNEL_Q4 for other bf16 / fp16 calls.
  *   - A key met for the first time with more than one usable kernel is tuned on the call's
- *     own arguments: each kernel runs once untimed and three times between two events on
- *     `stream`, the host waiting for the second event; the output is then that of one more
- *     run of the winner. Such a first call synchronizes the stream and cannot be captured in
+ *     own arguments: each kernel runs once untimed, then three rounds time two runs of each
+ *     kernel in turn between two events on `stream` (the host waiting for the second); a
+ *     kernel's time is its best round. The output is then that of one more run of the winner. Such a first call synchronizes the stream and cannot be captured in
  *     a CUDA graph (it returns PK_ERR_CAPTURE, nothing launched); later calls with the key
  *     are asynchronous. The cache lives until pk_tune_clear() or the end of the process.
  *   - Errors as pk_attend; longest < 0 gives PK_ERR_ARG.

@@ -14,15 +14,15 @@
 // storage type), which also keeps fp16 inputs of large magnitude inside their tolerance.
 //
 // Launch: one CTA per block of 32 tokens and group of four, two or one heads (one warp per
-// head: as many as let two CTAs share an SM). Every global read is an asynchronous copy into shared memory, all of a CTA's in
-// flight at once: each warp's raw q, k and v rows of its head over the staged tokens
-// [t0 - W, t0 + 32 + W), and the CTA's cos / sin rows of those tokens' positions. Then a
-// warp rotates its k rows to fp32 (rows padded so that consecutive rows start four banks
-// apart) and lane l takes query row t0 + l: q' in registers, the 2 w + 1 scores (kept in
-// shared memory), the softmax, and 64 fp32 output accumulators. The sequence of every staged
-// token comes from the offsets cu[s0 ..] staged once per CTA, s0 being the sequence of the
-// block's first staged token; pk_band_prep_kernel (launched just before, on the same stream)
-// checks cu and writes s0 for every block.
+// head: as many as let two CTAs share an SM). Every global read is an asynchronous copy into
+// shared memory, all of a CTA's in flight at once: each warp's raw q, k and v rows of its head
+// over the staged tokens [t0 - W, t0 + 32 + W), and the CTA's cos / sin rows of those tokens'
+// positions. A warp then rotates its k rows to fp32 in place and computes its 32 query rows in
+// register tiles (R rows x 16 features a lane, so that each key and value granule it loads
+// serves up to R rows; see the kernel). The sequence of every staged token comes from the
+// offsets cu[s0 ..] staged once per CTA, s0 being the sequence of the block's first staged
+// token; pk_band_prep_kernel (launched just before, on the same stream) checks cu and writes s0
+// for every block.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -41,55 +41,29 @@ template <typename F>
 struct Store;
 template <>
 struct Store<float> {
-  static constexpr int kVStride = 68;  // elements per staged v row
   __device__ static __forceinline__ float to_f(float x) { return x; }
 };
 template <>
 struct Store<__nv_bfloat16> {
-  static constexpr int kVStride = 72;  // 144 bytes: rows 4 banks apart
   __device__ static __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 };
 template <>
 struct Store<__half> {
-  static constexpr int kVStride = 72;
   __device__ static __forceinline__ float to_f(__half x) { return __half2float(x); }
 };
 
-// 8 stored elements (16 bytes for 16-bit types, two 16-byte loads for fp32) as fp32
-template <typename F>
-__device__ __forceinline__ void load8(const F* p, float (&x)[8]) {
-  if constexpr (sizeof(F) == 4) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  } else {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-    const F* e = reinterpret_cast<const F*>(&u);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) x[k] = Store<F>::to_f(e[k]);
-  }
-}
-
 template <int OUT>
-__device__ __forceinline__ void store8(void* out, int64_t at, const float (&y)[8]) {
+__device__ __forceinline__ void store4(void* out, int64_t at, float y0, float y1, float y2, float y3) {
   if constexpr (OUT == PK_F32) {
-    float4* d = reinterpret_cast<float4*>(static_cast<float*>(out) + at);
-    d[0] = make_float4(y[0], y[1], y[2], y[3]);
-    d[1] = make_float4(y[4], y[5], y[6], y[7]);
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + at) = make_float4(y0, y1, y2, y3);
+  } else if constexpr (OUT == PK_BF16) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(y0, y1), b = __floats2bfloat162_rn(y2, y3);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + at) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
   } else {
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if constexpr (OUT == PK_BF16) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * k], y[2 * k + 1]);
-        w[k] = *reinterpret_cast<const uint32_t*>(&h);
-      } else {
-        const __half2 h = __floats2half2_rn(y[2 * k], y[2 * k + 1]);
-        w[k] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-    }
-    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + at) = make_uint4(w[0], w[1], w[2], w[3]);
+    const __half2 a = __floats2half2_rn(y0, y1), b = __floats2half2_rn(y2, y3);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + at) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
   }
 }
 
@@ -149,34 +123,73 @@ __device__ __forceinline__ void band_cp16(void* dst, const void* src) {
 }
 
 // Shared-memory layout of a CTA (W: the instance's largest window; rows: 32 + 2 W staged
-// tokens; VS: elements per staged 16-bit or fp32 row, padded so rows start 4 banks apart):
-//   k'   [4][rows][68] fp32        rotated keys
-//   v    [4][rows][VS] stored      values
-//   q    [4][32][VS]   stored      raw queries (then the scores [4][2 W + 1][32] fp32)
-//   kraw [4][rows][VS] stored      raw keys
-//   tab  [rows][2][32] stored      cos and sin rows of each staged token's position
+// tokens; heads: one warp each):
+//   k'  [heads][rows][68] fp32     rotated keys (a 68-float row starts four banks after the
+//                                  one before); the raw 16-bit row is copied into its last 128
+//                                  bytes (byte 144 on) and rotated in place
+//   v   [heads][rows][VS] stored   values as stored (VS: 72 16-bit or 68 fp32 elements)
+//   q   [heads][32][VS]   stored   raw queries
+//   tab [rows][2][32]     stored   cos and sin rows of each staged token's position
 template <typename F, int W>
 struct BandSmem {
   static constexpr int kRows = kBandRows + 2 * W;
-  static constexpr int kVS = Store<F>::kVStride;
-  // bytes of one head's rows (k', v, q, raw k) and of the CTA's table rows
-  static constexpr size_t kPerHead = sizeof(float) * kRows * kKStride + sizeof(F) * kRows * kVS +
-                                     sizeof(F) * kBandRows * kVS + sizeof(F) * kRows * kVS;
+  static constexpr int kVS = sizeof(F) == 4 ? 68 : 72;
+  static constexpr size_t kRowBytes = sizeof(float) * kKStride;  // 272
+  static constexpr size_t kRawAt = sizeof(F) == 4 ? 0 : 144;     // raw 16-bit k row inside its fp32 row
+  static constexpr size_t kPerHead = kRows * kRowBytes + sizeof(F) * kRows * kVS + sizeof(F) * kBandRows * kVS;
   static constexpr size_t kTabBytes = sizeof(F) * kRows * 2 * kHalf;
   // heads per CTA (one warp each): four, two or one, whichever lets two CTAs share an SM
   static constexpr size_t kTwoPerSm = 113 * 1024;
   static constexpr int kHeads = 4 * kPerHead + kTabBytes <= kTwoPerSm ? 4 : 2 * kPerHead + kTabBytes <= kTwoPerSm ? 2 : 1;
   static constexpr size_t kK = 0;
-  static constexpr size_t kV = kK + sizeof(float) * kHeads * kRows * kKStride;
+  static constexpr size_t kV = kK + kHeads * kRows * kRowBytes;
   static constexpr size_t kQ = kV + sizeof(F) * kHeads * kRows * kVS;
-  static constexpr size_t kKraw = kQ + sizeof(F) * kHeads * kBandRows * kVS;
-  static constexpr size_t kTab = kKraw + sizeof(F) * kHeads * kRows * kVS;
+  static constexpr size_t kTab = kQ + sizeof(F) * kHeads * kBandRows * kVS;
   static constexpr size_t kBytes = kTab + kTabBytes;
   static_assert(kBytes <= 227 * 1024, "fits the shared memory a block may use");
-  static_assert(sizeof(float) * (2 * W + 1) * 32 <= sizeof(F) * kBandRows * kVS, "scores fit the q area");
+  static_assert(kRawAt + 128 <= kRowBytes, "a raw 16-bit row fits inside its fp32 row");
 };
 
+// 8 stored elements (16 bytes of a 16-bit type, 32 bytes of fp32) from shared memory, as fp32
+template <typename F>
+__device__ __forceinline__ void lds8(const F* p, float (&x)[8]) {
+  if constexpr (sizeof(F) == 4) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const F* e = reinterpret_cast<const F*>(&u);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = Store<F>::to_f(e[k]);
+  }
+}
+// 4 stored elements (8 bytes of a 16-bit type, 16 bytes of fp32) from shared memory, as fp32
+template <typename F>
+__device__ __forceinline__ void lds4(const F* p, float (&x)[4]) {
+  if constexpr (sizeof(F) == 4) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const F* e = reinterpret_cast<const F*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[k] = Store<F>::to_f(e[k]);
+  }
+}
+__device__ __forceinline__ void sts8(float* p, const float (&y)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(y[0], y[1], y[2], y[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(y[4], y[5], y[6], y[7]);
+}
+
 // W: the largest window this instance serves (4, 8 or 16); the call's window is 1 .. W.
+//
+// The products: lane (g, e) of a warp, g = lane / 4, e = lane % 4, takes R consecutive query
+// rows of its block (R = 4 for W <= 4, else 2; 8 R rows per pass) and 16 of the 64 features:
+// the 4-feature granules e, e + 4, e + 8, e + 12, which hold both members of their rotary
+// pairs (u, u + 32). Each key row it loads serves up to R of its rows: the partial scores
+// of its features are summed over the four lanes of the group by two shuffles, and its
+// share of out accumulates from the value granules of the same features.
 template <typename F, int OUT, int W>
 __global__ void __launch_bounds__(kBandRows * BandSmem<F, W>::kHeads)
 pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, const F* __restrict__ sin_t,
@@ -189,11 +202,12 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
   constexpr int kChunk = 16 / sizeof(F);          // elements per 16-byte chunk
   constexpr int kRowChunks = kD / kChunk;         // chunks per 64-element row
   constexpr int kTabChunks = kHalf / kChunk;      // chunks per 32-element table row
+  constexpr int R = W <= 4 ? 4 : 2;               // query rows per lane
+  constexpr int kKeys = R + 2 * W;                // key rows a lane's group reads
   extern __shared__ __align__(16) unsigned char band_smem[];
   auto s_k = reinterpret_cast<float (*)[kRowsSt][kKStride]>(band_smem + L::kK);
   auto s_v = reinterpret_cast<F (*)[kRowsSt][kVS]>(band_smem + L::kV);
   auto s_q = reinterpret_cast<F (*)[kBandRows][kVS]>(band_smem + L::kQ);
-  auto s_kr = reinterpret_cast<F (*)[kRowsSt][kVS]>(band_smem + L::kKraw);
   auto s_tab = reinterpret_cast<F (*)[2][kHalf]>(band_smem + L::kTab);
   __shared__ uint32_t s_cu[kBandCu + 1];
   __shared__ int s_ncu;
@@ -206,6 +220,7 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
   const long long base = t0 - W;  // token of staged row 0
   const int h = blockIdx.y * L::kHeads + warp;
   const int64_t ldq = 3ll * H * kD;
+  auto raw_k = [&](int r) { return reinterpret_cast<F*>(reinterpret_cast<unsigned char*>(s_k[warp][r]) + L::kRawAt); };
   // the offsets were checked (and `first` written) by the kernel launched just before
   griddep_wait();
   if (__ldcg(&ctl->ntiles) == 0u) return;
@@ -215,7 +230,7 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
     for (int i = lane; i < kRowsSt * kRowChunks; i += 32) {
       const int r = i / kRowChunks, c = i % kRowChunks;
       const long long a = base + r;
-      F* kd = s_kr[warp][r] + c * kChunk;
+      F* kd = raw_k(r) + c * kChunk;
       F* vd = s_v[warp][r] + c * kChunk;
       if (a >= 0 && a < T) {
         const F* row = qkv + a * ldq;
@@ -278,113 +293,161 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
   __syncthreads();
   if (h >= H) return;
 
-  // k' = rot(k) in fp32: four lanes per row, lane chunk c < 4 holding elements 8 c .. 8 c + 7
-  // of each half (the rotary pairs (u, u + 32))
-  for (int i = lane; i < kRowsSt * 4; i += 32) {
-    const int r = i >> 2, c = i & 3;
-    const F* kr = s_kr[warp][r];
-    const F* tc = s_tab[r][0];
-    const F* ts = s_tab[r][1];
-    float* kd = s_k[warp][r];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int u = 8 * c + e;
-      const float x1 = Store<F>::to_f(kr[u]), x2 = Store<F>::to_f(kr[u + kHalf]);
-      const float cc = Store<F>::to_f(tc[u]), ss = Store<F>::to_f(ts[u]);
-      kd[u] = x1 * cc - x2 * ss;
-      kd[u + kHalf] = x1 * ss + x2 * cc;
+  // k' = rot(k) in fp32, in place: a row's raw elements are all read (by the four lanes that
+  // share it: chunk pair c < 4 holds elements 8 c .. 8 c + 7 of each half) before any of its
+  // fp32 values are written
+#pragma unroll 1
+  for (int r0 = 0; r0 < kRowsSt; r0 += 8) {
+    const int r = r0 + (lane >> 2), c = lane & 3;
+    float x1[8], x2[8], tc[8], ts[8];
+    const bool in = r < kRowsSt;
+    if (in) {
+      lds8(raw_k(r) + 8 * c, x1);
+      lds8(raw_k(r) + 8 * c + kHalf, x2);
+      lds8(&s_tab[r][0][8 * c], tc);
+      lds8(&s_tab[r][1][8 * c], ts);
     }
-  }
-  // this lane's query row: q' = rot(q, pos) * scale in fp32
-  const long long a = t0 + lane;
-  const bool row_ok = a < T;
-  float q[kD];
-  int lo = 0, hi = 0;
-  {
-    const int r = lane + W;
-    const F* qr = s_q[warp][lane];
-    const F* tc = s_tab[r][0];
-    const F* ts = s_tab[r][1];
+    __syncwarp();
+    if (in) {
+      float y1[8], y2[8];
 #pragma unroll
-    for (int u = 0; u < kHalf; ++u) {
-      const float x1 = Store<F>::to_f(qr[u]), x2 = Store<F>::to_f(qr[u + kHalf]);
-      const float cc = Store<F>::to_f(tc[u]), ss = Store<F>::to_f(ts[u]);
-      q[u] = (x1 * cc - x2 * ss) * scale;
-      q[u + kHalf] = (x1 * ss + x2 * cc) * scale;
-    }
-    if (row_ok) {
-      lo = max(s_seq_lo[r], static_cast<int>(a) - window);
-      hi = min(s_seq_hi[r], static_cast<int>(a) + window + 1);
+      for (int k = 0; k < 8; ++k) {
+        y1[k] = x1[k] * tc[k] - x2[k] * ts[k];
+        y2[k] = x1[k] * ts[k] + x2[k] * tc[k];
+      }
+      sts8(s_k[warp][r] + 8 * c, y1);
+      sts8(s_k[warp][r] + 8 * c + kHalf, y2);
     }
   }
   __syncwarp();
 
-  // scores of the keys a - W .. a + W (staged rows lane .. lane + 2 W), kept per lane in shared
-  // memory; invisible ones -inf. The key loops stay rolled (a small register footprint).
-  // (the raw q rows are read: their area holds the scores now)
-  float* sc = reinterpret_cast<float*>(s_q[warp]) + lane;  // score d of this lane at sc[32 d]
-  float m = -INFINITY;
+  const int g = lane >> 2, e = lane & 3;
+  // the lane's 16 features: granules e, e + 4 (first half of the rotary pairs), e + 8, e + 12
+  // (their partners); q' and the key granules are held in that order
 #pragma unroll 1
-  for (int d = 0; d <= 2 * W; ++d) {
-    const long long j = a - W + d;
-    const float* kr = s_k[warp][lane + d];
-    float acc0 = 0.f, acc1 = 0.f;
+  for (int rb = R * g; rb < kBandRows; rb += 8 * R) {
+    // q' of the lane's rows, its features, in fp32
+    float qv[R][16];
 #pragma unroll
-    for (int u = 0; u < kD; u += 8) {
-      const float4 x = *reinterpret_cast<const float4*>(kr + u);
-      const float4 y = *reinterpret_cast<const float4*>(kr + u + 4);
-      acc0 = fmaf(q[u], x.x, acc0);
-      acc1 = fmaf(q[u + 1], x.y, acc1);
-      acc0 = fmaf(q[u + 2], x.z, acc0);
-      acc1 = fmaf(q[u + 3], x.w, acc1);
-      acc0 = fmaf(q[u + 4], y.x, acc0);
-      acc1 = fmaf(q[u + 5], y.y, acc1);
-      acc0 = fmaf(q[u + 6], y.z, acc0);
-      acc1 = fmaf(q[u + 7], y.w, acc1);
+    for (int i = 0; i < R; ++i) {
+      const int row = rb + i, r = row + W;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float x1[4], x2[4], tc[4], ts[4];
+        const int u = 4 * (e + 4 * c);
+        lds4(s_q[warp][row] + u, x1);
+        lds4(s_q[warp][row] + u + kHalf, x2);
+        lds4(&s_tab[r][0][u], tc);
+        lds4(&s_tab[r][1][u], ts);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          qv[i][4 * c + k] = (x1[k] * tc[k] - x2[k] * ts[k]) * scale;
+          qv[i][8 + 4 * c + k] = (x1[k] * ts[k] + x2[k] * tc[k]) * scale;
+        }
+      }
     }
-    const float sv = (j >= lo && j < hi) ? acc0 + acc1 : -INFINITY;
-    sc[32 * d] = sv;
-    m = fmaxf(m, sv);
-  }
-  // softmax weights (a row past T has none) and the weighted sum of the visible values
-  float l = 0.f;
-  float o[kD];
+    // partial scores of the lane's features: row i against key rb + kk (d = kk - i)
+    float ps[R][2 * W + 1];
 #pragma unroll
-  for (int u = 0; u < kD; ++u) o[u] = 0.f;
-#pragma unroll 1
-  for (int d = 0; d <= 2 * W; ++d) {
-    const float p = row_ok ? __expf(sc[32 * d] - m) : 0.f;
-    l += p;
-    const F* vr = s_v[warp][lane + d];
+    for (int i = 0; i < R; ++i)
 #pragma unroll
-    for (int u = 0; u < kD; u += 8) {
-      float x[8];
-      if constexpr (sizeof(F) == 4) {
-        const float4 a4 = *reinterpret_cast<const float4*>(vr + u);
-        const float4 b4 = *reinterpret_cast<const float4*>(vr + u + 4);
-        x[0] = a4.x; x[1] = a4.y; x[2] = a4.z; x[3] = a4.w;
-        x[4] = b4.x; x[5] = b4.y; x[6] = b4.z; x[7] = b4.w;
-      } else {
-        const uint4 w4 = *reinterpret_cast<const uint4*>(vr + u);
-        const F* e = reinterpret_cast<const F*>(&w4);
+      for (int d = 0; d <= 2 * W; ++d) ps[i][d] = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = Store<F>::to_f(e[k]);
+    for (int kk = 0; kk < kKeys; ++kk) {
+      const float* kr = s_k[warp][rb + kk];
+      float kv[16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float4 x = *reinterpret_cast<const float4*>(kr + 4 * (e + 4 * c));
+        kv[4 * c] = x.x;
+        kv[4 * c + 1] = x.y;
+        kv[4 * c + 2] = x.z;
+        kv[4 * c + 3] = x.w;
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) o[u + k] = fmaf(p, x[k], o[u + k]);
-    }
-  }
-  if (row_ok) {
-    const float inv = 1.0f / l;
-    const int64_t at = a * static_cast<int64_t>(H) * kD + static_cast<int64_t>(h) * kD;
+      for (int i = 0; i < R; ++i) {
+        const int d = kk - i;
+        if (d >= 0 && d <= 2 * W) {
+          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int u = 0; u < kD; u += 8) {
-      float y[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) y[k] = o[u + k] * inv;
-      store8<OUT>(out, at + u, y);
+          for (int f = 0; f < 16; f += 2)
+            acc = __ffma2_rn(make_float2(qv[i][f], qv[i][f + 1]), make_float2(kv[f], kv[f + 1]), acc);
+          ps[i][d] = acc.x + acc.y;
+        }
+      }
     }
-    lse[static_cast<int64_t>(h) * T + a] = m + logf(l);
+    // whole scores (the four lanes of the group), the mask, the softmax
+    float l[R], m[R];
+    bool ok[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const long long a = t0 + rb + i;
+      ok[i] = a < T;
+      const int r = rb + i + W;
+      const int lo = ok[i] ? max(s_seq_lo[r], static_cast<int>(a) - window) : 0;
+      const int hi = ok[i] ? min(s_seq_hi[r], static_cast<int>(a) + window + 1) : 0;
+      m[i] = -INFINITY;
+#pragma unroll
+      for (int d = 0; d <= 2 * W; ++d) {
+        float x = ps[i][d];
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        const long long j = a - W + d;
+        x = (j >= lo && j < hi) ? x : -INFINITY;
+        ps[i][d] = x;
+        m[i] = fmaxf(m[i], x);
+      }
+      l[i] = 0.f;
+#pragma unroll
+      for (int d = 0; d <= 2 * W; ++d) {
+        const float pw = ok[i] ? __expf(ps[i][d] - m[i]) : 0.f;
+        ps[i][d] = pw;
+        l[i] += pw;
+      }
+    }
+    // out: the lane's features of each row, from the value granules of key rb + kk
+    float2 o[R][8];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+      for (int f = 0; f < 8; ++f) o[i][f] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int kk = 0; kk < kKeys; ++kk) {
+      float vv[16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float x[4];
+        lds4(s_v[warp][rb + kk] + 4 * (e + 4 * c), x);
+        vv[4 * c] = x[0];
+        vv[4 * c + 1] = x[1];
+        vv[4 * c + 2] = x[2];
+        vv[4 * c + 3] = x[3];
+      }
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const int d = kk - i;
+        if (d >= 0 && d <= 2 * W) {
+          const float2 p2 = make_float2(ps[i][d], ps[i][d]);
+#pragma unroll
+          for (int f = 0; f < 8; ++f) o[i][f] = __ffma2_rn(p2, make_float2(vv[2 * f], vv[2 * f + 1]), o[i][f]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      if (!ok[i]) continue;
+      const long long a = t0 + rb + i;
+      const float inv = 1.0f / l[i];
+      const int64_t at = a * static_cast<int64_t>(H) * kD + static_cast<int64_t>(h) * kD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        // granule e + 4 c: this lane's features 4 c .. 4 c + 3
+        const float y0 = o[i][2 * c].x * inv, y1 = o[i][2 * c].y * inv;
+        const float y2 = o[i][2 * c + 1].x * inv, y3 = o[i][2 * c + 1].y * inv;
+        store4<OUT>(out, at + 4 * (e + 4 * c), y0, y1, y2, y3);
+      }
+      if (e == 0) lse[static_cast<int64_t>(h) * T + a] = m[i] + logf(l[i]);
+    }
   }
 }
 
@@ -397,8 +460,13 @@ constexpr size_t band_smem_bytes() {
 
 template <typename F, int OUT, int W>
 cudaError_t band_attr() {
-  return cudaFuncSetAttribute(pk_attend_band_kernel<F, OUT, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(band_smem_bytes<F, W>()));
+  cudaError_t e = cudaFuncSetAttribute(pk_attend_band_kernel<F, OUT, W>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(band_smem_bytes<F, W>()));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pk_attend_band_kernel<F, OUT, W>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
 }
 
 template <typename F, int OUT>
