@@ -169,7 +169,6 @@ struct Ring {
   __device__ __forceinline__ uint32_t phase(uint32_t depth) const { return (n / depth) & 1u; }
 };
 
-__device__ __forceinline__ uint32_t round16(uint32_t n) { return (n + 15u) & ~15u; }
 
 // The key stream of an item, as every role keeps it in registers.
 struct Stream {
@@ -485,6 +484,11 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, uint8_t* smem
 
 __device__ void mma_issuer(const Params& p, uint8_t* smem, Meta* meta, uint32_t tmem, bool bf16, int x) {
   Bars& B = meta->bars;
+  // Every S product is 128 keys wide and every PV product runs over all 128 keys of its tile:
+  // the columns past a tile's keys are masked scores and zero probabilities, so the extra
+  // work changes no result, and the issue sequence carries no per-tile arithmetic or branch
+  // (an MMA issued behind scalar code waits for it: a fixed sequence keeps the tensor pipe fed).
+  const uint32_t idesc_s = idesc_f16(bf16, 128, 128, false, false);
   const uint32_t idesc_pv = idesc_f16(bf16, 128, 64, false, true);
   // operand descriptors of the first buffer of each kind; a K step of 16 adds 32 bytes (Q,
   // K) or 2048 bytes (V) to the start address field (address >> 4), and the next 16 KB tile
@@ -495,22 +499,21 @@ __device__ void mma_issuer(const Params& p, uint8_t* smem, Meta* meta, uint32_t 
   const uint32_t tS = tmem + col_s(x), tP = tmem + col_p(x), tO = tmem + col_o(x);
   uint32_t it = 0, sc = 0, pr = 0, qn = 0;
   bool pend = false;  // an S_X was issued whose reading has not been awaited yet
-  Ring k, v;
+  uint32_t kst = 0, kph = 0, vst = 0, vph = 0;  // ring stage and phase of the next K, V tile
   bool bad = false;
 
   for (;;) {
     const uint32_t mb = it & 1u;
     if (!wait_bar(meta, p.ctl, &B.item_full[mb], (it >> 1) & 1u, p.timeout_ns)) break;
     const bool valid = meta->box[mb].valid != 0;
-    const Stream sm = stream_of(meta->box[mb]);
+    const uint32_t n = meta->box[mb].nstream;
+    const uint32_t lo = x == 0 ? 0u : meta->box[mb].b0, hi = x == 0 ? meta->box[mb].a1 : meta->box[mb].b1;
     mbar_arrive(smem_u32(&B.item_empty[mb]));
     ++it;
     if (!valid) break;
-    const uint32_t lo = x == 0 ? 0u : sm.b0, hi = x == 0 ? sm.a1 : sm.b1;
-    for (uint32_t t = 0; t <= sm.n && !bad; ++t) {
-      if (t < sm.n) {
-        const uint32_t st = k.stage(kKStages);
-        if (!wait_bar(meta, p.ctl, &B.k_ready[st], k.phase(kKStages), p.timeout_ns)) {
+    for (uint32_t t = 0; t <= n && !bad; ++t) {
+      if (t < n) {
+        if (!wait_bar(meta, p.ctl, &B.k_ready[kst], kph, p.timeout_ns)) {
           bad = true;
           break;
         }
@@ -528,27 +531,27 @@ __device__ void mma_issuer(const Params& p, uint8_t* smem, Meta* meta, uint32_t 
             ++sc;
           }
           tc_fence_after();
-          const uint32_t idesc = idesc_f16(bf16, 128, round16(stream_tile(sm, t).nkeys), false, false);
-          const uint64_t dq = dq0 + qb * 1024, dk = dk0 + st * 1024;
-          umma_f16_ss(tS, dq, dk, idesc, 0u);
-#pragma unroll
-          for (int ks = 1; ks < 4; ++ks) umma_f16_ss(tS, dq + ks * 2, dk + ks * 2, idesc, 1u);
+          const uint64_t dq = dq0 + qb * 1024, dk = dk0 + kst * 1024;
+          umma_f16_ss(tS, dq, dk, idesc_s, 0u);
+          umma_f16_ss(tS, dq + 2, dk + 2, idesc_s, 1u);
+          umma_f16_ss(tS, dq + 4, dk + 4, idesc_s, 1u);
+          umma_f16_ss(tS, dq + 6, dk + 6, idesc_s, 1u);
           umma_commit(smem_u32(&B.s_full[x]));
-          umma_commit(smem_u32(&B.k_empty[st]));
+          umma_commit(smem_u32(&B.k_empty[kst]));
           pend = true;
           if (t + 1 == hi) {
             umma_commit(smem_u32(&B.q_empty[x][qb]));
             ++qn;
           }
         } else {
-          mbar_arrive(smem_u32(&B.k_empty[st]));
+          mbar_arrive(smem_u32(&B.k_empty[kst]));
         }
-        ++k.n;
+        kst = (kst + 1) & (kKStages - 1);
+        kph ^= kst == 0 ? 1u : 0u;
       }
       if (t >= 1) {
         const uint32_t j = t - 1;
-        const uint32_t st = v.stage(kVStages);
-        if (!wait_bar(meta, p.ctl, &B.v_full[st], v.phase(kVStages), p.timeout_ns)) {
+        if (!wait_bar(meta, p.ctl, &B.v_full[vst], vph, p.timeout_ns)) {
           bad = true;
           break;
         }
@@ -559,18 +562,17 @@ __device__ void mma_issuer(const Params& p, uint8_t* smem, Meta* meta, uint32_t 
           }
           ++pr;
           tc_fence_after();
-          const uint32_t ksteps = round16(stream_tile(sm, j).nkeys) / 16;
-          const uint64_t dv = dv0 + st * 1024;
+          const uint64_t dv = dv0 + vst * 1024;
           umma_f16_ts(tO, tP, dv, idesc_pv, j > lo ? 1u : 0u);
 #pragma unroll
-          for (uint32_t ks = 1; ks < 8; ++ks)
-            if (ks < ksteps) umma_f16_ts(tO, tP + ks * 8, dv + ks * 128, idesc_pv, 1u);
+          for (uint32_t ks = 1; ks < 8; ++ks) umma_f16_ts(tO, tP + ks * 8, dv + ks * 128, idesc_pv, 1u);
           umma_commit(smem_u32(&B.pv_done[x]));
-          umma_commit(smem_u32(&B.v_empty[st]));
+          umma_commit(smem_u32(&B.v_empty[vst]));
         } else {
-          mbar_arrive(smem_u32(&B.v_empty[st]));
+          mbar_arrive(smem_u32(&B.v_empty[vst]));
         }
-        ++v.n;
+        vst = vst + 1 == kVStages ? 0u : vst + 1;
+        vph ^= vst == 0 ? 1u : 0u;
       }
     }
     if (bad) break;

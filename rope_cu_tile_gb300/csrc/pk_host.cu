@@ -285,6 +285,7 @@ TuneKey tune_key(int dev, int dtype, int H, int window, long long T, long long l
 // The kernels a call may run, fastest first unknown: narrow windows keep to the band kernel
 // (fp32 arithmetic: the tensor-core kernels round q' and k' to the element type, which costs
 // fp16 inputs of large magnitude their tolerance), fp32 inputs to the CUDA-core kernels.
+constexpr int kMaxCandidates = 3;  // the longest list tune_candidates writes
 int tune_candidates(int dtype, int window, int* c) {
   if (window >= 1 && window <= kBandMaxW) {
     c[0] = kKernelBand;
@@ -324,7 +325,7 @@ int attend_tuned(int dtype, const void* qkv, const void* cos, const void* sin, c
   if (it != g_tune.end()) {
     kernel = it->second;
   } else {
-    int cand[3];
+    int cand[kMaxCandidates];
     const int n = tune_candidates(dtype, window, cand);
     kernel = cand[0];
     if (n > 1) {
@@ -344,7 +345,7 @@ int attend_tuned(int dtype, const void* qkv, const void* cos, const void* sin, c
       // every candidate once untimed, then kTuneRounds rounds over the candidates in turn (so
       // that clock or cache drift during the tuning touches them alike), each timing two launches;
       // a candidate's time is its best round
-      float best_ms[3] = {0.f, 0.f, 0.f};
+      float best_ms[kMaxCandidates] = {};
       for (int i = 0; i < n && rc == PK_OK; ++i) rc = run(cand[i], nullptr);
       for (int round = 0; round < kTuneRounds && rc == PK_OK; ++round) {
         for (int i = 0; i < n && rc == PK_OK; ++i) {
