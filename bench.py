@@ -74,10 +74,11 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 KERNEL_NAMES = {0: "pk_attend_band_kernel", 1: "pk_attend_f32_kernel", 2: "pk_attend_tc_kernel",
-                3: "pk_attend_q4_kernel", 4: "pk_attend_tc_kernel (single-record items)"}
+                3: "pk_attend_q4_kernel", 4: "pk_attend_tc_kernel (single-record items)",
+                5: "pk_attend_split_kernel"}
 # the source file of each forward kernel (enum pk_kernel)
 KERNEL_SOURCES = {0: "pk_attend_band.cu", 1: "pk_attend_f32.cu", 2: "pk_attend_tc.cu", 3: "pk_attend_q4.cu",
-                  4: "pk_attend_tc.cu"}
+                  4: "pk_attend_tc.cu", 5: "pk_attend_split.cu"}
 
 
 def kernel_source_hash(kernel: int = 2) -> str:
@@ -489,9 +490,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="long", choices=list(synth.CONFIG_NAMES))
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "tc_single", "q4"],
-                    help="auto: pk_attend_tuned picks (default); otherwise pk_attend with that tensor-core "
-                         "kernel (windows of 1..16 always run the band kernel)")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "tc_single", "q4", "f32", "split"],
+                    help="auto: pk_attend_tuned picks (default); otherwise pk_attend with that kernel "
+                         "(tc, tc_single, q4: 16-bit inputs; f32, split: fp32 inputs; windows of 1..16 "
+                         "always run the band kernel)")
     ap.add_argument("--op", default="attend", choices=["attend", "rope", "backward"],
                     help="attend: the attention path (default); rope: the standalone rotation; "
                          "backward: pk_attend_backward")

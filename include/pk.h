@@ -29,7 +29,12 @@
  * Kernels and precision (enum pk_kernel; pk_forward_kernel says which one a call runs):
  *   - 1 <= window <= 16, any element type: PK_KERNEL_BAND, CUDA cores, every product and sum
  *     in fp32 from the stored values (a row sees at most 33 keys: the work is moving qkv).
- *   - otherwise fp32 inputs: PK_KERNEL_F32, CUDA cores, fp32.
+ *   - otherwise fp32 inputs: PK_KERNEL_F32, CUDA cores, fp32; or (PK_ATTN=split, or picked by
+ *     pk_attend_tuned) PK_KERNEL_SPLIT: q and k rotated in fp32, then every value of q', k', v
+ *     and of the probabilities taken as a pair of bf16 values hi + lo (16 significant bits)
+ *     and each product as three bf16 tensor-core products with fp32 accumulation -- within
+ *     the fp32 tolerance, on the tensor cores. It keeps a copy of qkv's size (T x 6 H x 64
+ *     bf16 values) in the stream's workspace.
  *   - otherwise bf16 and fp16 inputs: a tensor-core kernel (tcgen05, fp32 accumulation) after
  *     rotation in fp32, the rotated q and k rounded to the input type; a positive scale
  *     multiplies the fp32 scores, any other scale the rotated q; the probabilities are
@@ -61,6 +66,8 @@
  *   PK_ATTN=q4|tc_single   pk_attend and its typed forms run PK_KERNEL_Q4 or
  *                          PK_KERNEL_TC_SINGLE instead of PK_KERNEL_TC for bf16 / fp16 inputs
  *                          outside the narrow windows (read at every call).
+ *   PK_ATTN=split          the same for fp32 inputs with an fp32 output: PK_KERNEL_SPLIT
+ *                          instead of PK_KERNEL_F32.
  */
 #ifndef PK_H
 #define PK_H
@@ -99,7 +106,10 @@ enum pk_kernel {
                                  128-key stream tiles */
     PK_KERNEL_Q4 = 3,         /* 16-bit: tcgen05, two pipes of two query tiles per SM,
                                  64-key stream tiles */
-    PK_KERNEL_TC_SINGLE = 4   /* 16-bit: PK_KERNEL_TC with one tile record per work item */
+    PK_KERNEL_TC_SINGLE = 4,  /* 16-bit: PK_KERNEL_TC with one tile record per work item */
+    PK_KERNEL_SPLIT = 5       /* fp32: tcgen05 on bf16 hi / lo operand pairs, three products each
+                                 (S = Qh Kh + Qh Kl + Ql Kh, O += Ph Vh + Ph Vl + Pl Vh), after a
+                                 pre-pass that writes the rotated split copy; fp32 output only */
 };
 
 /* Limits: T <= PK_MAX_T, H <= PK_MAX_H. */
@@ -138,8 +148,9 @@ int pk_attend_dt(int dtype, const void *qkv, const void *cos, const void *sin,
  *   - Key: (current device, dtype, H, window + 1 (0 when window = 0), T rounded up to a power
  *     of two, longest rounded up to a power of two); pk_tune_key writes it as text.
  *   - Usable kernels: PK_KERNEL_BAND for 1 <= window <= 16 (its fp32 arithmetic keeps fp16
- *     inputs of large magnitude in tolerance), PK_KERNEL_F32 for other fp32 calls, and
- *     PK_KERNEL_TC, PK_KERNEL_TC_SINGLE and PK_KERNEL_Q4 for other bf16 / fp16 calls.
+ *     inputs of large magnitude in tolerance), PK_KERNEL_F32 and PK_KERNEL_SPLIT for other
+ *     fp32 calls, and PK_KERNEL_TC, PK_KERNEL_TC_SINGLE and PK_KERNEL_Q4 for other bf16 /
+ *     fp16 calls.
  *   - A key met for the first time with more than one usable kernel is tuned on the call's
  *     own arguments: each kernel runs once untimed, then three rounds time two runs of each
  *     kernel in turn between two events on `stream` (the host waiting for the second); a
@@ -214,7 +225,8 @@ int pk_profile_stop(double *schedule_ms, double *attend_ms, int *calls);
  * a plugin whose enqueue step may not allocate, an application whose pool allocator owns
  * the device) or that cannot afford the synchronization a cudaMalloc brings use this call
  * instead: it allocates nothing, and runs the kernels pk_attend_dt runs for the same
- * arguments (pk_forward_kernel) on a scratch area compiled into
+ * arguments (pk_forward_kernel; PK_KERNEL_F32 where that is PK_KERNEL_SPLIT, whose copy of
+ * qkv has no place in a fixed scratch area) on a scratch area compiled into
  * the library (a static __device__ array of about 4 MB, present on every GPU that loads
  * the library until the process exits).
  *   - dtype: enum pk_dtype; the other arguments as pk_attend.

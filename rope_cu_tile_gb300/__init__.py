@@ -33,7 +33,7 @@ EXPORTS = ("pk_attend", "pk_attend_bf16", "pk_attend_f16", "pk_attend_f32", "pk_
            "pk_version", "pk_release", "pk_profile_start", "pk_profile_stop", "pk_attend_noalloc", "pk_rope", "pk_attend_mixed",
            "pk_attend_backward", "pk_attend_tuned", "pk_tune_pick", "pk_tune_key", "pk_tune_clear",
            "pk_forward_kernel", "pk_kernel_name", "pk_attend_mixed_ops")
-KERNELS = {0: "band", 1: "f32", 2: "tc", 3: "q4", 4: "tc_single"}
+KERNELS = {0: "band", 1: "f32", 2: "tc", 3: "q4", 4: "tc_single", 5: "split"}
 
 _lib = None
 

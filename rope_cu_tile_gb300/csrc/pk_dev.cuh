@@ -64,15 +64,18 @@ constexpr int kKernelF32 = 1;   // fp32 inputs, CUDA cores
 constexpr int kKernelTc = 2;    // 16-bit inputs, paired-stream tensor-core kernel
 constexpr int kKernelQ4 = 3;    // 16-bit inputs, four-chain tensor-core kernel
 constexpr int kKernelTcSingle = 4;  // 16-bit inputs, paired-stream kernel with one record per item
+constexpr int kKernelSplit = 5;     // fp32 inputs, tensor cores on split bf16 operands (needs a scratch copy)
 int select_forward_kernel(int dtype, int window);
+// bytes of the split copy kKernelSplit reads (T x 6 H 64 bf16 values)
+inline long long split_copy_bytes(long long T, int H) { return T * 6 * H * kD * 2; }
 // The launches of one forward call on caller-provided scratch (control block, `cap` tile
-// records, the scheduler's staging slots); `ev`, when not null, gets three events recorded
-// (before the first launch, between the preparation and the attention kernel, after it).
-// Returns a pk_status code.
+// records, the scheduler's staging slots, and for kKernelSplit the split copy `copy` of
+// `copy_bytes` bytes); `ev`, when not null, gets three events recorded (before the first
+// launch, between the preparation and the attention kernel, after it). Returns a pk_status code.
 int forward_launch(int kernel, int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin,
                    const uint32_t* cu, int S, long long T, int H, int window, float scale, void* out, float* lse,
-                   Ctl* ctl, TileRec* tiles, long long cap, TileRec* stage, int sms, unsigned long long timeout_ns,
-                   cudaStream_t stream, cudaEvent_t* ev);
+                   Ctl* ctl, TileRec* tiles, long long cap, TileRec* stage, void* copy, long long copy_bytes, int sms,
+                   unsigned long long timeout_ns, cudaStream_t stream, cudaEvent_t* ev);
 
 // status codes (mirror enum pk_status)
 constexpr int kErrBadCu = 5;
@@ -280,6 +283,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane, waited for before returning.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {

@@ -44,6 +44,12 @@ cudaError_t band_prep_launch(const uint32_t* cu, int S, long long T, uint32_t* f
 cudaError_t band_launch(int dtype, int out_dtype, const void* qkv, const void* cos_t, const void* sin_t,
                         const uint32_t* cu, int S, uint32_t* first, void* out, float* lse, Ctl* ctl, int H, long long T,
                         int window, float scale, cudaStream_t stream);
+cudaError_t attend_split_prepare();
+cudaError_t split16_launch(const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu, int S,
+                           long long T, int H, float q_mul, const Ctl* ctl, void* y, int sms, cudaStream_t stream);
+cudaError_t attend_split_launch(const CUtensorMap& tmap, const uint32_t* cu, const TileRec* tiles, float* out,
+                                float* lse, Ctl* ctl, int H, long long T, int window, float scale,
+                                unsigned long long timeout_ns, int grid, cudaStream_t stream);
 cudaError_t attend_f32_launch(const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu,
                               const TileRec* tiles, void* out, int out_dtype, float* lse, Ctl* ctl, int H,
                               long long T, int window, float scale, int grid, cudaStream_t stream);
@@ -137,11 +143,14 @@ unsigned long long timeout_ns() {
 //   kBand  narrow windows (1 <= w <= kBandMaxW), any element type: CUDA cores, fp32 (no tile
 //          records: a check of cu replaces the scheduler);
 //   kF32   fp32 inputs otherwise: CUDA cores, fp32;
+//   kSplit fp32 inputs otherwise: tensor cores on split bf16 operands (a pre-pass writes the
+//          rotated hi / lo copy into the workspace);
 //   kTc    16-bit inputs: the paired-stream tensor-core kernel (two query tiles in flight per
 //          SM, 128-key stream tiles);
 //   kQ4    16-bit inputs: the four-chain tensor-core kernel (two pipes of two query tiles,
 //          64-key stream tiles).
-// PK_ATTN=tc, q4 or tc_single picks the tensor-core kernel for 16-bit inputs.
+// PK_ATTN=tc, q4 or tc_single picks the tensor-core kernel for 16-bit inputs; PK_ATTN=f32 or
+// split the kernel for fp32 inputs.
 constexpr int kBandMaxW = 16;
 int tensor_kernel_choice() {
   const char* e = std::getenv("PK_ATTN");
@@ -154,7 +163,10 @@ int tensor_kernel_choice() {
 
 int select_forward_kernel(int dtype, int window) {
   if (window >= 1 && window <= kBandMaxW) return kKernelBand;
-  if (dtype == PK_F32) return kKernelF32;
+  if (dtype == PK_F32) {
+    const char* e = std::getenv("PK_ATTN");
+    return (e && std::strcmp(e, "split") == 0) ? kKernelSplit : kKernelF32;
+  }
   return tensor_kernel_choice();
 }
 
@@ -173,7 +185,7 @@ int device_info(int dev, DeviceInfo** out) {
   if (!di.supported) return PK_ERR_UNSUPPORTED;
   if (!di.attrs_set) {
     if (attend_tc_prepare() != cudaSuccess || attend_q4_prepare() != cudaSuccess || band_prepare() != cudaSuccess ||
-        schedule_prepare() != cudaSuccess || backward_prepare() != cudaSuccess)
+        attend_split_prepare() != cudaSuccess || schedule_prepare() != cudaSuccess || backward_prepare() != cudaSuccess)
       return PK_ERR_CUDA;
     di.attrs_set = true;
   }
@@ -254,6 +266,8 @@ int launch_schedule(const uint32_t* cu, int S, int64_t T, int window, Workspace*
 }
 
 // out_dtype: the output's type (the input type, except for fp32 inputs with a 16-bit output)
+int ops16_scratch(Workspace* ws, cudaStream_t stream, int64_t bytes);
+
 int attend(int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin, const uint32_t* cu, int S,
            int64_t T, int H, int window, float scale, void* out, float* lse, cudaStream_t stream) {
   int rc = check_args(dtype, qkv, cos, sin, cu, S, T, H, window, out, lse);
@@ -265,11 +279,14 @@ int attend(int dtype, int out_dtype, const void* qkv, const void* cos, const voi
   if ((rc = device_info(dev, &di)) != PK_OK) return rc;
   Workspace* ws = nullptr;
   if ((rc = workspace(dev, stream, T, &ws)) != PK_OK) return rc;
+  int kernel = select_forward_kernel(dtype, window);
+  if (kernel == kKernelSplit && out_dtype != PK_F32) kernel = kKernelF32;  // the split kernel writes fp32
+  if (kernel == kKernelSplit && (rc = ops16_scratch(ws, stream, split_copy_bytes(T, H))) != PK_OK) return rc;
   cudaEvent_t* ev = nullptr;
   if (g_prof.on && g_prof.dev == dev && g_prof.used < g_prof.cap) ev = g_prof.ev + 3 * g_prof.used++;
-  return forward_launch(select_forward_kernel(dtype, window), dtype, out_dtype, qkv, cos, sin, cu, S,
-                        static_cast<long long>(T), H, window, scale, out, lse, ws->ctl, ws->tiles, ws->cap, ws->stage,
-                        di->sms, timeout_ns(), stream, ev);
+  return forward_launch(kernel, dtype, out_dtype, qkv, cos, sin, cu, S, static_cast<long long>(T), H, window, scale,
+                        out, lse, ws->ctl, ws->tiles, ws->cap, ws->stage, ws->ops16, ws->ops16_bytes, di->sms,
+                        timeout_ns(), stream, ev);
 }
 
 long long next_pow2(long long x) {
@@ -293,7 +310,8 @@ int tune_candidates(int dtype, int window, int* c) {
   }
   if (dtype == PK_F32) {
     c[0] = kKernelF32;
-    return 1;
+    c[1] = kKernelSplit;
+    return 2;
   }
   c[0] = kKernelTc;
   c[1] = kKernelTcSingle;
@@ -316,8 +334,11 @@ int attend_tuned(int dtype, const void* qkv, const void* cos, const void* sin, c
   Workspace* ws = nullptr;
   if ((rc = workspace(dev, stream, T, &ws)) != PK_OK) return rc;
   auto run = [&](int kernel, cudaEvent_t* ev) {
+    int r = PK_OK;
+    if (kernel == kKernelSplit && (r = ops16_scratch(ws, stream, split_copy_bytes(T, H))) != PK_OK) return r;
     return forward_launch(kernel, dtype, dtype, qkv, cos, sin, cu, S, static_cast<long long>(T), H, window, scale, out,
-                          lse, ws->ctl, ws->tiles, ws->cap, ws->stage, di->sms, timeout_ns(), stream, ev);
+                          lse, ws->ctl, ws->tiles, ws->cap, ws->stage, ws->ops16, ws->ops16_bytes, di->sms,
+                          timeout_ns(), stream, ev);
   };
   const TuneKey key = tune_key(dev, dtype, H, window, T, longest);
   auto it = g_tune.find(key);
@@ -495,8 +516,8 @@ int attend_backward(int dtype, const void* qkv, const void* cos, const void* sin
 
 int forward_launch(int kernel, int dtype, int out_dtype, const void* qkv, const void* cos, const void* sin,
                    const uint32_t* cu, int S, long long T, int H, int window, float scale, void* out, float* lse,
-                   Ctl* ctl, TileRec* tiles, long long cap, TileRec* stage, int sms, unsigned long long timeout,
-                   cudaStream_t stream, cudaEvent_t* ev) {
+                   Ctl* ctl, TileRec* tiles, long long cap, TileRec* stage, void* copy, long long copy_bytes, int sms,
+                   unsigned long long timeout, cudaStream_t stream, cudaEvent_t* ev) {
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return PK_ERR_CUDA;
   cudaError_t e = cudaSuccess;
   if (kernel == kKernelBand) {
@@ -510,9 +531,32 @@ int forward_launch(int kernel, int dtype, int out_dtype, const void* qkv, const 
     if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return PK_ERR_CUDA;
     return PK_OK;
   }
+  if (kernel == kKernelSplit &&
+      (dtype != PK_F32 || out_dtype != PK_F32 || !copy || copy_bytes < split_copy_bytes(T, H)))
+    return PK_ERR_INTERNAL;
   if (schedule_launch(cu, S, T, window, tiles, cap, stage, ctl, stream) != cudaSuccess) return PK_ERR_CUDA;
+  // the split kernel's pre-pass: q, k rotated in fp32, then q', k', v as bf16 hi / lo pairs
+  // (a positive scale multiplies the scores in the kernel, any other the rotated q here)
+  if (kernel == kKernelSplit &&
+      split16_launch(static_cast<const float*>(qkv), static_cast<const float*>(cos), static_cast<const float*>(sin),
+                     cu, S, T, H, scale > 0.0f ? 1.0f : scale, ctl, copy, sms, stream) != cudaSuccess)
+    return PK_ERR_CUDA;
   if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return PK_ERR_CUDA;
-  if (kernel == kKernelF32) {
+  if (kernel == kKernelSplit) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return PK_ERR_CUDA;
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(6) * H * kD, static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(6) * H * kD * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kD), static_cast<cuuint32_t>(kBR)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, copy, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PK_ERR_CUDA;
+    e = attend_split_launch(tmap, cu, tiles, static_cast<float*>(out), lse, ctl, H, T, window, scale, timeout, sms,
+                            stream);
+  } else if (kernel == kKernelF32) {
     e = attend_f32_launch(static_cast<const float*>(qkv), static_cast<const float*>(cos),
                           static_cast<const float*>(sin), cu, tiles, out, out_dtype, lse, ctl, H, T, window, scale,
                           sms * 4, stream);
@@ -626,6 +670,7 @@ const char* pk_kernel_name(int kernel) {
     case kKernelTc: return "pk_attend_tc_kernel";
     case kKernelQ4: return "pk_attend_q4_kernel";
     case kKernelTcSingle: return "pk_attend_tc_kernel (single-record items)";
+    case kKernelSplit: return "pk_attend_split_kernel";
     default: return "";
   }
 }
@@ -780,5 +825,6 @@ int pk_release(void) {
 }  // extern "C"
 
 static_assert(pk::kKernelBand == PK_KERNEL_BAND && pk::kKernelF32 == PK_KERNEL_F32 && pk::kKernelTc == PK_KERNEL_TC &&
-                  pk::kKernelQ4 == PK_KERNEL_Q4 && pk::kKernelTcSingle == PK_KERNEL_TC_SINGLE,
+                  pk::kKernelQ4 == PK_KERNEL_Q4 && pk::kKernelTcSingle == PK_KERNEL_TC_SINGLE &&
+                  pk::kKernelSplit == PK_KERNEL_SPLIT,
               "kernel ids match enum pk_kernel");

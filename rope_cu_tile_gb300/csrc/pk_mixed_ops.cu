@@ -76,6 +76,65 @@ pk_rotate16_kernel(const float* __restrict__ qkv, const float* __restrict__ cos_
   }
 }
 
+// Split copy for fp32 inputs on the tensor cores: every value x of q' (rotated, times q_mul),
+// k' (rotated) and v becomes two bf16 values, hi = bf16(x) and lo = bf16(x - hi), so that
+// hi + lo carries 16 significant bits of x. Row a of y holds 6 H 64 values: the hi copy of
+// the packed row [q' | k' | v] in columns [0, 3 H 64) and the lo copy in [3 H 64, 6 H 64).
+// The products S = Qh Kh^T + Qh Kl^T + Ql Kh^T then match the fp32 scores to about 2^-16
+// of their terms' size (the Ql Kl^T term, 2^-16 smaller again, is left out).
+__device__ __forceinline__ void split_store(uint16_t* hi, uint16_t* lo, float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  *hi = __bfloat16_as_ushort(h);
+  *lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+}
+
+__global__ void __launch_bounds__(256)
+pk_split16_kernel(const float* __restrict__ qkv, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
+                  const uint32_t* __restrict__ cu, int S, long long T, int H, float q_mul, const Ctl* ctl,
+                  uint16_t* __restrict__ y) {
+  if (__ldcg(&ctl->ntiles) == 0u) return;
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t ld = 3ll * H * kD;
+  for (long long a = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); a < T;
+       a += nwarps) {
+    const uint32_t s = seq_of_token(cu, 0u, static_cast<uint32_t>(S), static_cast<uint32_t>(a));
+    const int64_t pos = a - static_cast<long long>(__ldg(cu + s));
+    const float c = __ldg(cos_t + pos * kHalf + lane), sn = __ldg(sin_t + pos * kHalf + lane);
+    const float* x = qkv + a * ld;
+    uint16_t* yh = y + a * 2 * ld;
+    uint16_t* yl = yh + ld;
+    for (int part = 0; part < 2; ++part) {
+      for (int h = 0; h < H; ++h) {
+        const int64_t off = static_cast<int64_t>(part * H + h) * kD;
+        const float x1 = __ldg(x + off + lane), x2 = __ldg(x + off + lane + kHalf);
+        float y1 = fmaf(x1, c, -(x2 * sn));
+        float y2 = fmaf(x1, sn, x2 * c);
+        if (part == 0 && q_mul != 1.0f) {
+          y1 *= q_mul;
+          y2 *= q_mul;
+        }
+        split_store(yh + off + lane, yl + off + lane, y1);
+        split_store(yh + off + lane + kHalf, yl + off + lane + kHalf, y2);
+      }
+    }
+    for (int h = 0; h < H; ++h) {
+      const int64_t off = static_cast<int64_t>(2 * H + h) * kD;
+      split_store(yh + off + lane, yl + off + lane, __ldg(x + off + lane));
+      split_store(yh + off + lane + kHalf, yl + off + lane + kHalf, __ldg(x + off + lane + kHalf));
+    }
+  }
+}
+
+// Host side: the split copy (T x 6 H 64 bf16 values) of an fp32 qkv into `y`, on `stream`
+// after the tile scheduler.
+cudaError_t split16_launch(const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu, int S,
+                           long long T, int H, float q_mul, const Ctl* ctl, void* y, int sms, cudaStream_t stream) {
+  const int blocks = static_cast<int>(min(static_cast<long long>(sms) * 8, (T + 7) / 8));
+  pk_split16_kernel<<<blocks, 256, 0, stream>>>(qkv, cos_t, sin_t, cu, S, T, H, q_mul, ctl, static_cast<uint16_t*>(y));
+  return cudaGetLastError();
+}
+
 // Host side: the rotated 16-bit copy of an fp32 qkv into `y` (T x 3 H 64 elements of
 // op_dtype), on `stream` after the tile scheduler.
 cudaError_t rotate16_launch(int op_dtype, const float* qkv, const float* cos_t, const float* sin_t, const uint32_t* cu,

@@ -122,9 +122,12 @@ extern "C" int pk_attend_noalloc(int dtype, const void* qkv, const void* cos, co
   // the control block starts each call at zero (the last call's counter and status stay in it)
   if (cudaMemsetAsync(ctl, 0, sizeof(Ctl), st) != cudaSuccess) return PK_ERR_CUDA;
   // the same kernels as pk_attend would run for these arguments
-  rc = forward_launch(select_forward_kernel(dtype, window), dtype, dtype, qkv, cos, sin, cu, S,
-                      static_cast<long long>(T), H, window, scale, out, lse, ctl, tiles, kNoallocCap, stage, s->sms,
-                      noalloc_timeout_ns(), st, nullptr);
+  // (the split kernel for fp32 inputs needs a copy of qkv's size: fp32 calls here run the
+  // CUDA-core kernel)
+  int kernel = select_forward_kernel(dtype, window);
+  if (kernel == kKernelSplit) kernel = kKernelF32;
+  rc = forward_launch(kernel, dtype, dtype, qkv, cos, sin, cu, S, static_cast<long long>(T), H, window, scale, out,
+                      lse, ctl, tiles, kNoallocCap, stage, nullptr, 0, s->sms, noalloc_timeout_ns(), st, nullptr);
   if (rc != PK_OK) return rc;
   if (status && cudaMemcpyAsync(status, &ctl->status, sizeof(int), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return PK_ERR_CUDA;

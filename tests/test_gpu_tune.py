@@ -15,6 +15,7 @@ SHAPES = [
     ("window_70", [900, 40, 300], "bf16", 2, 70),
     ("window_4", [7, 1, 16, 3, 200, 12], "f16", 3, 4),
     ("f32_w0", [37, 64, 150], "f32", 2, 0),
+    ("f32_w70_long", [1200, 300, 5], "f32", 2, 70),
 ]
 
 
@@ -42,7 +43,7 @@ def test_tuned_matches_oracle_and_keeps_its_pick(pk, orc, shape):
     if 1 <= w <= 16:
         assert pick == 0
     elif dtype == "f32":
-        assert pick == 1
+        assert pick in (1, 5)
     else:
         assert pick in (2, 3, 4)
     want_o, want_l = orc.attend(wl.qkv, wl.cos, wl.sin, wl.cu, H, w, wl.scale, dtype)

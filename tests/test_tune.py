@@ -54,4 +54,5 @@ def test_untuned_dispatch(lib):
             assert pk.pk_forward_kernel(dt, w) == (1 if dt == pk.PK_F32 else 2)
     assert [pk.pk_kernel_name(k) for k in range(5)][:4] == [
         "pk_attend_band_kernel", "pk_attend_f32_kernel", "pk_attend_tc_kernel", "pk_attend_q4_kernel"]
+    assert pk.pk_kernel_name(5) == "pk_attend_split_kernel"
     assert pk.pk_kernel_name(99) == ""
