@@ -494,6 +494,9 @@ def main():
                     help="auto: pk_attend_tuned picks (default); otherwise pk_attend with that kernel "
                          "(tc, tc_single, q4: 16-bit inputs; f32, split: fp32 inputs; windows of 1..16 "
                          "always run the band kernel)")
+    ap.add_argument("--storage", default=None, choices=["bf16", "f16", "f32"],
+                    help="store the workload's qkv and tables in this type instead of its own (same lengths, "
+                         "heads, window, tables and seed)")
     ap.add_argument("--op", default="attend", choices=["attend", "rope", "backward"],
                     help="attend: the attention path (default); rope: the standalone rotation; "
                          "backward: pk_attend_backward")
@@ -507,8 +510,13 @@ def main():
     if world > 1 and "RANK" not in os.environ:
         world = 1
     wl = synth.make_config(args.config)
+    workload = f"{args.config}: {synth.CONFIG_TEXT[args.config]}"
+    if args.storage is not None and args.storage != wl.dtype:
+        wl = synth.make_lens_workload(f"{args.config}_{args.storage}", wl.lens, args.storage, H=wl.H, window=wl.window,
+                                      base=wl.base, seed=synth.CONFIG_NAMES.index(args.config))
+        workload += f" (stored as {args.storage})"
     flops, abytes = work(wl)
-    cfg = {"workload": f"{args.config}: {synth.CONFIG_TEXT[args.config]}", "T": wl.T, "S": wl.S, "H": wl.H,
+    cfg = {"workload": workload, "T": wl.T, "S": wl.S, "H": wl.H,
            "D": 64, "window": wl.window, "scale": wl.scale, "seed": synth.CONFIG_NAMES.index(args.config),
            "useful_gflop": flops / 1e9, "algorithmic_mb": abytes / 1e6,
            "l2": l2_note(wl), "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
