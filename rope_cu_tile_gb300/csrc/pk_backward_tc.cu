@@ -45,14 +45,16 @@ constexpr int kRowWarp0 = 4;              // warps 4..7: the row group
 constexpr uint32_t kTile = 128u * 128u;   // 128 rows x 64 16-bit elements
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kTile;
-constexpr uint32_t kOffQ = kOffV + kTile;
-constexpr uint32_t kOffO = kOffQ + kTile;       // dout
-constexpr uint32_t kOffPt = kOffO + kTile;      // P^T  [key][query], two tiles
+constexpr uint32_t kOffQ = kOffV + kTile;       // Q' of buffer b at kOffQ + b kQBuf
+constexpr uint32_t kOffO = kOffQ + kTile;       // dout of buffer b at kOffO + b kQBuf
+constexpr uint32_t kQBuf = 2 * kTile;           // two chunk buffers (Q', dout), taken in turn
+constexpr uint32_t kOffPt = kOffQ + 2 * kQBuf;  // P^T  [key][query], two tiles
 constexpr uint32_t kOffSt = kOffPt + 2 * kTile; // dS^T [key][query], two tiles
 constexpr uint32_t kOffS = kOffSt + 2 * kTile;  // dS   [query][key], two tiles
 constexpr uint32_t kOffRow = kOffS + 2 * kTile; // per query of the chunk: lse log2(e), D
 struct TcBars {
-  uint64_t kv_full, kv_ready, q_full, q_ready, s_full, p_ready, c_done, drain;
+  uint64_t kv_full, kv_ready, q_ready, s_full, p_ready, c_done, drain;
+  uint64_t q_full[2], q_empty[2];  // per chunk buffer: loaded; its last products have read it
 };
 constexpr uint32_t kOffBar = kOffRow + 2 * 128 * 4;
 constexpr uint32_t kTcSmemUsed = kOffBar + sizeof(TcBars) + 16;
@@ -161,7 +163,10 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
   if (tid == 0) {
     mbar_init(smem_u32(&B.kv_full), 1);
     mbar_init(smem_u32(&B.kv_ready), 4);
-    mbar_init(smem_u32(&B.q_full), 1);
+    mbar_init(smem_u32(&B.q_full[0]), 1);
+    mbar_init(smem_u32(&B.q_full[1]), 1);
+    mbar_init(smem_u32(&B.q_empty[0]), 1);
+    mbar_init(smem_u32(&B.q_empty[1]), 1);
     mbar_init(smem_u32(&B.q_ready), 4);
     mbar_init(smem_u32(&B.s_full), 1);
     mbar_init(smem_u32(&B.p_ready), 4);
@@ -184,8 +189,8 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
 
   // running counts: items (kv barriers) and chunks (the chunk barriers) this CTA has stepped through
   uint32_t n_it = 0, n_ch = 0;
-  // the producer's loads so far; when the CTA gives up, the last of each is the only one that
-  // may still be in flight (a chunk's load follows the previous chunk's completed products)
+  // the producer's loads so far; when the CTA gives up, the last K / V load and the last load of
+  // each chunk buffer are the only ones that may still be in flight
   uint32_t kv_loads = 0, q_loads = 0;
 
   const uint32_t idS = idesc_f16(BF16, 128, 128, false, false);
@@ -206,8 +211,10 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
     const uint32_t nchunks = (rec.nk + 127u) / 128u;
 
     if (warp == 0 && lane == 0) {
-      // producer: K and V of the key tile, then Q and dout of each chunk once the previous
-      // chunk's products (which read those buffers) have completed
+      // producer: K and V of the key tile, then Q and dout of each chunk into the chunk buffers
+      // in turn (global chunk g into buffer g & 1, its (g >> 1)-th use), each once the products
+      // of the chunk two back, which read that buffer, have completed -- so the next chunk's
+      // copy is in flight while the current one is worked on
       mbar_arrive_expect_tx(smem_u32(&B.kv_full), 2 * kTile);
       tma_load_2d(smem_u32(smem + kOffK), &tmap_qkv, smem_u32(&B.kv_full), static_cast<int32_t>(hd + h * 64),
                   static_cast<int32_t>(rec.q0));
@@ -215,13 +222,12 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
                   static_cast<int32_t>(rec.q0));
       ++kv_loads;
       for (uint32_t c = 0; c < nchunks; ++c) {
-        if (c > 0) {
-          if (!tc_wait(&B.c_done, (n_ch + c - 1) & 1u, p, &s_abort)) break;
-        }
+        const uint32_t g = n_ch + c, b = g & 1u;
+        if (g >= 2 && !tc_wait(&B.q_empty[b], ((g >> 1) - 1u) & 1u, p, &s_abort)) break;
         const int32_t qb = static_cast<int32_t>(rec.k0 + 128u * c);
-        mbar_arrive_expect_tx(smem_u32(&B.q_full), 2 * kTile);
-        tma_load_2d(smem_u32(smem + kOffQ), &tmap_qkv, smem_u32(&B.q_full), static_cast<int32_t>(h * 64), qb);
-        tma_load_2d(smem_u32(smem + kOffO), &tmap_dout, smem_u32(&B.q_full), static_cast<int32_t>(h * 64), qb);
+        mbar_arrive_expect_tx(smem_u32(&B.q_full[b]), 2 * kTile);
+        tma_load_2d(smem_u32(smem + kOffQ + b * kQBuf), &tmap_qkv, smem_u32(&B.q_full[b]), static_cast<int32_t>(h * 64), qb);
+        tma_load_2d(smem_u32(smem + kOffO + b * kQBuf), &tmap_dout, smem_u32(&B.q_full[b]), static_cast<int32_t>(h * 64), qb);
         ++q_loads;
       }
     } else if (warp == 1 && lane == 0) {
@@ -242,12 +248,16 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
       bool ok = tc_wait(&B.kv_ready, n_it & 1u, p, &s_abort);
       for (uint32_t c = 0; ok && c < nchunks; ++c) {
         const uint32_t ph = (n_ch + c) & 1u;
+        const uint32_t b = ph;                              // the chunk's buffer
+        const uint64_t boff = static_cast<uint64_t>(b) * (kQBuf >> 4);  // descriptor offset of buffer b
         if (!(ok = tc_wait(&B.q_ready, ph, p, &s_abort))) break;
         tc_fence_after();
 #pragma unroll
-        for (uint32_t ks = 0; ks < 4; ++ks) umma_f16_ss(tmem + kColS, aK + 2 * ks, bQ + 2 * ks, idS, ks > 0 ? 1u : 0u);
+        for (uint32_t ks = 0; ks < 4; ++ks)
+          umma_f16_ss(tmem + kColS, aK + 2 * ks, bQ + boff + 2 * ks, idS, ks > 0 ? 1u : 0u);
 #pragma unroll
-        for (uint32_t ks = 0; ks < 4; ++ks) umma_f16_ss(tmem + kColDP, aV + 2 * ks, bO + 2 * ks, idS, ks > 0 ? 1u : 0u);
+        for (uint32_t ks = 0; ks < 4; ++ks)
+          umma_f16_ss(tmem + kColDP, aV + 2 * ks, bO + boff + 2 * ks, idS, ks > 0 ? 1u : 0u);
         umma_commit(smem_u32(&B.s_full));
         if (!(ok = tc_wait(&B.p_ready, ph, p, &s_abort))) break;
         tc_fence_after();
@@ -257,11 +267,12 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
           const uint64_t aT = (ks < 4 ? aSt0 : aSt1) + 2 * (ks & 3u);
           const uint64_t aD = (ks < 4 ? aS0 : aS1) + 2 * (ks & 3u);
           const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
-          umma_f16_ss(tmem + kColDV, aP, mO + 128 * ks, idG, acc);
-          umma_f16_ss(tmem + kColDK, aT, mQ + 128 * ks, idG, acc);
+          umma_f16_ss(tmem + kColDV, aP, mO + boff + 128 * ks, idG, acc);
+          umma_f16_ss(tmem + kColDK, aT, mQ + boff + 128 * ks, idG, acc);
           umma_f16_ss(tmem + kColDQ, aD, mK + 128 * ks, idG, ks > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(&B.c_done));
+        umma_commit(smem_u32(&B.q_empty[b]));
       }
       // every product issued has completed before the item ends (and before tensor memory is freed)
       umma_commit(smem_u32(&B.drain));
@@ -292,27 +303,31 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
         if (lane == 0) mbar_arrive(smem_u32(&B.kv_ready));
       }
       const float c1 = p.scale * kLog2eTc;
-      for (uint32_t c = 0; !bad && c < nchunks; ++c) {
-        const uint32_t ph = (n_ch + c) & 1u;
-        const uint32_t qb = rec.k0 + 128u * c;
-        // Q' row t of the chunk, its lse and D
-        bad = group_any(!tc_wait(&B.q_full, ph, p, &s_abort));
-        if (bad) break;
-        {
-          const uint32_t a = qb + static_cast<uint32_t>(t);
-          float l2 = 0.f, d = 0.f;
-          if (a < qend) {
-            const uint32_t sa = rec.kind == 0 ? rec.seq : seq_of_token(p.cu, rec.seq, rec.nseq, a);
-            rotate_row<BF16>(smem + kOffQ, t, p.cos_t, p.sin_t, a - __ldg(p.cu + sa));
-            l2 = __ldg(p.lse + static_cast<int64_t>(h) * p.T + a) * kLog2eTc;
-            d = __ldg(p.D + static_cast<int64_t>(h) * p.T + a);
-          }
-          sL2[t] = l2;
-          sD[t] = d;
+      // Q' row t of chunk c (rotated in its buffer), its lse and D; then q_ready. Chunk c + 1 is
+      // staged as soon as chunk c's P^T and dS are written, so its rotation runs while chunk c's
+      // products do (lse and D are single-buffered: every thread has read chunk c's by then).
+      auto stage_chunk = [&](uint32_t c) -> bool {
+        const uint32_t g = n_ch + c, bq = g & 1u;
+        if (group_any(!tc_wait(&B.q_full[bq], (g >> 1) & 1u, p, &s_abort))) return true;
+        const uint32_t a = rec.k0 + 128u * c + static_cast<uint32_t>(t);
+        float l2 = 0.f, d = 0.f;
+        if (a < qend) {
+          const uint32_t sa = rec.kind == 0 ? rec.seq : seq_of_token(p.cu, rec.seq, rec.nseq, a);
+          rotate_row<BF16>(smem + kOffQ + bq * kQBuf, t, p.cos_t, p.sin_t, a - __ldg(p.cu + sa));
+          l2 = __ldg(p.lse + static_cast<int64_t>(h) * p.T + a) * kLog2eTc;
+          d = __ldg(p.D + static_cast<int64_t>(h) * p.T + a);
         }
+        sL2[t] = l2;
+        sD[t] = d;
         fence_proxy_async_smem();
         asm volatile("bar.sync 1, 128;" ::: "memory");  // the row group's lse / D are in place
         if (lane == 0) mbar_arrive(smem_u32(&B.q_ready));
+        return false;
+      };
+      if (!bad && nchunks > 0) bad = stage_chunk(0);
+      for (uint32_t c = 0; !bad && c < nchunks; ++c) {
+        const uint32_t ph = (n_ch + c) & 1u;
+        const uint32_t qb = rec.k0 + 128u * c;
         // P^T and dS^T of key row t (32 queries at a time), and dS's column t
         bad = group_any(!tc_wait(&B.s_full, ph, p, &s_abort));
         if (bad) break;
@@ -361,6 +376,10 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
         tc_fence_before();
         asm volatile("bar.sync 1, 128;" ::: "memory");  // every column of dS is written
         if (lane == 0) mbar_arrive(smem_u32(&B.p_ready));
+        if (c + 1 < nchunks) {
+          bad = stage_chunk(c + 1);
+          if (bad) break;
+        }
         // dQ' of query row t, added to the fp32 accumulator
         bad = group_any(!tc_wait(&B.c_done, ph, p, &s_abort));
         if (bad) break;
@@ -424,7 +443,10 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
   // the producer's copies in flight land before the CTA's shared memory goes away
   if (warp == 0 && lane == 0 && s_abort) {
     if (kv_loads) mbar_wait(smem_u32(&B.kv_full), (kv_loads - 1u) & 1u, p.timeout_ns);
-    if (q_loads) mbar_wait(smem_u32(&B.q_full), (q_loads - 1u) & 1u, p.timeout_ns);
+    // chunk loads go to buffer g & 1 in the order of the CTA's global chunk index g, as
+    // q_loads counts them: the last load of each buffer
+    for (uint32_t g = q_loads >= 2 ? q_loads - 2 : 0; g < q_loads; ++g)
+      mbar_wait(smem_u32(&B.q_full[g & 1u]), (g >> 1) & 1u, p.timeout_ns);
   }
   tc_fence_before();
   __syncthreads();

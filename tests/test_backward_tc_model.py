@@ -1,8 +1,9 @@
 """A discrete-event model of the hand-off protocol of the tcgen05 backward kernel
-(rope_cu_tile_gb300/csrc/pk_backward_tc.cu): the TMA producer, the MMA issuer, the four warps
+(rope_cu_tile_gb300/csrc/pk_backward_tc.cu): the TMA producer (query chunks into two buffers in
+turn, each reloaded once the products that read it have completed), the MMA issuer, the four warps
 of the row group (with their group barriers: a reducing barrier for each give-up decision and
-the plain ones between their shared-memory writes and reads), and the CTA-wide barrier between
-work items.
+the plain ones between their shared-memory writes and reads; chunk c + 1 staged right after chunk
+c's probabilities), and the CTA-wide barrier between work items.
 
 Each mbarrier wait in the kernel is bounded; a group or CTA barrier is not. The model checks,
 under random timings, that (1) without faults every wait that passes saw the event it was meant
@@ -51,7 +52,8 @@ class Cta:
         self.lose = lose  # name of the arrival to drop, or None
         self.late = late  # name of the arrival to deliver at about the wait bound
         self.per_warp = per_warp  # negative control: each warp of the row group decides alone
-        self.bar = {k: Barrier(c) for k, c in (("kv_full", 1), ("kv_ready", 4), ("q_full", 1), ("q_ready", 4),
+        self.bar = {k: Barrier(c) for k, c in (("kv_full", 1), ("kv_ready", 4), ("q_full0", 1), ("q_full1", 1),
+                                               ("q_empty0", 1), ("q_empty1", 1), ("q_ready", 4),
                                                ("s_full", 1), ("p_ready", 4), ("c_done", 1), ("drain", 1))}
         self.group = {}  # named-barrier instance -> arrivals (and OR of the flags)
         self.cta = {}    # CTA barrier instance -> arrivals
@@ -119,13 +121,14 @@ def producer(cta):
             break
         cta.later(cta.rng.randint(300, 1500), "kv_full", f"kv{n_it}")
         for c in range(nch):
-            if c > 0:
+            g = n_ch + c
+            if g >= 2:
                 r = []
-                yield from wait_bounded(cta, "c_done", (n_ch + c - 1) & 1,
-                                        lambda k=n_ch + c - 1: cta.log.get(f"cd{k}", 0) == 1, f"c_done {n_ch + c - 1}", r)
+                yield from wait_bounded(cta, f"q_empty{g & 1}", ((g >> 1) - 1) & 1,
+                                        lambda k=g - 2: cta.log.get(f"qe{k}", 0) == 1, f"q_empty {g - 2}", r)
                 if not r[0]:
                     break
-            cta.later(cta.rng.randint(300, 1500), "q_full", f"q{n_ch + c}")
+            cta.later(cta.rng.randint(300, 1500), f"q_full{g & 1}", f"q{g}")
         n_it += 1
         n_ch += nch
     yield from cta_barrier(cta, "end")
@@ -153,7 +156,9 @@ def issuer(cta):
             yield from wait_bounded(cta, "p_ready", ph, lambda k=n_ch + c: cta.log.get(f"pr{k}", 0) == 4, "p_ready", r)
             if not (ok := r[0]):
                 break
-            cta.later(cta.rng.randint(800, 1600), "c_done", f"cd{n_ch + c}")
+            d = cta.rng.randint(800, 1600)
+            cta.later(d, "c_done", f"cd{n_ch + c}")
+            cta.later(d, f"q_empty{(n_ch + c) & 1}", f"qe{n_ch + c}")
         cta.later(cta.rng.randint(800, 1700), "drain", f"dr{n_it}")
         r = []
         yield from wait_bounded(cta, "drain", n_it & 1, lambda: True, "drain", r)
@@ -176,20 +181,25 @@ def row_warp(cta, w):
             yield ("delay", cta.rng.randint(50, 300))
             cta.note(f"kr{n_it}")
             cta.bar["kv_ready"].arrive()
+        def stage(k):
+            r = []
+            yield ("delay", cta.rng.randint(1, 1500))
+            yield from wait_bounded(cta, f"q_full{k & 1}", (k >> 1) & 1, lambda k=k: cta.log.get(f"q{k}", 0) == 1,
+                                    "q_full", r)
+            if (yield from group_barrier(cta, ("qf", k), not r[0])):
+                return True
+            yield ("delay", cta.rng.randint(50, 300))
+            yield from group_barrier(cta, ("lse", k))
+            cta.note(f"qr{k}")
+            cta.bar["q_ready"].arrive()
+            return False
+        if not bad and nch > 0:
+            bad = yield from stage(n_ch)
         for c in range(nch):
             if bad:
                 break
             k = n_ch + c
             ph = k & 1
-            r = []
-            yield ("delay", cta.rng.randint(1, 1500))
-            yield from wait_bounded(cta, "q_full", ph, lambda k=k: cta.log.get(f"q{k}", 0) == 1, "q_full", r)
-            if (bad := (yield from group_barrier(cta, ("qf", k), not r[0]))):
-                break
-            yield ("delay", cta.rng.randint(50, 300))
-            yield from group_barrier(cta, ("lse", k))
-            cta.note(f"qr{k}")
-            cta.bar["q_ready"].arrive()
             r = []
             yield ("delay", cta.rng.randint(1, 1500))
             yield from wait_bounded(cta, "s_full", ph, lambda k=k: cta.log.get(f"sf{k}", 0) == 1, "s_full", r)
@@ -199,6 +209,9 @@ def row_warp(cta, w):
             yield from group_barrier(cta, ("ds", k))
             cta.note(f"pr{k}")
             cta.bar["p_ready"].arrive()
+            if c + 1 < nch:
+                if (bad := (yield from stage(k + 1))):
+                    break
             r = []
             yield ("delay", cta.rng.randint(1, 1500))
             yield from wait_bounded(cta, "c_done", ph, lambda k=k: cta.log.get(f"cd{k}", 0) == 1, "c_done", r)
