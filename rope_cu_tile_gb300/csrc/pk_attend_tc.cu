@@ -73,7 +73,8 @@ struct ItemBox {
   uint32_t a1;       // A uses stream tiles [0, a1)
   uint32_t b0, b1;   // B uses stream tiles [b0, b1) (empty without B)
   uint32_t end;      // shared stream: one past its last key token
-  uint32_t pad[7];
+  uint32_t ss_a, se_a, ss_b, se_b;  // a piece's sequence [start, end) (A, B; unused for a group)
+  uint32_t pad[3];
 };
 static_assert(sizeof(ItemBox) % 16 == 0, "item box keeps 16-byte alignment");
 
@@ -415,6 +416,12 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, uint8_t* smem
     bx.b0 = b0;
     bx.b1 = b1;
     bx.end = end;
+    // a piece's sequence bounds travel with the item (only a group's rows need the offsets
+    // of its member sequences staged)
+    bx.ss_a = ra.kind == 0 ? __ldg(p.cu + ra.seq) : 0u;
+    bx.se_a = ra.kind == 0 ? __ldg(p.cu + ra.seq + 1) : 0u;
+    bx.ss_b = has_b && rb.kind == 0 ? __ldg(p.cu + rb.seq) : 0u;
+    bx.se_b = has_b && rb.kind == 0 ? __ldg(p.cu + rb.seq + 1) : 0u;
     // (the test hook leaves the consumers waiting: their bounded waits time out and the CTA
     // unwinds with PK_ERR_TIMEOUT)
     if (!(p.skip_first_item_arrive && it == 0)) mbar_arrive(smem_u32(&B.item_full[mb]));
@@ -601,6 +608,7 @@ __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
   const uint32_t tbl0 = smem_u32(smem + kOffTbl + t * 2 * kRowTblBytes);
   const uint8_t* tblp = smem + kOffTbl + t * 2 * kRowTblBytes;
   uint32_t it = 0, qn0 = 0, qn1 = 0;
+  uint32_t staged = 0;        // items whose member offsets were staged (those with a group)
   uint32_t kst = 0, kph = 0;  // K ring stage and phase of the next K tile
   uint32_t buf = 0;           // table buffer of the next job
   bool bad = false;
@@ -613,36 +621,43 @@ __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
     const bool valid = bx.valid != 0, has_b = bx.has_b != 0;
     const TileRec ra = bx.a, rb = bx.b;
     const Stream sm = stream_of(bx);
-    // stage the member offsets of A and B (a group needs them to find each row's sequence)
-    uint32_t* off_a = meta->cu_rot[mb][0];
-    uint32_t* off_b = meta->cu_rot[mb][1];
-    if (valid) {
+    const uint32_t ss_a = bx.ss_a, ss_b = bx.ss_b;
+    // stage the member offsets of A and B when either is a group (a group needs them to find
+    // each row's sequence; a piece's bounds came with the item)
+    const bool grp = valid && (ra.kind != 0 || (has_b && rb.kind != 0));
+    const uint32_t sb = staged & 1u;
+    uint32_t* off_a = meta->cu_rot[sb][0];
+    uint32_t* off_b = meta->cu_rot[sb][1];
+    if (grp) {
       stage_cu(p, ra, off_a, t, 128);
       if (has_b) stage_cu(p, rb, off_b, t, 128);
     }
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(smem_u32(&B.item_empty[mb]));
-      if (valid) mbar_arrive(smem_u32(&B.cu_rot[mb]));
+      if (grp) mbar_arrive(smem_u32(&B.cu_rot[sb]));
     }
     ++it;
     if (!valid) break;
-    bad |= !wait_bar(meta, p.ctl, &B.cu_rot[mb], ((it - 1) >> 1) & 1u, p.timeout_ns);
-    bad = __any_sync(0xffffffffu, bad);
-    if (bad) break;
+    if (grp) {
+      bad |= !wait_bar(meta, p.ctl, &B.cu_rot[sb], (staged >> 1) & 1u, p.timeout_ns);
+      ++staged;
+      bad = __any_sync(0xffffffffu, bad);
+      if (bad) break;
+    }
 
     // positions of row t of Q_A and Q_B (for a group also of its key row t)
     const bool qok_a = t < static_cast<int>(ra.rows);
     const bool qok_b = has_b && t < static_cast<int>(rb.rows);
     uint32_t qpos_a = 0u, qpos_b = 0u;
     if (qok_a) {
-      uint32_t ss, se;
-      seq_bounds(p, ra, off_a, ra.q0 + t, ss, se);
+      uint32_t ss = ss_a, se;
+      if (ra.kind != 0) seq_bounds(p, ra, off_a, ra.q0 + t, ss, se);
       qpos_a = ra.q0 + t - ss;
     }
     if (qok_b) {
-      uint32_t ss, se;
-      seq_bounds(p, rb, off_b, rb.q0 + t, ss, se);
+      uint32_t ss = ss_b, se;
+      if (rb.kind != 0) seq_bounds(p, rb, off_b, rb.q0 + t, ss, se);
       qpos_b = rb.q0 + t - ss;
     }
 
@@ -653,8 +668,8 @@ __device__ void rotator(const Params& p, uint8_t* smem, Meta* meta, int t) {
     const uint32_t seg_a_end = sm.shared ? sm.n : sm.a1;
     const uint32_t a_kend = sm.shared ? sm.end : sm.a_k0 + sm.a_nk;
     const uint32_t b_kend = sm.b_k0 + sm.b_nk;
-    const int32_t a_pbase = ra.kind != 0 ? 0 : static_cast<int32_t>(sm.a_k0 + t) - static_cast<int32_t>(off_a[0]);
-    const int32_t b_pbase = (!has_b || rb.kind != 0) ? 0 : static_cast<int32_t>(sm.b_k0 + t) - static_cast<int32_t>(off_b[0]);
+    const int32_t a_pbase = ra.kind != 0 ? 0 : static_cast<int32_t>(sm.a_k0 + t) - static_cast<int32_t>(ss_a);
+    const int32_t b_pbase = (!has_b || rb.kind != 0) ? 0 : static_cast<int32_t>(sm.b_k0 + t) - static_cast<int32_t>(ss_b);
     auto krow = [&](uint32_t j, uint32_t& pos) -> bool {
       const bool inb = j >= seg_a_end;
       const uint32_t jj = inb ? j - seg_a_end : j;
@@ -776,28 +791,33 @@ __device__ void softmax_wg(const Params& p, Meta* meta, int x, uint32_t tmem) {
     const uint32_t jlo = x == 0 ? 0u : bx.b0, jhi = x == 0 ? bx.a1 : bx.b1;
     const uint32_t kbase = (x == 0 || bx.shared) ? bx.a.k0 + jlo * kBC : bx.b.k0;
     const uint32_t kend = bx.shared ? bx.end : rec.k0 + rec.nk;
+    // a piece's sequence bounds came with the item; a group's member offsets are staged
+    const uint32_t box_ss = x == 0 ? bx.ss_a : bx.ss_b, box_se = x == 0 ? bx.se_a : bx.se_b;
+    const bool grp = rec.kind != 0;
     uint32_t* off = meta->cu_sm[x][used & 1u];
-    if (mine) stage_cu(p, rec, off, r, 128);
+    if (mine && grp) stage_cu(p, rec, off, r, 128);
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(smem_u32(&B.item_empty[mb]));
-      if (mine) mbar_arrive(smem_u32(&B.cu_sm[x][used & 1u]));
+      if (mine && grp) mbar_arrive(smem_u32(&B.cu_sm[x][used & 1u]));
     }
     ++it;
     if (!valid) break;
     if (!mine) continue;
-    bad |= !wait_bar(meta, p.ctl, &B.cu_sm[x][used & 1u], (used >> 1) & 1u, p.timeout_ns);
-    ++used;
-    bad = __any_sync(0xffffffffu, bad);
-    if (bad) break;
+    if (grp) {
+      bad |= !wait_bar(meta, p.ctl, &B.cu_sm[x][used & 1u], (used >> 1) & 1u, p.timeout_ns);
+      ++used;
+      bad = __any_sync(0xffffffffu, bad);
+      if (bad) break;
+    }
 
     // this thread's query row and its visible key interval [lo, hi) (tokens < 2^31)
     const bool row_ok = r < static_cast<int>(rec.rows);
     const int a = static_cast<int>(rec.q0) + r;
     int lo = 0, hi = 0;
     if (row_ok) {
-      uint32_t ss, se;
-      seq_bounds(p, rec, off, static_cast<uint32_t>(a), ss, se);
+      uint32_t ss = box_ss, se = box_se;
+      if (grp) seq_bounds(p, rec, off, static_cast<uint32_t>(a), ss, se);
       lo = static_cast<int>(ss);
       hi = static_cast<int>(se);
       if (p.window > 0) {
@@ -1005,8 +1025,9 @@ pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_c
   tc_fence_after();
 
   // Register split (warpgroup-wide): the launch gives 512 x 128 = 65536 registers; the
-  // producer / MMA warpgroup drops to 80, the rotation warpgroup to 64, and the two softmax
-  // warpgroups rise to 184: 128 x 80 + 128 x 64 + 256 x 184 = 65536.
+  // producer / MMA warpgroup drops to 80 and the rotation warpgroup to 96 (the code after a
+  // decrease is compiled within it), and the two softmax warpgroups rise to 160 (their code is
+  // compiled within the launch's 128 either way): 128 x 80 + 128 x 96 + 256 x 160 = 63488.
   if (warp < kWarpRot) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
     // (each role reads what it needs after its own register change: nothing computed
@@ -1022,10 +1043,10 @@ pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_c
       if (lane == 0) mma_issuer(p, smem, meta, meta->tmem, BF16, warp - kWarpMma);
     }
   } else if (warp < kWarpSm) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
     rotator<BF16>(p, smem, meta, tid - kWarpRot * 32);
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 160;" ::: "memory");
     softmax_wg<BF16, OUT32>(p, meta, (warp - kWarpSm) >> 2, meta->tmem);
   }
 
