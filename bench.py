@@ -55,9 +55,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel's sources have the recorded hash (kernel_source_hash; otherwise reported as null).
 NCU_TRAFFIC = {  # {config_name: (kernel_source_hash() of the captured kernel, bytes per launch)}
     # pk_attend_tc_kernel on the long batch (profiles/pk_attend_tc_kernel_long.md)
-    "long": ("96899a5d901697a1fed78a32b088acc4bc93558f", 1068418304),
+    "long": ("6511010fddcbff84325ff2d8ef5926f2fc66e814", 1068108544),
     # pk_attend_band_kernel on the short-sequence workload (profiles/pk_attend_band_kernel_short.md)
-    "short": ("75957ecff2b1eaf2f48650772648e805c159a53c", 384529664),
+    "short": ("7f2a6e736eb1e3fe0bcc42af75fc83a3788cca52", 384193024),
 }
 
 
