@@ -14,10 +14,11 @@
 // storage type), which also keeps fp16 inputs of large magnitude inside their tolerance.
 //
 // Launch: one CTA per block of 32 tokens and group of four, two or one heads (one warp per
-// head: as many as let two CTAs share an SM). Every global read is an asynchronous copy into
-// shared memory, all of a CTA's in flight at once: each warp's raw q, k and v rows of its head
-// over the staged tokens [t0 - W, t0 + 32 + W), and the CTA's cos / sin rows of those tokens'
-// positions. A warp then rotates its k rows to fp32 in place and computes its 32 query rows in
+// head: as many as let two CTAs share an SM). Every global read is in flight at once: each
+// warp's raw k and v rows of its head over the staged tokens [t0 - W, t0 + 32 + W) and the
+// CTA's cos / sin rows of those tokens' positions as asynchronous copies into shared memory,
+// and each lane's own q features of its first rows straight into registers (q needs no
+// staging: a lane reads only its own rows and features, once). A warp then rotates its k rows to fp32 in place and computes its 32 query rows in
 // register tiles (R rows x 16 features a lane, so that each key and value granule it loads
 // serves up to R rows; see the kernel). The sequence of every staged token comes from the
 // offsets cu[s0 ..] staged once per CTA, s0 being the sequence of the block's first staged
@@ -128,7 +129,6 @@ __device__ __forceinline__ void band_cp16(void* dst, const void* src) {
 //                                  one before); the raw 16-bit row is copied into its last 128
 //                                  bytes (byte 144 on) and rotated in place
 //   v   [heads][rows][VS] stored   values as stored (VS: 72 16-bit or 68 fp32 elements)
-//   q   [heads][32][VS]   stored   raw queries
 //   tab [rows][2][32]     stored   cos and sin rows of each staged token's position
 template <typename F, int W>
 struct BandSmem {
@@ -136,15 +136,14 @@ struct BandSmem {
   static constexpr int kVS = sizeof(F) == 4 ? 68 : 72;
   static constexpr size_t kRowBytes = sizeof(float) * kKStride;  // 272
   static constexpr size_t kRawAt = sizeof(F) == 4 ? 0 : 144;     // raw 16-bit k row inside its fp32 row
-  static constexpr size_t kPerHead = kRows * kRowBytes + sizeof(F) * kRows * kVS + sizeof(F) * kBandRows * kVS;
+  static constexpr size_t kPerHead = kRows * kRowBytes + sizeof(F) * kRows * kVS;
   static constexpr size_t kTabBytes = sizeof(F) * kRows * 2 * kHalf;
   // heads per CTA (one warp each): four, two or one, whichever lets two CTAs share an SM
   static constexpr size_t kTwoPerSm = 113 * 1024;
   static constexpr int kHeads = 4 * kPerHead + kTabBytes <= kTwoPerSm ? 4 : 2 * kPerHead + kTabBytes <= kTwoPerSm ? 2 : 1;
   static constexpr size_t kK = 0;
   static constexpr size_t kV = kK + kHeads * kRows * kRowBytes;
-  static constexpr size_t kQ = kV + sizeof(F) * kHeads * kRows * kVS;
-  static constexpr size_t kTab = kQ + sizeof(F) * kHeads * kBandRows * kVS;
+  static constexpr size_t kTab = kV + sizeof(F) * kHeads * kRows * kVS;
   static constexpr size_t kBytes = kTab + kTabBytes;
   static_assert(kBytes <= 227 * 1024, "fits the shared memory a block may use");
   static_assert(kRawAt + 128 <= kRowBytes, "a raw 16-bit row fits inside its fp32 row");
@@ -177,6 +176,29 @@ __device__ __forceinline__ void lds4(const F* p, float (&x)[4]) {
     for (int k = 0; k < 4; ++k) x[k] = Store<F>::to_f(e[k]);
   }
 }
+// 4 consecutive stored elements (one feature granule) in registers: 8 bytes of a 16-bit type,
+// 16 of fp32; read from global memory and widened to fp32
+template <typename F>
+struct Granule {
+  using type = uint2;
+  __device__ static __forceinline__ type load(const F* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+  __device__ static __forceinline__ type zero() { return make_uint2(0u, 0u); }
+  __device__ static __forceinline__ void widen(const type& g, float (&x)[4]) {
+    const F* e = reinterpret_cast<const F*>(&g);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[k] = Store<F>::to_f(e[k]);
+  }
+};
+template <>
+struct Granule<float> {
+  using type = float4;
+  __device__ static __forceinline__ type load(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+  __device__ static __forceinline__ type zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ static __forceinline__ void widen(const type& g, float (&x)[4]) {
+    x[0] = g.x; x[1] = g.y; x[2] = g.z; x[3] = g.w;
+  }
+};
+
 __device__ __forceinline__ void sts8(float* p, const float (&y)[8]) {
   reinterpret_cast<float4*>(p)[0] = make_float4(y[0], y[1], y[2], y[3]);
   reinterpret_cast<float4*>(p)[1] = make_float4(y[4], y[5], y[6], y[7]);
@@ -207,7 +229,6 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
   extern __shared__ __align__(16) unsigned char band_smem[];
   auto s_k = reinterpret_cast<float (*)[kRowsSt][kKStride]>(band_smem + L::kK);
   auto s_v = reinterpret_cast<F (*)[kRowsSt][kVS]>(band_smem + L::kV);
-  auto s_q = reinterpret_cast<F (*)[kBandRows][kVS]>(band_smem + L::kQ);
   auto s_tab = reinterpret_cast<F (*)[2][kHalf]>(band_smem + L::kTab);
   __shared__ uint32_t s_cu[kBandCu + 1];
   __shared__ int s_ncu;
@@ -241,16 +262,23 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
         *reinterpret_cast<uint4*>(vd) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    for (int i = lane; i < kBandRows * kRowChunks; i += 32) {
-      const int r = i / kRowChunks, c = i % kRowChunks;
-      const long long a = t0 + r;
-      F* qd = s_q[warp][r] + c * kChunk;
-      if (a < T)
-        band_cp16(qd, qkv + a * ldq + static_cast<int64_t>(h) * kD + c * kChunk);
-      else
-        *reinterpret_cast<uint4*>(qd) = make_uint4(0u, 0u, 0u, 0u);
-    }
   }
+  // this lane's raw q granules (e, e + 4, e + 8, e + 12) of the R rows it takes first, into
+  // registers while the copies are in flight
+  const int g = lane >> 2, e = lane & 3;
+  using QG = Granule<F>;
+  typename QG::type qraw[R][4];
+  auto load_q = [&](int rb) {
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const long long a = t0 + rb + i;
+#pragma unroll
+      for (int gi = 0; gi < 4; ++gi)
+        qraw[i][gi] = (h < H && a < T) ? QG::load(qkv + a * ldq + static_cast<int64_t>(h) * kD + 4 * (e + 4 * gi))
+                                       : QG::zero();
+    }
+  };
+  load_q(R * g);
   // stage cu[s0 .. s0 + kBandCu] (the block's staged tokens start in sequence s0)
   const uint32_t s0 = __ldg(first + b);
   for (int i = tid; i <= kBandCu; i += blockDim.x)
@@ -321,11 +349,11 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
   }
   __syncwarp();
 
-  const int g = lane >> 2, e = lane & 3;
   // the lane's 16 features: granules e, e + 4 (first half of the rotary pairs), e + 8, e + 12
   // (their partners); q' and the key granules are held in that order
 #pragma unroll 1
   for (int rb = R * g; rb < kBandRows; rb += 8 * R) {
+    if (rb != R * g) load_q(rb);
     // q' of the lane's rows, its features, in fp32
     float qv[R][16];
 #pragma unroll
@@ -335,8 +363,8 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
       for (int c = 0; c < 2; ++c) {
         float x1[4], x2[4], tc[4], ts[4];
         const int u = 4 * (e + 4 * c);
-        lds4(s_q[warp][row] + u, x1);
-        lds4(s_q[warp][row] + u + kHalf, x2);
+        QG::widen(qraw[i][c], x1);
+        QG::widen(qraw[i][c + 2], x2);
         lds4(&s_tab[r][0][u], tc);
         lds4(&s_tab[r][1][u], ts);
 #pragma unroll
