@@ -16,8 +16,11 @@
 // and the row group (thread = query row) adds scale dQ' to the fp32 dq accumulator. At the end of
 // the item dK' and dV are complete: dk = rot^T(scale dK') and dv are rounded once and written.
 //
-// Roles (256 threads): warp 0 lane 0 the TMA producer, warp 1 lane 0 the MMA issuer, warp 2 owns
-// the tensor memory (512 columns), warps 4-7 the row group (warp w reads TMEM lanes 32 (w - 4) ..).
+// Roles (384 threads): warp 0 lane 0 the TMA producer, warp 1 lane 0 the MMA issuer, warp 2 owns
+// the tensor memory (512 columns), warps 4-11 the row group in two halves of four warps (warp w
+// reads TMEM lanes 32 (w % 4) ..): row t is shared by thread t of each half, which take half of
+// the row's work each (half the chunk pairs of a rotation, 64 of a chunk's 128 queries, 32 of
+// the 64 dimensions of dQ', dK', dV).
 // Within an item the three roles step through the chunks in lockstep on mbarriers (each barrier
 // completes once per chunk and every waiter waits for every phase, so a parity test is never two
 // phases away from its barrier); items are separated by a CTA-wide barrier.
@@ -40,8 +43,9 @@ namespace pk {
 
 namespace {
 
-constexpr int kTcThreads = 256;
-constexpr int kRowWarp0 = 4;              // warps 4..7: the row group
+constexpr int kTcThreads = 384;
+constexpr int kRowWarp0 = 4;              // warps 4..11: the row group, two halves of four warps
+constexpr int kRowThreads = 256;
 constexpr uint32_t kTile = 128u * 128u;   // 128 rows x 64 16-bit elements
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kTile;
@@ -92,15 +96,15 @@ __device__ __forceinline__ uint8_t* chunk_at(uint8_t* tile, int r, int c) {
   return tile + r * 128 + ((c ^ (r & 7)) << 4);
 }
 
-// Row r of a landed [128][64] tile rotated in place at position pos (pairs u, u + 32: chunk c
-// with chunk c + 4), tables in the element type.
+// Chunk pairs c0, c0 + 1 of row r of a landed [128][64] tile rotated in place at position pos
+// (pairs u, u + 32: chunk c with chunk c + 4), tables in the element type.
 template <bool BF16>
 __device__ __forceinline__ void rotate_row(uint8_t* tile, int r, const uint16_t* cos_t, const uint16_t* sin_t,
-                                           uint32_t pos) {
+                                           uint32_t pos, int c0) {
   const uint4* cr = reinterpret_cast<const uint4*>(cos_t + static_cast<int64_t>(pos) * 32);
   const uint4* sr = reinterpret_cast<const uint4*>(sin_t + static_cast<int64_t>(pos) * 32);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = c0; c < c0 + 2; ++c) {
     uint4* p1 = reinterpret_cast<uint4*>(chunk_at(tile, r, c));
     uint4* p2 = reinterpret_cast<uint4*>(chunk_at(tile, r, c + 4));
     const uint4 x1 = *p1, x2 = *p2, tc = __ldg(cr + c), ts = __ldg(sr + c);
@@ -128,13 +132,13 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, const Tc
   return false;
 }
 
-// The row group's decision to give up, taken together: a barrier over its 128 threads (named
+// The row group's decision to give up, taken together: a barrier over its 256 threads (named
 // barrier 1) that ORs their flags, so that no warp waits at a later group barrier for a warp
 // that has left.
 __device__ __forceinline__ bool group_any(bool v) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\t"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(v ? 1u : 0u)
@@ -162,14 +166,14 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
 
   if (tid == 0) {
     mbar_init(smem_u32(&B.kv_full), 1);
-    mbar_init(smem_u32(&B.kv_ready), 4);
+    mbar_init(smem_u32(&B.kv_ready), 8);
     mbar_init(smem_u32(&B.q_full[0]), 1);
     mbar_init(smem_u32(&B.q_full[1]), 1);
     mbar_init(smem_u32(&B.q_empty[0]), 1);
     mbar_init(smem_u32(&B.q_empty[1]), 1);
-    mbar_init(smem_u32(&B.q_ready), 4);
+    mbar_init(smem_u32(&B.q_ready), 8);
     mbar_init(smem_u32(&B.s_full), 1);
-    mbar_init(smem_u32(&B.p_ready), 4);
+    mbar_init(smem_u32(&B.p_ready), 8);
     mbar_init(smem_u32(&B.c_done), 1);
     mbar_init(smem_u32(&B.drain), 1);
     s_abort = 0;
@@ -280,8 +284,9 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
     } else if (warp >= kRowWarp0) {
       // the row group: thread t is key row t (rotation, P^T / dS^T, dK / dV) and query row t
       // of each chunk (rotation of Q', lse and D, dQ')
-      const int t = tid - kRowWarp0 * 32;
-      const uint32_t lanes = static_cast<uint32_t>((warp - kRowWarp0) * 32) << 16;
+      const int t = (tid - kRowWarp0 * 32) & 127;   // the row
+      const int hf = (tid - kRowWarp0 * 32) >> 7;   // the half of its work
+      const uint32_t lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const bool kok = t < static_cast<int>(rec.rows);
       const uint32_t b = rec.q0 + static_cast<uint32_t>(t);
       int64_t klo = 0, khi = 0, kstart = 0;
@@ -297,7 +302,7 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
       }
       bool bad = group_any(!tc_wait(&B.kv_full, n_it & 1u, p, &s_abort));
       if (!bad) {
-        if (kok) rotate_row<BF16>(smem + kOffK, t, p.cos_t, p.sin_t, static_cast<uint32_t>(b - kstart));
+        if (kok) rotate_row<BF16>(smem + kOffK, t, p.cos_t, p.sin_t, static_cast<uint32_t>(b - kstart), 2 * hf);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&B.kv_ready));
@@ -313,14 +318,18 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
         float l2 = 0.f, d = 0.f;
         if (a < qend) {
           const uint32_t sa = rec.kind == 0 ? rec.seq : seq_of_token(p.cu, rec.seq, rec.nseq, a);
-          rotate_row<BF16>(smem + kOffQ + bq * kQBuf, t, p.cos_t, p.sin_t, a - __ldg(p.cu + sa));
-          l2 = __ldg(p.lse + static_cast<int64_t>(h) * p.T + a) * kLog2eTc;
-          d = __ldg(p.D + static_cast<int64_t>(h) * p.T + a);
+          rotate_row<BF16>(smem + kOffQ + bq * kQBuf, t, p.cos_t, p.sin_t, a - __ldg(p.cu + sa), 2 * hf);
+          if (hf == 0) {
+            l2 = __ldg(p.lse + static_cast<int64_t>(h) * p.T + a) * kLog2eTc;
+            d = __ldg(p.D + static_cast<int64_t>(h) * p.T + a);
+          }
         }
-        sL2[t] = l2;
-        sD[t] = d;
+        if (hf == 0) {
+          sL2[t] = l2;
+          sD[t] = d;
+        }
         fence_proxy_async_smem();
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the row group's lse / D are in place
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // the row group's lse / D are in place
         if (lane == 0) mbar_arrive(smem_u32(&B.q_ready));
         return false;
       };
@@ -333,7 +342,7 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
         if (bad) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
           float s[32], dp[32];
           tmem_ld32(tmem + lanes + kColS + 32 * cb, s);
           tmem_ld32(tmem + lanes + kColDP + 32 * cb, dp);
@@ -374,7 +383,7 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // every column of dS is written
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // every column of dS is written
         if (lane == 0) mbar_arrive(smem_u32(&B.p_ready));
         if (c + 1 < nchunks) {
           bad = stage_chunk(c + 1);
@@ -385,13 +394,13 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
         if (bad) break;
         tc_fence_after();
         {
-          float v[64];
-          tmem_ld64(tmem + lanes + kColDQ, v);
+          float v[32];
+          tmem_ld32(tmem + lanes + kColDQ + 32 * hf, v);
           const uint32_t a = qb + static_cast<uint32_t>(t);
           if (a < qend) {
-            float4* dst = reinterpret_cast<float4*>(p.dq + static_cast<int64_t>(a) * hd + h * 64);
+            float4* dst = reinterpret_cast<float4*>(p.dq + static_cast<int64_t>(a) * hd + h * 64 + 32 * hf);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
+            for (int j = 0; j < 8; ++j)
               atomicAdd(dst + j, make_float4(p.scale * v[4 * j], p.scale * v[4 * j + 1], p.scale * v[4 * j + 2],
                                              p.scale * v[4 * j + 3]));
           }
@@ -400,9 +409,12 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
       }
       // dk = rot^T(scale dK') and dv of key row t, rounded once
       if (!bad) {
-        float k2[64], v2[64];
-        tmem_ld64(tmem + lanes + kColDK, k2);
-        tmem_ld64(tmem + lanes + kColDV, v2);
+        // this half: the pairs u in [16 hf, 16 hf + 16) of dk (columns u and u + 32) and the
+        // dimensions [32 hf, 32 hf + 32) of dv
+        float ka[16], kb[16], v2[32];
+        tmem_ld16(tmem + lanes + kColDK + 16 * hf, ka);
+        tmem_ld16(tmem + lanes + kColDK + 32 + 16 * hf, kb);
+        tmem_ld32(tmem + lanes + kColDV + 32 * hf, v2);
         if (kok) {
           const uint32_t pos = static_cast<uint32_t>(b - kstart);
           const uint16_t* cr = p.cos_t + static_cast<int64_t>(pos) * 32;
@@ -410,7 +422,8 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
           uint16_t* rowk = p.dqkv + static_cast<int64_t>(b) * ldq + hd + h * 64;
           uint16_t* rowv = p.dqkv + static_cast<int64_t>(b) * ldq + 2 * hd + h * 64;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * hf + cc;
             const uint4 tc4 = __ldg(reinterpret_cast<const uint4*>(cr) + c);
             const uint4 ts4 = __ldg(reinterpret_cast<const uint4*>(sr) + c);
             const uint32_t ac[4] = {tc4.x, tc4.y, tc4.z, tc4.w}, as[4] = {ts4.x, ts4.y, ts4.z, ts4.w};
@@ -418,9 +431,9 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const float2 co = Elem<BF16>::unpack(ac[i]), si = Elem<BF16>::unpack(as[i]);
-              const int u = 8 * c + 2 * i;
-              const float xa0 = p.scale * k2[u], xb0 = p.scale * k2[u + 32];
-              const float xa1 = p.scale * k2[u + 1], xb1 = p.scale * k2[u + 33];
+              const int u = 8 * cc + 2 * i;  // index into this half's 16 pairs
+              const float xa0 = p.scale * ka[u], xb0 = p.scale * kb[u];
+              const float xa1 = p.scale * ka[u + 1], xb1 = p.scale * kb[u + 1];
               ya[i] = Elem<BF16>::pack(fmaf(xa0, co.x, xb0 * si.x), fmaf(xa1, co.y, xb1 * si.y));
               yb[i] = Elem<BF16>::pack(fmaf(xb0, co.x, -xa0 * si.x), fmaf(xb1, co.y, -xa1 * si.y));
             }
@@ -428,8 +441,8 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
             reinterpret_cast<uint4*>(rowk)[c + 4] = make_uint4(yb[0], yb[1], yb[2], yb[3]);
           }
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            reinterpret_cast<uint4*>(rowv)[c] =
+          for (int c = 0; c < 4; ++c)
+            reinterpret_cast<uint4*>(rowv)[4 * hf + c] =
                 make_uint4(Elem<BF16>::pack(v2[8 * c], v2[8 * c + 1]), Elem<BF16>::pack(v2[8 * c + 2], v2[8 * c + 3]),
                            Elem<BF16>::pack(v2[8 * c + 4], v2[8 * c + 5]), Elem<BF16>::pack(v2[8 * c + 6], v2[8 * c + 7]));
         }

@@ -1,6 +1,6 @@
 """A discrete-event model of the hand-off protocol of the tcgen05 backward kernel
 (rope_cu_tile_gb300/csrc/pk_backward_tc.cu): the TMA producer (query chunks into two buffers in
-turn, each reloaded once the products that read it have completed), the MMA issuer, the four warps
+turn, each reloaded once the products that read it have completed), the MMA issuer, the eight warps
 of the row group (with their group barriers: a reducing barrier for each give-up decision and
 the plain ones between their shared-memory writes and reads; chunk c + 1 staged right after chunk
 c's probabilities), and the CTA-wide barrier between work items.
@@ -18,6 +18,7 @@ import random
 import pytest
 
 TIMEOUT = 20000
+NW = 8  # warps of the row group (two halves of four)
 
 
 class Barrier:
@@ -52,9 +53,9 @@ class Cta:
         self.lose = lose  # name of the arrival to drop, or None
         self.late = late  # name of the arrival to deliver at about the wait bound
         self.per_warp = per_warp  # negative control: each warp of the row group decides alone
-        self.bar = {k: Barrier(c) for k, c in (("kv_full", 1), ("kv_ready", 4), ("q_full0", 1), ("q_full1", 1),
-                                               ("q_empty0", 1), ("q_empty1", 1), ("q_ready", 4),
-                                               ("s_full", 1), ("p_ready", 4), ("c_done", 1), ("drain", 1))}
+        self.bar = {k: Barrier(c) for k, c in (("kv_full", 1), ("kv_ready", NW), ("q_full0", 1), ("q_full1", 1),
+                                               ("q_empty0", 1), ("q_empty1", 1), ("q_ready", NW),
+                                               ("s_full", 1), ("p_ready", NW), ("c_done", 1), ("drain", 1))}
         self.group = {}  # named-barrier instance -> arrivals (and OR of the flags)
         self.cta = {}    # CTA barrier instance -> arrivals
 
@@ -95,13 +96,13 @@ def wait_bounded(cta, key, parity, observed, what, out):
 
 
 def group_barrier(cta, tag, flag=False):
-    """A named barrier over the row group's 4 warps (unbounded), ORing the flags."""
+    """A named barrier over the row group's warps (unbounded), ORing the flags."""
     if cta.per_warp and tag[0] in ("kv", "qf", "sf", "cd"):
         return flag  # the negative control: no shared decision, no barrier
     g = cta.group.setdefault(tag, [0, False])
     g[0] += 1
     g[1] = g[1] or flag
-    while cta.group[tag][0] < 4:
+    while cta.group[tag][0] < NW:
         yield ("blocked", f"group barrier {tag}")
     return cta.group[tag][1]
 
@@ -141,19 +142,19 @@ def issuer(cta):
         if cta.abort:
             break
         r = []
-        yield from wait_bounded(cta, "kv_ready", n_it & 1, lambda k=n_it: cta.log.get(f"kr{k}", 0) == 4, "kv_ready", r)
+        yield from wait_bounded(cta, "kv_ready", n_it & 1, lambda k=n_it: cta.log.get(f"kr{k}", 0) == NW, "kv_ready", r)
         ok = r[0]
         for c in range(nch):
             if not ok:
                 break
             ph = (n_ch + c) & 1
             r = []
-            yield from wait_bounded(cta, "q_ready", ph, lambda k=n_ch + c: cta.log.get(f"qr{k}", 0) == 4, "q_ready", r)
+            yield from wait_bounded(cta, "q_ready", ph, lambda k=n_ch + c: cta.log.get(f"qr{k}", 0) == NW, "q_ready", r)
             if not (ok := r[0]):
                 break
             cta.later(cta.rng.randint(300, 700), "s_full", f"sf{n_ch + c}")
             r = []
-            yield from wait_bounded(cta, "p_ready", ph, lambda k=n_ch + c: cta.log.get(f"pr{k}", 0) == 4, "p_ready", r)
+            yield from wait_bounded(cta, "p_ready", ph, lambda k=n_ch + c: cta.log.get(f"pr{k}", 0) == NW, "p_ready", r)
             if not (ok := r[0]):
                 break
             d = cta.rng.randint(800, 1600)
@@ -225,7 +226,7 @@ def row_warp(cta, w):
 
 def simulate(items, seed, lose=None, late=None, per_warp=False):
     cta = Cta(items, seed, lose, late, per_warp)
-    roles = [producer(cta), issuer(cta)] + [row_warp(cta, w) for w in range(4)]
+    roles = [producer(cta), issuer(cta)] + [row_warp(cta, w) for w in range(NW)]
     # the idle warps (2, 3 and the non-leading lanes) only meet the CTA barriers
     def idle():
         for i in range(len(items)):
