@@ -55,9 +55,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel's sources have the recorded hash (kernel_source_hash; otherwise reported as null).
 NCU_TRAFFIC = {  # {config_name: (kernel_source_hash() of the captured kernel, bytes per launch)}
     # pk_attend_tc_kernel on the long batch (profiles/pk_attend_tc_kernel_long.md)
-    "long": ("6511010fddcbff84325ff2d8ef5926f2fc66e814", 1068108544),
+    "long": ("414b83eb1f91883680a3ea1527db8f3feee173ef", 1067798016),
     # pk_attend_band_kernel on the short-sequence workload (profiles/pk_attend_band_kernel_short.md)
-    "short": ("7f2a6e736eb1e3fe0bcc42af75fc83a3788cca52", 384193024),
+    "short": ("2139807925fd59237e19369393c755a854bcc03c", 382657024),
 }
 
 
