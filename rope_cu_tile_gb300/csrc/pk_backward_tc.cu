@@ -341,6 +341,15 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
         bad = group_any(!tc_wait(&B.s_full, ph, p, &s_abort));
         if (bad) break;
         tc_fence_after();
+        // the chunk's queries q this key row sees: [v_lo, v_hi) (same sequence, window, q < qend)
+        int v_lo = 0, v_hi = 0;
+        if (kok) {
+          v_lo = static_cast<int>(min(max(klo - static_cast<int64_t>(qb), static_cast<int64_t>(0)), static_cast<int64_t>(128)));
+          v_hi = static_cast<int>(min(max(min(khi, static_cast<int64_t>(qend)) - static_cast<int64_t>(qb),
+                                          static_cast<int64_t>(0)), static_cast<int64_t>(128)));
+          v_hi = max(v_hi, v_lo);
+        }
+        const float2 c1c1 = make_float2(c1, c1);
 #pragma unroll 1
         for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
           float s[32], dp[32];
@@ -349,17 +358,17 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
           uint32_t pw[16], dw[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            float pv[2], dv[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int q = 32 * cb + i + e;
-              const int64_t a = static_cast<int64_t>(qb) + q;
-              const bool vis = kok && a < static_cast<int64_t>(qend) && a >= klo && a < khi;
-              pv[e] = vis ? ex2_tc(s[i + e] * c1 - sL2[q]) : 0.f;
-              dv[e] = pv[e] * (dp[i + e] - sD[q]);
-            }
-            pw[i / 2] = Elem<BF16>::pack(pv[0], pv[1]);
-            dw[i / 2] = Elem<BF16>::pack(dv[0], dv[1]);
+            const int q = 32 * cb + i;
+            const float2 l2 = *reinterpret_cast<const float2*>(sL2 + q);
+            const float2 dd = *reinterpret_cast<const float2*>(sD + q);
+            const float2 x = __ffma2_rn(make_float2(s[i], s[i + 1]), c1c1, make_float2(-l2.x, -l2.y));
+            float p0 = ex2_tc(x.x), p1 = ex2_tc(x.y);
+            p0 = static_cast<unsigned>(q - v_lo) < static_cast<unsigned>(v_hi - v_lo) ? p0 : 0.f;
+            p1 = static_cast<unsigned>(q + 1 - v_lo) < static_cast<unsigned>(v_hi - v_lo) ? p1 : 0.f;
+            const float2 dv = __fmul2_rn(make_float2(p0, p1),
+                                         __fadd2_rn(make_float2(dp[i], dp[i + 1]), make_float2(-dd.x, -dd.y)));
+            pw[i / 2] = Elem<BF16>::pack(p0, p1);
+            dw[i / 2] = Elem<BF16>::pack(dv.x, dv.y);
           }
           // rows of P^T and dS^T: queries 32 cb .. 32 cb + 31 are chunks 4 (cb & 1) .. + 3 of tile cb / 2
           uint8_t* tp = smem + kOffPt + (cb >> 1) * kTile;
