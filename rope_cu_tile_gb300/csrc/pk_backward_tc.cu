@@ -9,10 +9,11 @@
 // from the scheduler's counter by persistent CTAs, one per SM. Per item the CTA rotates K' once
 // and walks the visible queries in chunks of 128:
 //   S^T = K' Q'^T and dP^T = V dout^T         (M = 128 keys, N = 128 queries, K = 64)  -> TMEM
-//   the row group (thread = key row) forms P^T and dS^T from both rows and writes them, and dS,
-//   to shared memory as 16-bit operands
+//   the row group (thread = key row) forms P^T and dS^T from both rows and writes them to
+//   shared memory as 16-bit operands
 //   dV += P^T dout, dK' += dS^T Q'             (M = 128 keys, N = 64, K = 128 queries) -> TMEM
 //   dQ' = dS K'                                (M = 128 queries, N = 64, K = 128 keys)  -> TMEM
+//   (dS read from the dS^T tiles as an MN-major operand)
 // and the row group (thread = query row) adds scale dQ' to the fp32 dq accumulator. At the end of
 // the item dK' and dV are complete: dk = rot^T(scale dK') and dv are rounded once and written.
 //
@@ -26,10 +27,11 @@
 // phases away from its barrier); items are separated by a CTA-wide barrier.
 //
 // Shared memory: K', V, Q', dout as 128 x 64 tiles, 128-byte swizzled as TMA lands them (row r
-// at 128 r, its 16-byte chunk c at (c ^ (r & 7)) 16); P^T, dS^T as [key][query] and dS as
-// [query][key], each two such tiles side by side (64 columns each). K-major operands advance 32
-// bytes per K step of 16 inside a tile; the MN-major ones (dout, Q', K' as the B side of the
-// products with N = 64) advance 2048 bytes (16 rows).
+// at 128 r, its 16-byte chunk c at (c ^ (r & 7)) 16); P^T, dS^T as [key][query], each two such
+// tiles side by side (64 queries each). K-major operands advance 32 bytes per K step of 16 inside
+// a tile; the MN-major ones (dout, Q', K' as the B side of the products with N = 64, and dS^T as
+// the A side of dQ' with M = 128: its two tiles are the two swizzle atoms along M) advance 2048
+// bytes (16 rows).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,7 +47,6 @@ namespace {
 
 constexpr int kTcThreads = 384;
 constexpr int kRowWarp0 = 4;              // warps 4..11: the row group, two halves of four warps
-constexpr int kRowThreads = 256;
 constexpr uint32_t kTile = 128u * 128u;   // 128 rows x 64 16-bit elements
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kTile;
@@ -54,8 +55,7 @@ constexpr uint32_t kOffO = kOffQ + kTile;       // dout of buffer b at kOffO + b
 constexpr uint32_t kQBuf = 2 * kTile;           // two chunk buffers (Q', dout), taken in turn
 constexpr uint32_t kOffPt = kOffQ + 2 * kQBuf;  // P^T  [key][query], two tiles
 constexpr uint32_t kOffSt = kOffPt + 2 * kTile; // dS^T [key][query], two tiles
-constexpr uint32_t kOffS = kOffSt + 2 * kTile;  // dS   [query][key], two tiles
-constexpr uint32_t kOffRow = kOffS + 2 * kTile; // per query of the chunk: lse log2(e), D
+constexpr uint32_t kOffRow = kOffSt + 2 * kTile; // per query of the chunk: lse log2(e), D
 struct TcBars {
   uint64_t kv_full, kv_ready, q_ready, s_full, p_ready, c_done, drain;
   uint64_t q_full[2], q_empty[2];  // per chunk buffer: loaded; its last products have read it
@@ -247,8 +247,12 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
       const uint64_t aPt1 = sdesc_sw128(smem_u32(smem + kOffPt + kTile), 16, 1024);
       const uint64_t aSt0 = sdesc_sw128(smem_u32(smem + kOffSt), 16, 1024);
       const uint64_t aSt1 = sdesc_sw128(smem_u32(smem + kOffSt + kTile), 16, 1024);
-      const uint64_t aS0 = sdesc_sw128(smem_u32(smem + kOffS), 16, 1024);
-      const uint64_t aS1 = sdesc_sw128(smem_u32(smem + kOffS + kTile), 16, 1024);
+      // dS as the A side of dQ' = dS K' (M = 128 queries, K = keys), read from the dS^T tiles
+      // [key][query] as an MN-major operand: queries 64 .. 127 are the next swizzle atom along M
+      // (the second tile, kTile bytes on), 8-key row groups 1024 bytes apart, a K step of 16 keys
+      // 2048 bytes
+      const uint64_t mSt = sdesc_sw128(smem_u32(smem + kOffSt), kTile, 1024);
+      const uint32_t idQ = idesc_f16(BF16, 128, 64, true, true);
       bool ok = tc_wait(&B.kv_ready, n_it & 1u, p, &s_abort);
       for (uint32_t c = 0; ok && c < nchunks; ++c) {
         const uint32_t ph = (n_ch + c) & 1u;
@@ -269,11 +273,11 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
         for (uint32_t ks = 0; ks < 8; ++ks) {
           const uint64_t aP = (ks < 4 ? aPt0 : aPt1) + 2 * (ks & 3u);
           const uint64_t aT = (ks < 4 ? aSt0 : aSt1) + 2 * (ks & 3u);
-          const uint64_t aD = (ks < 4 ? aS0 : aS1) + 2 * (ks & 3u);
+
           const uint32_t acc = (c > 0 || ks > 0) ? 1u : 0u;
           umma_f16_ss(tmem + kColDV, aP, mO + boff + 128 * ks, idG, acc);
           umma_f16_ss(tmem + kColDK, aT, mQ + boff + 128 * ks, idG, acc);
-          umma_f16_ss(tmem + kColDQ, aD, mK + 128 * ks, idG, ks > 0 ? 1u : 0u);
+          umma_f16_ss(tmem + kColDQ, mSt + 128 * ks, mK + 128 * ks, idQ, ks > 0 ? 1u : 0u);
         }
         umma_commit(smem_u32(&B.c_done));
         umma_commit(smem_u32(&B.q_empty[b]));
@@ -379,20 +383,10 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
             *reinterpret_cast<uint4*>(chunk_at(tp, t, ch)) = make_uint4(pw[4 * j], pw[4 * j + 1], pw[4 * j + 2], pw[4 * j + 3]);
             *reinterpret_cast<uint4*>(chunk_at(tt, t, ch)) = make_uint4(dw[4 * j], dw[4 * j + 1], dw[4 * j + 2], dw[4 * j + 3]);
           }
-          // dS [query][key]: column t of rows 32 cb .. 32 cb + 31 (key t sits in tile t / 64, chunk
-          // (t % 64) / 8, element t % 8)
-          uint8_t* ts = smem + kOffS + (t >> 6) * kTile;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int q = 32 * cb + i;
-            const uint32_t w = dw[i >> 1];
-            const uint16_t v16 = static_cast<uint16_t>((i & 1) ? (w >> 16) : (w & 0xFFFFu));
-            *reinterpret_cast<uint16_t*>(chunk_at(ts, q, (t & 63) >> 3) + 2 * (t & 7)) = v16;
-          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        asm volatile("bar.sync 1, 256;" ::: "memory");  // every column of dS is written
+        __syncwarp();  // (each warp writes only its own rows: its lanes' writes precede its arrival)
         if (lane == 0) mbar_arrive(smem_u32(&B.p_ready));
         if (c + 1 < nchunks) {
           bad = stage_chunk(c + 1);
