@@ -48,16 +48,18 @@ namespace {
 constexpr int kTcThreads = 384;
 constexpr int kRowWarp0 = 4;              // warps 4..11: the row group, two halves of four warps
 constexpr uint32_t kTile = 128u * 128u;   // 128 rows x 64 16-bit elements
-constexpr uint32_t kOffK = 0;
-constexpr uint32_t kOffV = kOffK + kTile;
-constexpr uint32_t kOffQ = kOffV + kTile;       // Q' of buffer b at kOffQ + b kQBuf
+constexpr uint32_t kOffK = 0;                   // K' of item buffer b at kOffK + b kKVBuf
+constexpr uint32_t kOffV = kOffK + kTile;       // V of item buffer b at kOffV + b kKVBuf
+constexpr uint32_t kKVBuf = 2 * kTile;          // two item buffers (K', V), taken in turn
+constexpr uint32_t kOffQ = kOffK + 2 * kKVBuf;  // Q' of buffer b at kOffQ + b kQBuf
 constexpr uint32_t kOffO = kOffQ + kTile;       // dout of buffer b at kOffO + b kQBuf
 constexpr uint32_t kQBuf = 2 * kTile;           // two chunk buffers (Q', dout), taken in turn
 constexpr uint32_t kOffPt = kOffQ + 2 * kQBuf;  // P^T  [key][query], two tiles
 constexpr uint32_t kOffSt = kOffPt + 2 * kTile; // dS^T [key][query], two tiles
 constexpr uint32_t kOffRow = kOffSt + 2 * kTile; // per query of the chunk: lse log2(e), D
 struct TcBars {
-  uint64_t kv_full, kv_ready, q_ready, s_full, p_ready, c_done, drain;
+  uint64_t kv_ready, q_ready, s_full, p_ready, c_done, drain;
+  uint64_t kv_full[2];             // per item buffer: K and V loaded
   uint64_t q_full[2], q_empty[2];  // per chunk buffer: loaded; its last products have read it
 };
 constexpr uint32_t kOffBar = kOffRow + 2 * 128 * 4;
@@ -165,7 +167,8 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
   const int64_t ldq = 3 * hd;
 
   if (tid == 0) {
-    mbar_init(smem_u32(&B.kv_full), 1);
+    mbar_init(smem_u32(&B.kv_full[0]), 1);
+    mbar_init(smem_u32(&B.kv_full[1]), 1);
     mbar_init(smem_u32(&B.kv_ready), 8);
     mbar_init(smem_u32(&B.q_full[0]), 1);
     mbar_init(smem_u32(&B.q_full[1]), 1);
@@ -200,8 +203,10 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
   const uint32_t idS = idesc_f16(BF16, 128, 128, false, false);
   const uint32_t idG = idesc_f16(BF16, 128, 64, false, true);
 
+  // items are claimed one ahead: the first here, each next one by the producer (thread 0) while
+  // the current one runs, so that it can load the next item's K, V and first query chunk early
+  if (tid == 0) s_item = atomicAdd(&p.ctl->next, 1u);
   for (;;) {
-    if (tid == 0) s_item = atomicAdd(&p.ctl->next, 1u);
     __syncthreads();
     tc_fence_after();
     const unsigned int item = s_item;
@@ -215,34 +220,52 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
     const uint32_t nchunks = (rec.nk + 127u) / 128u;
 
     if (warp == 0 && lane == 0) {
-      // producer: K and V of the key tile, then Q and dout of each chunk into the chunk buffers
-      // in turn (global chunk g into buffer g & 1, its (g >> 1)-th use), each once the products
-      // of the chunk two back, which read that buffer, have completed -- so the next chunk's
-      // copy is in flight while the current one is worked on
-      mbar_arrive_expect_tx(smem_u32(&B.kv_full), 2 * kTile);
-      tma_load_2d(smem_u32(smem + kOffK), &tmap_qkv, smem_u32(&B.kv_full), static_cast<int32_t>(hd + h * 64),
-                  static_cast<int32_t>(rec.q0));
-      tma_load_2d(smem_u32(smem + kOffV), &tmap_qkv, smem_u32(&B.kv_full), static_cast<int32_t>(2 * hd + h * 64),
-                  static_cast<int32_t>(rec.q0));
-      ++kv_loads;
-      for (uint32_t c = 0; c < nchunks; ++c) {
-        const uint32_t g = n_ch + c, b = g & 1u;
-        if (g >= 2 && !tc_wait(&B.q_empty[b], ((g >> 1) - 1u) & 1u, p, &s_abort)) break;
-        const int32_t qb = static_cast<int32_t>(rec.k0 + 128u * c);
+      // producer: K and V of an item into item buffer (item count) & 1, then Q and dout of each
+      // chunk into the chunk buffers in turn (global chunk g into buffer g & 1, its (g >> 1)-th
+      // use), each once the products of the chunk two back, which read that buffer, have
+      // completed -- so the next chunk's copy is in flight while the current one is worked on.
+      // The next item's K, V and first chunk are loaded before this item ends.
+      auto load_kv = [&](const TileRec& r, int hh) {
+        const uint32_t kb = kv_loads & 1u;
+        mbar_arrive_expect_tx(smem_u32(&B.kv_full[kb]), 2 * kTile);
+        tma_load_2d(smem_u32(smem + kOffK + kb * kKVBuf), &tmap_qkv, smem_u32(&B.kv_full[kb]),
+                    static_cast<int32_t>(hd + hh * 64), static_cast<int32_t>(r.q0));
+        tma_load_2d(smem_u32(smem + kOffV + kb * kKVBuf), &tmap_qkv, smem_u32(&B.kv_full[kb]),
+                    static_cast<int32_t>(2 * hd + hh * 64), static_cast<int32_t>(r.q0));
+        ++kv_loads;
+      };
+      auto load_chunk = [&](const TileRec& r, int hh, uint32_t g, uint32_t c) -> bool {
+        const uint32_t b = g & 1u;
+        if (g >= 2 && !tc_wait(&B.q_empty[b], ((g >> 1) - 1u) & 1u, p, &s_abort)) return false;
+        const int32_t qb = static_cast<int32_t>(r.k0 + 128u * c);
         mbar_arrive_expect_tx(smem_u32(&B.q_full[b]), 2 * kTile);
-        tma_load_2d(smem_u32(smem + kOffQ + b * kQBuf), &tmap_qkv, smem_u32(&B.q_full[b]), static_cast<int32_t>(h * 64), qb);
-        tma_load_2d(smem_u32(smem + kOffO + b * kQBuf), &tmap_dout, smem_u32(&B.q_full[b]), static_cast<int32_t>(h * 64), qb);
+        tma_load_2d(smem_u32(smem + kOffQ + b * kQBuf), &tmap_qkv, smem_u32(&B.q_full[b]), static_cast<int32_t>(hh * 64), qb);
+        tma_load_2d(smem_u32(smem + kOffO + b * kQBuf), &tmap_dout, smem_u32(&B.q_full[b]), static_cast<int32_t>(hh * 64), qb);
         ++q_loads;
+        return true;
+      };
+      const bool first = n_it == 0;  // nothing of this item was loaded ahead
+      bool ok = true;
+      if (first) load_kv(rec, h);
+      for (uint32_t c = first ? 0u : 1u; ok && c < nchunks; ++c) ok = load_chunk(rec, h, n_ch + c, c);
+      const unsigned int nxt = atomicAdd(&p.ctl->next, 1u);
+      if (ok && nxt < n_items) {
+        const TileRec rn = p.tiles[nxt / static_cast<unsigned int>(H)];
+        const int hn = static_cast<int>(nxt % static_cast<unsigned int>(H));
+        load_kv(rn, hn);
+        load_chunk(rn, hn, n_ch + nchunks, 0u);
       }
+      s_item = nxt;  // read by every thread after the next CTA-wide barrier
     } else if (warp == 1 && lane == 0) {
       // MMA issuer
-      const uint64_t aK = sdesc_sw128(smem_u32(smem + kOffK), 16, 1024);
-      const uint64_t aV = sdesc_sw128(smem_u32(smem + kOffV), 16, 1024);
+      const uint32_t kvo = (n_it & 1u) * kKVBuf;  // this item's K / V buffer
+      const uint64_t aK = sdesc_sw128(smem_u32(smem + kOffK + kvo), 16, 1024);
+      const uint64_t aV = sdesc_sw128(smem_u32(smem + kOffV + kvo), 16, 1024);
       const uint64_t bQ = sdesc_sw128(smem_u32(smem + kOffQ), 16, 1024);
       const uint64_t bO = sdesc_sw128(smem_u32(smem + kOffO), 16, 1024);
       const uint64_t mO = sdesc_sw128(smem_u32(smem + kOffO), 8192, 1024);  // dout as MN-major B
       const uint64_t mQ = sdesc_sw128(smem_u32(smem + kOffQ), 8192, 1024);  // Q' as MN-major B
-      const uint64_t mK = sdesc_sw128(smem_u32(smem + kOffK), 8192, 1024);  // K' as MN-major B
+      const uint64_t mK = sdesc_sw128(smem_u32(smem + kOffK + kvo), 8192, 1024);  // K' as MN-major B
       const uint64_t aPt0 = sdesc_sw128(smem_u32(smem + kOffPt), 16, 1024);
       const uint64_t aPt1 = sdesc_sw128(smem_u32(smem + kOffPt + kTile), 16, 1024);
       const uint64_t aSt0 = sdesc_sw128(smem_u32(smem + kOffSt), 16, 1024);
@@ -304,9 +327,11 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
           khi = min(se, static_cast<int64_t>(b) + p.window + 1);
         }
       }
-      bool bad = group_any(!tc_wait(&B.kv_full, n_it & 1u, p, &s_abort));
+      bool bad = group_any(!tc_wait(&B.kv_full[n_it & 1u], (n_it >> 1) & 1u, p, &s_abort));
       if (!bad) {
-        if (kok) rotate_row<BF16>(smem + kOffK, t, p.cos_t, p.sin_t, static_cast<uint32_t>(b - kstart), 2 * hf);
+        if (kok)
+          rotate_row<BF16>(smem + kOffK + (n_it & 1u) * kKVBuf, t, p.cos_t, p.sin_t, static_cast<uint32_t>(b - kstart),
+                           2 * hf);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&B.kv_ready));
@@ -458,7 +483,9 @@ pk_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_cons
 
   // the producer's copies in flight land before the CTA's shared memory goes away
   if (warp == 0 && lane == 0 && s_abort) {
-    if (kv_loads) mbar_wait(smem_u32(&B.kv_full), (kv_loads - 1u) & 1u, p.timeout_ns);
+    // K / V loads go to item buffer (load count) & 1: the last load of each buffer
+    for (uint32_t k = kv_loads >= 2 ? kv_loads - 2 : 0; k < kv_loads; ++k)
+      mbar_wait(smem_u32(&B.kv_full[k & 1u]), (k >> 1) & 1u, p.timeout_ns);
     // chunk loads go to buffer g & 1 in the order of the CTA's global chunk index g, as
     // q_loads counts them: the last load of each buffer
     for (uint32_t g = q_loads >= 2 ? q_loads - 2 : 0; g < q_loads; ++g)

@@ -1,6 +1,7 @@
 """A discrete-event model of the hand-off protocol of the tcgen05 backward kernel
 (rope_cu_tile_gb300/csrc/pk_backward_tc.cu): the TMA producer (query chunks into two buffers in
-turn, each reloaded once the products that read it have completed), the MMA issuer, the eight warps
+turn, each reloaded once the products that read it have completed; the next item's K / V, into the
+other of two item buffers, and first chunk loaded before the current item ends), the MMA issuer, the eight warps
 of the row group (with their group barriers: a reducing barrier for each give-up decision and
 the plain ones between their shared-memory writes and reads; chunk c + 1 staged right after chunk
 c's probabilities), and the CTA-wide barrier between work items.
@@ -53,7 +54,7 @@ class Cta:
         self.lose = lose  # name of the arrival to drop, or None
         self.late = late  # name of the arrival to deliver at about the wait bound
         self.per_warp = per_warp  # negative control: each warp of the row group decides alone
-        self.bar = {k: Barrier(c) for k, c in (("kv_full", 1), ("kv_ready", NW), ("q_full0", 1), ("q_full1", 1),
+        self.bar = {k: Barrier(c) for k, c in (("kv_full0", 1), ("kv_full1", 1), ("kv_ready", NW), ("q_full0", 1), ("q_full1", 1),
                                                ("q_empty0", 1), ("q_empty1", 1), ("q_ready", NW),
                                                ("s_full", 1), ("p_ready", NW), ("c_done", 1), ("drain", 1))}
         self.group = {}  # named-barrier instance -> arrivals (and OR of the flags)
@@ -115,21 +116,35 @@ def cta_barrier(cta, tag, n=3 + NW):  # producer, issuer, the row group's warps,
 
 
 def producer(cta):
+    """Item i's K / V go to item buffer i & 1; the next item's K / V and first chunk are loaded
+    before the current item ends (only the CTA's first item is loaded at its start)."""
     n_it = n_ch = 0
+
+    def load_chunk(g):
+        if g >= 2:
+            r = []
+            yield from wait_bounded(cta, f"q_empty{g & 1}", ((g >> 1) - 1) & 1,
+                                    lambda k=g - 2: cta.log.get(f"qe{k}", 0) == 1, f"q_empty {g - 2}", r)
+            if not r[0]:
+                return False
+        cta.later(cta.rng.randint(300, 1500), f"q_full{g & 1}", f"q{g}")
+        return True
+
     for i, nch in enumerate(cta.items):
         yield from cta_barrier(cta, ("item", i))
         if cta.abort:
             break
-        cta.later(cta.rng.randint(300, 1500), "kv_full", f"kv{n_it}")
-        for c in range(nch):
-            g = n_ch + c
-            if g >= 2:
-                r = []
-                yield from wait_bounded(cta, f"q_empty{g & 1}", ((g >> 1) - 1) & 1,
-                                        lambda k=g - 2: cta.log.get(f"qe{k}", 0) == 1, f"q_empty {g - 2}", r)
-                if not r[0]:
-                    break
-            cta.later(cta.rng.randint(300, 1500), f"q_full{g & 1}", f"q{g}")
+        first = i == 0
+        if first:
+            cta.later(cta.rng.randint(300, 1500), "kv_full0", "kv0")
+        ok = True
+        for c in range(0 if first else 1, nch):
+            ok = yield from load_chunk(n_ch + c)
+            if not ok:
+                break
+        if ok and i + 1 < len(cta.items):
+            cta.later(cta.rng.randint(300, 1500), f"kv_full{(i + 1) & 1}", f"kv{i + 1}")
+            yield from load_chunk(n_ch + nch)
         n_it += 1
         n_ch += nch
     yield from cta_barrier(cta, "end")
@@ -176,7 +191,8 @@ def row_warp(cta, w):
             break
         r = []
         yield ("delay", cta.rng.randint(1, 1500))  # warps reach their waits at different times
-        yield from wait_bounded(cta, "kv_full", n_it & 1, lambda k=n_it: cta.log.get(f"kv{k}", 0) == 1, "kv_full", r)
+        yield from wait_bounded(cta, f"kv_full{n_it & 1}", (n_it >> 1) & 1, lambda k=n_it: cta.log.get(f"kv{k}", 0) == 1,
+                                "kv_full", r)
         bad = yield from group_barrier(cta, ("kv", n_it), not r[0])
         if not bad:
             yield ("delay", cta.rng.randint(50, 300))
