@@ -65,3 +65,13 @@ def test_clock_summary():
     assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 3
     c.lines = []
     assert c.summary() is None
+
+
+def test_kernel_tables_cover_every_forward_kernel():
+    """Every forward kernel id has a name and a source file in the bench's tables (the roofline's
+    traffic record is keyed by that source's hash)."""
+    bench = _load("bench")
+    assert set(bench.KERNEL_NAMES) == set(bench.KERNEL_SOURCES) == set(range(6))
+    for k, src in bench.KERNEL_SOURCES.items():
+        assert os.path.exists(os.path.join(ROOT, "rope_cu_tile_gb300", "csrc", src)), (k, src)
+        assert len(bench.kernel_source_hash(k)) == 40
