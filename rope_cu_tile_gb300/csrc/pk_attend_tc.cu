@@ -484,10 +484,12 @@ __device__ void producer(const CUtensorMap* tmap, const Params& p, uint8_t* smem
 // sub-partitions, so that each keeps its share of the tensor pipe fed). For every stream
 // tile t: once K(t) is rotated, S_X(t) = Q_X K(t)^T if X's range holds t (after Q_X is
 // rotated and S_X's previous scores were read); then, once V(t - 1) has landed,
-// O_X += P_X(t - 1) V(t - 1) if X's range holds t - 1 (after P_X is written). K and V ring
-// stages are released by both issuers (barriers of count 2): by a commit after the MMAs
-// that read them, or by a plain arrival for a tile outside X's range -- made only after the
-// tile's own ready / full phase was seen, so an issuer never runs a phase ahead.
+// O_X += P_X(t - 1) V(t - 1) if X's range holds t - 1 (after P_X is written); a tile outside
+// X's range is seen after that product, so the last PV of the range does not wait for the
+// rotation of the next tile. K and V ring stages are released by both issuers (barriers of
+// count 2): by a commit after the MMAs that read them, or by a plain arrival for a tile
+// outside X's range -- made only after the tile's own ready / full phase was seen. Every
+// stage's phases are waited for in order: a parity wait is only sound one phase at a time.
 
 __device__ void mma_issuer(const Params& p, uint8_t* smem, Meta* meta, uint32_t tmem, bool bf16, int x) {
   Bars& B = meta->bars;
@@ -519,39 +521,38 @@ __device__ void mma_issuer(const Params& p, uint8_t* smem, Meta* meta, uint32_t 
     ++it;
     if (!valid) break;
     for (uint32_t t = 0; t <= n && !bad; ++t) {
-      if (t < n) {
+      // a tile of X's range: S_X(t) now; any other tile: seen after O_X += P_X(t - 1) V(t - 1),
+      // so that the last PV of the range is not held back by the next tile's rotation
+      const bool own = t < n && t >= lo && t < hi;
+      if (own) {
         if (!wait_bar(meta, p.ctl, &B.k_ready[kst], kph, p.timeout_ns)) {
           bad = true;
           break;
         }
-        if (t >= lo && t < hi) {
-          const uint32_t qb = qn & 1u;
-          if (t == lo && !wait_bar(meta, p.ctl, &B.q_ready[x][qb], (qn >> 1) & 1u, p.timeout_ns)) {
+        const uint32_t qb = qn & 1u;
+        if (t == lo && !wait_bar(meta, p.ctl, &B.q_ready[x][qb], (qn >> 1) & 1u, p.timeout_ns)) {
+          bad = true;
+          break;
+        }
+        if (pend) {
+          if (!wait_bar(meta, p.ctl, &B.s_consumed[x], sc & 1u, p.timeout_ns)) {
             bad = true;
             break;
           }
-          if (pend) {
-            if (!wait_bar(meta, p.ctl, &B.s_consumed[x], sc & 1u, p.timeout_ns)) {
-              bad = true;
-              break;
-            }
-            ++sc;
-          }
-          tc_fence_after();
-          const uint64_t dq = dq0 + qb * 1024, dk = dk0 + kst * 1024;
-          umma_f16_ss(tS, dq, dk, idesc_s, 0u);
-          umma_f16_ss(tS, dq + 2, dk + 2, idesc_s, 1u);
-          umma_f16_ss(tS, dq + 4, dk + 4, idesc_s, 1u);
-          umma_f16_ss(tS, dq + 6, dk + 6, idesc_s, 1u);
-          umma_commit(smem_u32(&B.s_full[x]));
-          umma_commit(smem_u32(&B.k_empty[kst]));
-          pend = true;
-          if (t + 1 == hi) {
-            umma_commit(smem_u32(&B.q_empty[x][qb]));
-            ++qn;
-          }
-        } else {
-          mbar_arrive(smem_u32(&B.k_empty[kst]));
+          ++sc;
+        }
+        tc_fence_after();
+        const uint64_t dq = dq0 + qb * 1024, dk = dk0 + kst * 1024;
+        umma_f16_ss(tS, dq, dk, idesc_s, 0u);
+        umma_f16_ss(tS, dq + 2, dk + 2, idesc_s, 1u);
+        umma_f16_ss(tS, dq + 4, dk + 4, idesc_s, 1u);
+        umma_f16_ss(tS, dq + 6, dk + 6, idesc_s, 1u);
+        umma_commit(smem_u32(&B.s_full[x]));
+        umma_commit(smem_u32(&B.k_empty[kst]));
+        pend = true;
+        if (t + 1 == hi) {
+          umma_commit(smem_u32(&B.q_empty[x][qb]));
+          ++qn;
         }
         kst = (kst + 1) & (kKStages - 1);
         kph ^= kst == 0 ? 1u : 0u;
@@ -580,6 +581,15 @@ __device__ void mma_issuer(const Params& p, uint8_t* smem, Meta* meta, uint32_t 
         }
         vst = vst + 1 == kVStages ? 0u : vst + 1;
         vph ^= vst == 0 ? 1u : 0u;
+      }
+      if (t < n && !own) {
+        if (!wait_bar(meta, p.ctl, &B.k_ready[kst], kph, p.timeout_ns)) {
+          bad = true;
+          break;
+        }
+        mbar_arrive(smem_u32(&B.k_empty[kst]));
+        kst = (kst + 1) & (kKStages - 1);
+        kph ^= kst == 0 ? 1u : 0u;
       }
     }
     if (bad) break;
@@ -1025,9 +1035,9 @@ pk_attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_c
   tc_fence_after();
 
   // Register split (warpgroup-wide): the launch gives 512 x 128 = 65536 registers; the
-  // producer / MMA warpgroup drops to 80 and the rotation warpgroup to 96 (the code after a
-  // decrease is compiled within it), and the two softmax warpgroups rise to 160 (their code is
-  // compiled within the launch's 128 either way): 128 x 80 + 128 x 96 + 256 x 160 = 63488.
+  // producer / MMA warpgroup drops to 80 and the rotation warpgroup to 96, and the two softmax
+  // warpgroups rise to 160 (ptxas compiles the code after each change within the new count;
+  // the softmax code needs no more than 128): 128 x 80 + 128 x 96 + 256 x 160 = 63488.
   if (warp < kWarpRot) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
     // (each role reads what it needs after its own register change: nothing computed

@@ -15,7 +15,8 @@ of its thread has completed; a TMA load arrives on its barrier after a random la
 
 Score-buffer protocols:
 - one_buffer: the kernel as built. One score buffer per query tile; S(t) waits until that tile's
-  softmax warps have loaded the last half of S(t - 1) (`s_consumed`).
+  softmax warps have loaded the last half of S(t - 1) (`s_consumed`); an issuer sees a key tile
+  outside its query tile's range after the PV of the tile before it.
 - three_buffers: three score buffers shared by both query tiles, P written over the buffer its S
   came from, products numbered in stream order (A before B at a tile) and product n using
   buffer n % 3; S(n) waits for the PV of product n - 3 (`s_free`), for the softmax to have seen
@@ -23,12 +24,16 @@ Score-buffer protocols:
   counter that only grows).
 - three_buffers_unordered, three_buffers_no_taken: the same without the last two waits, or
   without `s_taken`; both are unsound and the model must find it.
+- one_buffer_skip: one_buffer with issuers that never wait for a key or value tile outside their
+  query tile's range (the issuer whose range holds the tile arrives in the other's place). A
+  stage's next wait then names a phase two ahead of the one last seen, which a parity test cannot
+  tell from the one before: unsound, and the model must find it.
 """
 import random
 
 import pytest
 
-PROTOCOLS = ("one_buffer", "three_buffers", "three_buffers_unordered", "three_buffers_no_taken")
+PROTOCOLS = ("one_buffer", "one_buffer_skip", "three_buffers", "three_buffers_unordered", "three_buffers_no_taken")
 K_STAGES, V_STAGES = 4, 3
 ITEM_CONSUMERS = 2 + 4 + 4 + 4  # issuers, rotation warps, softmax warps of A and of B
 
@@ -206,7 +211,8 @@ def rotation_warp(m):
 
 def issuer(m, x):
     proto = m.protocol
-    shared = proto != "one_buffer"
+    shared = proto not in ("one_buffer", "one_buffer_skip")
+    skip = proto == "one_buffer_skip"
     ordered = proto in ("three_buffers", "three_buffers_no_taken")
     with_taken = proto == "three_buffers"
     kn = vn = qn = 0
@@ -219,12 +225,15 @@ def issuer(m, x):
         a1, b0, b1, ns = m.items[i]
         lo, hi = (0, a1) if x == 0 else (b0, b1)
         for t in range(ns + 1):
-            if t < ns:
+            own = t < ns and lo <= t < hi
+            # as built, a tile outside X's range is seen after the PV of the previous tile
+            late = not shared and not own
+            if t < ns and not late:
                 g = kn
                 st = g % K_STAGES
                 yield m.wait(("k_ready", st), (g // K_STAGES) & 1, lambda g=g: m.count(f"krot{g}") == 4,
                              f"K{g} rotated")
-                if lo <= t < hi:
+                if own:
                     n = m.number[(i, t, x)]
                     q, qb = qn, qn & 1
                     if t == lo:
@@ -247,6 +256,9 @@ def issuer(m, x):
                     m.mma(x, m.rng.randint(200, 400), f"s{n}")
                     m.commit(x, ("s_full", x))
                     m.commit(x, ("k_empty", st), f"kfree{g}")
+                    olo, ohi = (b0, b1) if x == 0 else (0, a1)
+                    if skip and not (olo <= t < ohi):
+                        m.arrive(("k_empty", st), f"kfree{g}")
                     if ordered:
                         m.issued = n + 1
                     n_s += 1
@@ -257,7 +269,9 @@ def issuer(m, x):
                 else:
                     m.arrive(("k_empty", st), f"kfree{g}")
                 kn += 1
-            if t >= 1:
+            if t >= 1 and skip and not (lo <= t - 1 < hi):
+                vn += 1
+            elif t >= 1:
                 g = vn
                 st = g % V_STAGES
                 yield m.wait(("v_full", st), (g // V_STAGES) & 1, lambda g=g: m.count(f"vland{g}") == 1, f"V{g} landed")
@@ -269,15 +283,27 @@ def issuer(m, x):
                     m.mma(x, m.rng.randint(300, 600), f"pv{n}")
                     m.commit(x, ("pv_done", x))
                     m.commit(x, ("v_empty", st), f"vfree{g}")
+                    olo, ohi = (b0, b1) if x == 0 else (0, a1)
+                    if skip and not (olo <= t - 1 < ohi):
+                        m.arrive(("v_empty", st), f"vfree{g}")
                     if shared:
                         m.commit(x, ("s_free", n % 3))
                 else:
                     m.arrive(("v_empty", st), f"vfree{g}")
                 vn += 1
+            if t < ns and late and skip:
+                kn += 1
+            elif t < ns and late:
+                g = kn
+                st = g % K_STAGES
+                yield m.wait(("k_ready", st), (g // K_STAGES) & 1, lambda g=g: m.count(f"krot{g}") == 4,
+                             f"K{g} rotated")
+                m.arrive(("k_empty", st), f"kfree{g}")
+                kn += 1
 
 
 def softmax_warp(m, x):
-    shared = m.protocol != "one_buffer"
+    shared = m.protocol not in ("one_buffer", "one_buffer_skip")
     with_taken = m.protocol == "three_buffers"
     n_s = n_pv = 0
     for i in range(len(m.items) + 1):
@@ -387,7 +413,7 @@ def test_protocol_sound(protocol):
     assert not bad, bad[:3]
 
 
-@pytest.mark.parametrize("protocol", ["three_buffers_unordered", "three_buffers_no_taken"])
+@pytest.mark.parametrize("protocol", ["three_buffers_unordered", "three_buffers_no_taken", "one_buffer_skip"])
 def test_model_finds_unsound_protocols(protocol):
     # negative controls: each lacks a wait the sound protocol has, and the model must notice
     bad = failures(protocol, range(60))
