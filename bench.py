@@ -55,7 +55,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel's sources have the recorded hash (kernel_source_hash; otherwise reported as null).
 NCU_TRAFFIC = {  # {config_name: (kernel_source_hash() of the captured kernel, bytes per launch)}
     # pk_attend_tc_kernel on the long batch (profiles/pk_attend_tc_kernel_long.md)
-    "long": ("414b83eb1f91883680a3ea1527db8f3feee173ef", 1067798016),
+    "long": ("cad64bfb4ee0faeb8642869856974c8a0c838bbc", 1067494144),
     # pk_attend_band_kernel on the short-sequence workload (profiles/pk_attend_band_kernel_short.md)
     "short": ("2139807925fd59237e19369393c755a854bcc03c", 382657024),
 }
