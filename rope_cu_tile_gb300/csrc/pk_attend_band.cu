@@ -210,8 +210,10 @@ __device__ __forceinline__ void sts8(float* p, const float (&y)[8]) {
 // rows of its block (R = 4 for W <= 4, else 2; 8 R rows per pass) and 16 of the 64 features:
 // the 4-feature granules e, e + 4, e + 8, e + 12, which hold both members of their rotary
 // pairs (u, u + 32). Each key row it loads serves up to R of its rows: the partial scores
-// of its features are summed over the four lanes of the group by two shuffles, and its
-// share of out accumulates from the value granules of the same features.
+// of its features are summed over the four lanes of the group (with R = 4 by two exchange
+// rounds that leave lane e the whole scores of row e, whose softmax it takes alone before
+// the weights are shared again; otherwise by two shuffles of every sum), and its share of
+// out accumulates from the value granules of the same features.
 template <typename F, int OUT, int W>
 __global__ void __launch_bounds__(kBandRows * BandSmem<F, W>::kHeads)
 pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, const F* __restrict__ sin_t,
@@ -266,6 +268,8 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
   // this lane's raw q granules (e, e + 4, e + 8, e + 12) of the R rows it takes first, into
   // registers while the copies are in flight
   const int g = lane >> 2, e = lane & 3;
+  // scores in base-2 units: q' carries scale * log2(e), so each weight is one ex2
+  const float sl2 = scale * 1.4426950408889634f;
   using QG = Granule<F>;
   typename QG::type qraw[R][4];
   auto load_q = [&](int rb) {
@@ -369,8 +373,8 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
         lds4(&s_tab[r][1][u], ts);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          qv[i][4 * c + k] = (x1[k] * tc[k] - x2[k] * ts[k]) * scale;
-          qv[i][8 + 4 * c + k] = (x1[k] * ts[k] + x2[k] * tc[k]) * scale;
+          qv[i][4 * c + k] = (x1[k] * tc[k] - x2[k] * ts[k]) * sl2;
+          qv[i][8 + 4 * c + k] = (x1[k] * ts[k] + x2[k] * tc[k]) * sl2;
         }
       }
     }
@@ -407,30 +411,87 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
     // whole scores (the four lanes of the group), the mask, the softmax
     float l[R], m[R];
     bool ok[R];
+    if constexpr (R == 4) {
+      // Lane e of a group finishes row e alone: two exchange rounds (each sends the half of its
+      // partial sums it does not keep) leave it the whole scores of its row; it takes that row's
+      // softmax, and the four rows' weights, maxima and sums are then shared within the group.
+      const bool hi2 = (e & 2) != 0, hi1 = (e & 1) != 0;
+      float h[2][2 * W + 1];
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      const long long a = t0 + rb + i;
-      ok[i] = a < T;
-      const int r = rb + i + W;
-      const int lo = ok[i] ? max(s_seq_lo[r], static_cast<int>(a) - window) : 0;
-      const int hi = ok[i] ? min(s_seq_hi[r], static_cast<int>(a) + window + 1) : 0;
-      m[i] = -INFINITY;
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int d = 0; d <= 2 * W; ++d) {
+          const float keep = hi2 ? ps[i + 2][d] : ps[i][d];
+          const float send = hi2 ? ps[i][d] : ps[i + 2][d];
+          h[i][d] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+      float sr[2 * W + 1];
 #pragma unroll
       for (int d = 0; d <= 2 * W; ++d) {
-        float x = ps[i][d];
-        x += __shfl_xor_sync(0xffffffffu, x, 1);
-        x += __shfl_xor_sync(0xffffffffu, x, 2);
-        const long long j = a - W + d;
-        x = (j >= lo && j < hi) ? x : -INFINITY;
-        ps[i][d] = x;
-        m[i] = fmaxf(m[i], x);
+        const float keep = hi1 ? h[1][d] : h[0][d];
+        const float send = hi1 ? h[0][d] : h[1][d];
+        sr[d] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
       }
-      l[i] = 0.f;
+      const long long a = t0 + rb + e;
+      const bool oke = a < T;
+      const int r = rb + e + W;
+      const int aw = static_cast<int>(a) - W;
+      const int dlo = oke ? max(s_seq_lo[r], static_cast<int>(a) - window) - aw : 0;
+      const int dhi = oke ? min(s_seq_hi[r], static_cast<int>(a) + window + 1) - aw : 0;
+      float me = -INFINITY;
 #pragma unroll
       for (int d = 0; d <= 2 * W; ++d) {
-        const float pw = ok[i] ? __expf(ps[i][d] - m[i]) : 0.f;
-        ps[i][d] = pw;
-        l[i] += pw;
+        const float x = (d >= dlo && d < dhi) ? sr[d] : -INFINITY;
+        sr[d] = x;
+        me = fmaxf(me, x);
+      }
+      float le = 0.f;
+#pragma unroll
+      for (int d = 0; d <= 2 * W; ++d) {
+        float pw;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(pw) : "f"(sr[d] - me));
+        pw = oke ? pw : 0.f;
+        sr[d] = pw;
+        le += pw;
+      }
+      const int grp = lane & ~3;
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+#pragma unroll
+        for (int d = 0; d <= 2 * W; ++d) ps[i][d] = __shfl_sync(0xffffffffu, sr[d], grp | i);
+        l[i] = __shfl_sync(0xffffffffu, le, grp | i);
+        m[i] = __shfl_sync(0xffffffffu, me, grp | i);
+        ok[i] = t0 + rb + i < T;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const long long a = t0 + rb + i;
+        ok[i] = a < T;
+        const int r = rb + i + W;
+        // key a - W + d is visible for d in [dlo, dhi) (tokens < 2^31)
+        const int aw = static_cast<int>(a) - W;
+        const int dlo = ok[i] ? max(s_seq_lo[r], static_cast<int>(a) - window) - aw : 0;
+        const int dhi = ok[i] ? min(s_seq_hi[r], static_cast<int>(a) + window + 1) - aw : 0;
+        m[i] = -INFINITY;
+#pragma unroll
+        for (int d = 0; d <= 2 * W; ++d) {
+          float x = ps[i][d];
+          x += __shfl_xor_sync(0xffffffffu, x, 1);
+          x += __shfl_xor_sync(0xffffffffu, x, 2);
+          x = (d >= dlo && d < dhi) ? x : -INFINITY;
+          ps[i][d] = x;
+          m[i] = fmaxf(m[i], x);
+        }
+        l[i] = 0.f;
+#pragma unroll
+        for (int d = 0; d <= 2 * W; ++d) {
+          float pw;
+          asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(pw) : "f"(ps[i][d] - m[i]));
+          pw = ok[i] ? pw : 0.f;
+          ps[i][d] = pw;
+          l[i] += pw;
+        }
       }
     }
     // out: the lane's features of each row, from the value granules of key rb + kk
@@ -474,7 +535,7 @@ pk_attend_band_kernel(const F* __restrict__ qkv, const F* __restrict__ cos_t, co
         const float y2 = o[i][2 * c + 1].x * inv, y3 = o[i][2 * c + 1].y * inv;
         store4<OUT>(out, at + 4 * (e + 4 * c), y0, y1, y2, y3);
       }
-      if (e == 0) lse[static_cast<int64_t>(h) * T + a] = m[i] + logf(l[i]);
+      if (e == 0) lse[static_cast<int64_t>(h) * T + a] = m[i] * 0.6931471805599453f + logf(l[i]);
     }
   }
 }
