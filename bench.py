@@ -57,7 +57,7 @@ NCU_TRAFFIC = {  # {config_name: (kernel_source_hash() of the captured kernel, b
     # pk_attend_tc_kernel on the long batch (profiles/pk_attend_tc_kernel_long.md)
     "long": ("cad64bfb4ee0faeb8642869856974c8a0c838bbc", 1067494144),
     # pk_attend_band_kernel on the short-sequence workload (profiles/pk_attend_band_kernel_short.md)
-    "short": ("2139807925fd59237e19369393c755a854bcc03c", 382657024),
+    "short": ("7e911277ba6985bdc10e830c5b59631600b83deb", 382067200),
 }
 
 
