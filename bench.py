@@ -55,7 +55,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel's sources have the recorded hash (kernel_source_hash; otherwise reported as null).
 NCU_TRAFFIC = {  # {config_name: (kernel_source_hash() of the captured kernel, bytes per launch)}
     # pk_attend_tc_kernel on the long batch (profiles/pk_attend_tc_kernel_long.md)
-    "long": ("cad64bfb4ee0faeb8642869856974c8a0c838bbc", 1067494144),
+    "long": ("2e6a5db189da945cdacae7f6da011250fa218392", 1067494144),
     # pk_attend_band_kernel on the short-sequence workload (profiles/pk_attend_band_kernel_short.md)
     "short": ("7e911277ba6985bdc10e830c5b59631600b83deb", 382067200),
 }
