@@ -24,6 +24,21 @@ def test_bench_imports_and_traffic_table():
     assert len(bench.kernel_source_hash()) == 40
 
 
+def test_traffic_records_name_no_other_kernel():
+    # a recorded capture is keyed by the source hash of the kernel that workload runs by default
+    # (windows 1..16: the narrow-window kernel; otherwise the paired tensor-core kernel, 16-bit
+    # inputs): it must not be the hash of another kernel's sources
+    import synth
+
+    bench = _load("bench")
+    for name, (sha, _) in bench.NCU_TRAFFIC.items():
+        w = synth.make_config("tiny").window if name == "tiny" else {"global": 0, "local": 64, "long": 0, "short": 4}[name]
+        own = 0 if 1 <= w <= 16 else 2
+        others = {bench.kernel_source_hash(k) for k in bench.KERNEL_SOURCES
+                  if bench.KERNEL_SOURCES[k] != bench.KERNEL_SOURCES[own]}
+        assert sha not in others, f"{name}: traffic recorded under another kernel's source hash"
+
+
 def test_graft_entry_imports():
     entry = _load("__graft_entry__")
     assert callable(entry.build) and callable(entry.smoke)
