@@ -218,7 +218,7 @@ int pk_profile_stop(double *schedule_ms, double *attend_ms, int *calls);
 
 /*
  * pk_attend_noalloc: the same forward pass for callers that cannot allocate device memory.
- * The paper has no counterpart to this entry point.
+ * hanzo-kernel 0.2.42 packed.rs has no counterpart to this entry point.
  *
  * pk_attend allocates a small workspace with cudaMalloc on first use per stream. Callers
  * that plan every byte of device memory themselves (a serving process with a fixed budget,
